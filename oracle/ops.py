@@ -1,0 +1,184 @@
+"""fp64 restatement of the decode-step hot path -- oracle, test infrastructure only.
+
+Each function is the plain definition of one step, with a library matmul as the
+only primitive; no blocking, fusion or reordering beyond the definition.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .mx import bf16_to_f64, f64_to_bf16, mx_dequantize, mx_quantize
+
+
+# --------------------------------------------------------------------------- GEMM
+def mx_gemm(aq, ascale, bq, bscale) -> np.ndarray:
+    """C = A' B'^T in fp64, A' [M,K] and B' [N,K] the dequantised MX operands.
+
+    [S2.1] "FP8 Quantization Strategy": the mxfp8 GEMM takes both operands as
+    1x32-block MX tensors (E4M3 + UE8M0) along the contraction dimension K.
+    """
+    return mx_dequantize(aq, ascale) @ mx_dequantize(bq, bscale).T
+
+
+def mx_gemm_sampled(aq, ascale, bq, bscale, rows, cols) -> np.ndarray:
+    """C[rows][:, cols] of ``mx_gemm``: one fp64 dot product per sampled entry."""
+    rows = np.asarray(rows)
+    cols = np.asarray(cols)
+    A = mx_dequantize(aq[rows], ascale[rows])
+    B = mx_dequantize(bq[cols], bscale[cols])
+    return A @ B.T
+
+
+# --------------------------------------------------------------------------- MLP
+def silu(g):
+    """silu(g) = g / (1 + e^-g) (fp64)."""
+    with np.errstate(over="ignore"):
+        return g / (1.0 + np.exp(-g))
+
+
+def swiglu_mlp(xq, xs, w13q, w13s, w2q, w2s, residual_bf16=None) -> dict:
+    """Qwen3-4B-shaped SwiGLU MLP over MX operands ([S2.1] "Kernel Benchmark
+    Results": quantise -> gate/up -> SwiGLU -> quantise -> down, with the SwiGLU
+    fused into the down projection's activation quantisation so that no bf16
+    intermediate exists).
+
+    W13 = [W_gate; W_up] stacked along N (rows 0..d_ff-1 gate, d_ff..2d_ff-1 up).
+    g, u = X' W_g'^T, X' W_u'^T; h = silu(g) * u; (hq, hs) = MX(h) along d_ff;
+    y = H' W_d'^T (+ residual), rounded once to bf16.
+    """
+    d_ff = w13q.shape[0] // 2
+    X = mx_dequantize(xq, xs)
+    W13 = mx_dequantize(w13q, w13s)
+    G = X @ W13[:d_ff].T
+    U = X @ W13[d_ff:].T
+    H = silu(G) * U
+    hq, hs = mx_quantize(H)
+    Y = mx_dequantize(hq, hs) @ mx_dequantize(w2q, w2s).T
+    if residual_bf16 is not None:
+        Y = Y + bf16_to_f64(residual_bf16)
+    return {"g": G, "u": U, "h": H, "hq": hq, "hs": hs, "y": Y, "y_bf16": f64_to_bf16(Y)}
+
+
+# --------------------------------------------------------------------------- RMSNorm
+def rmsnorm_bf16(x_bf16, gamma_bf16, eps) -> np.ndarray:
+    """RMSNorm of each row, rounded to bf16 (the input of the activation quantiser).
+
+    y = x * rsqrt(mean(x^2) + eps) * gamma. The pages give no precision for this
+    step; the reading used (both here and in the kernel, so that the bf16
+    rounding that decides the quantised codes is taken at the same precision):
+    mean(x^2) and rsqrt in fp64 (eps taken as the fp32 value passed by the
+    caller), the factor rounded to fp32, then x*r and (x*r)*gamma in fp32, then
+    bf16 round-to-nearest-even.
+    """
+    x = bf16_to_f64(x_bf16)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    r = (1.0 / np.sqrt(ms + np.float64(np.float32(eps)))).astype(np.float32)
+    y = (x.astype(np.float32) * r) * bf16_to_f64(gamma_bf16).astype(np.float32)
+    return f64_to_bf16(y.astype(np.float64))
+
+
+def rmsnorm_mx_quantize(x_bf16, gamma_bf16, eps):
+    return mx_quantize(bf16_to_f64(rmsnorm_bf16(x_bf16, gamma_bf16, eps)))
+
+
+# --------------------------------------------------------------------------- attention
+def gqa_decode_attention(q, k_prefix, v_prefix, scale) -> np.ndarray:
+    """GQA decode attention over each sequence's active prefix (fp64 brute force).
+
+    [FSKV] §5: the cache keeps its full capacity, and attention reads only the
+    filled prefix K[:, :, :kv_len], V[:, :, :kv_len]; KV heads are shared by
+    Hq/Hkv query heads (repeat_interleave(n_head // n_local_heads) in §5, i.e.
+    query head h reads KV head floor(h / (Hq/Hkv))). The decode query sits at
+    position kv_len-1, so no position inside the prefix is masked.
+
+    q: [bs, Hq, D] (fp64 values); k_prefix[b], v_prefix[b]: [Hkv, kv_len_b, D].
+    Returns o [bs, Hq, D] fp64 = softmax(scale * q K^T) V per (b, h).
+    """
+    bs, Hq, D = q.shape
+    out = np.zeros((bs, Hq, D))
+    for b in range(bs):
+        K = np.asarray(k_prefix[b], dtype=np.float64)
+        V = np.asarray(v_prefix[b], dtype=np.float64)
+        Hkv = K.shape[0]
+        grp = Hq // Hkv
+        for h in range(Hq):
+            g = h // grp
+            s = scale * (K[g] @ q[b, h])
+            p = np.exp(s - s.max())
+            out[b, h] = (p @ V[g]) / p.sum()
+    return out
+
+
+def gqa_attention_full_cache_masked(q, k_cache, v_cache, kv_len, scale) -> np.ndarray:
+    """The pre-fix formulation of [FSKV] §4: every query head attends over the
+    full capacity with KV heads expanded by repeat_interleave and positions
+    >= kv_len masked to -inf. Used only to check the invariant of [FSKV] §7
+    (active prefix == full cache + mask)."""
+    bs, Hq, D = q.shape
+    Hkv, cap = k_cache.shape[1], k_cache.shape[2]
+    K = np.repeat(np.asarray(k_cache, np.float64), Hq // Hkv, axis=1)
+    V = np.repeat(np.asarray(v_cache, np.float64), Hq // Hkv, axis=1)
+    s = scale * np.einsum("bhd,bhjd->bhj", q, K)
+    mask = np.arange(cap)[None, :] >= np.asarray(kv_len)[:, None]
+    s = np.where(mask[:, None, :], -np.inf, s)
+    p = np.exp(s - s.max(axis=-1, keepdims=True))
+    p = p / p.sum(axis=-1, keepdims=True)
+    return np.einsum("bhj,bhjd->bhd", p, V)
+
+
+# --------------------------------------------------------------------------- KV append
+def kv_append(k_cache, v_cache, k_new, v_new, kv_len):
+    """Write this step's K/V rows at position kv_len-1 of each sequence (in place
+    update of the preallocated cache, [FSKV] §5 "kv_cache.update"); kv_len is the
+    length after the append (prefill T, i-th decode T+i+1)."""
+    k_cache = k_cache.copy()
+    v_cache = v_cache.copy()
+    for b, n in enumerate(np.asarray(kv_len)):
+        k_cache[b, :, n - 1, :] = k_new[b]
+        v_cache[b, :, n - 1, :] = v_new[b]
+    return k_cache, v_cache
+
+
+# --------------------------------------------------------------------------- prev window
+def prev_tokens_shift(prev, next_tokens) -> np.ndarray:
+    """Slide the Dual-AR previous-tokens window by one frame ([S2.1] "DualAR:
+    S2-Specific Batching Constraints": prev int32 [bs, W, cw], next_tokens int32
+    [bs, cw]). Reading: frame 0 is the oldest and is dropped, frames move down by
+    one, and next_tokens becomes frame W-1."""
+    prev = np.asarray(prev)
+    nxt = np.asarray(next_tokens)
+    out = np.empty_like(prev)
+    out[:, :-1, :] = prev[:, 1:, :]
+    out[:, -1, :] = nxt
+    return out
+
+
+# --------------------------------------------------------------------------- layer step
+def decode_layer_step(x_bf16, gamma1, gamma2, wqkv, wo, w13, w2, k_prefix, v_prefix,
+                      kv_len, prev, next_tokens, Hq, Hkv, D, eps, scale) -> dict:
+    """One slow-AR decoder-layer step: RMSNorm -> MX quantise -> QKV projection ->
+    KV append -> GQA decode attention -> MX quantise -> O projection + residual ->
+    RMSNorm -> MX quantise -> SwiGLU MLP + residual; plus the prev-window shift.
+
+    wqkv/wo/w13/w2 are (q, scale) MX pairs. k_prefix[b]/v_prefix[b] hold the
+    kv_len[b]-1 rows already in the cache; the new row comes from the QKV
+    projection. Every bf16 tensor the kernels store is rounded to bf16 here too.
+    """
+    bs = x_bf16.shape[0]
+    xq, xs = rmsnorm_mx_quantize(x_bf16, gamma1, eps)
+    qkv = f64_to_bf16(mx_gemm(xq, xs, *wqkv))
+    qkv_f = bf16_to_f64(qkv)
+    q = qkv_f[:, : Hq * D].reshape(bs, Hq, D)
+    k_new = qkv_f[:, Hq * D:(Hq + Hkv) * D].reshape(bs, Hkv, D)
+    v_new = qkv_f[:, (Hq + Hkv) * D:].reshape(bs, Hkv, D)
+    kp = [np.concatenate([bf16_to_f64(k_prefix[b]), k_new[b][:, None, :]], axis=1) for b in range(bs)]
+    vp = [np.concatenate([bf16_to_f64(v_prefix[b]), v_new[b][:, None, :]], axis=1) for b in range(bs)]
+    for b in range(bs):
+        assert kp[b].shape[1] == kv_len[b]
+    o = f64_to_bf16(gqa_decode_attention(q, kp, vp, scale)).reshape(bs, Hq * D)
+    oq, os_ = mx_quantize(bf16_to_f64(o))
+    x1 = f64_to_bf16(bf16_to_f64(x_bf16) + mx_gemm(oq, os_, *wo))
+    hq_in, hs_in = rmsnorm_mx_quantize(x1, gamma2, eps)
+    mlp = swiglu_mlp(hq_in, hs_in, w13[0], w13[1], w2[0], w2[1], residual_bf16=x1)
+    return {"qkv": qkv, "o": o, "x1": x1, "y": mlp["y"], "y_bf16": mlp["y_bf16"],
+            "prev": prev_tokens_shift(prev, next_tokens)}
