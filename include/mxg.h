@@ -1,0 +1,166 @@
+/*
+ * libmxg -- C ABI of the GB300 (sm_103a) kernels for one slow-AR decoder-layer step of
+ * Dual-AR TTS decoding: MXFP8 activation quantisation, the MXFP8 SwiGLU MLP, GQA decode
+ * attention over the active prefix of a preallocated KV cache, and the prev-tokens window
+ * shift.
+ *
+ * Pages that define the operations (cited by title and section):
+ *   [S2.1] "How We Made Our Text-to-Speech API Free: The Inference Engineering Behind
+ *          S2.1 Pro" -- sections "FP8 Quantization Strategy", "Kernel Benchmark Results",
+ *          "DualAR: S2-Specific Batching Constraints", "What's Open Source".
+ *   [FSKV] "Fish Speech KV Cache 推理优化记录" -- §4 (bottleneck: the full cache is passed
+ *          although a causal mask exists), §5 (keep the capacity, read only the active
+ *          prefix), §7 (review: defining correctness).
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer is a DEVICE pointer unless stated otherwise; the caller owns every
+ *     buffer. The library never allocates, frees or synchronises, so each call only
+ *     enqueues kernels on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *   - bf16 tensors are IEEE bfloat16 bit patterns (uint16). MXFP8 tensors are two arrays:
+ *     `q` = E4M3 bytes [rows, K] row-major and `s` = UE8M0 scale bytes [rows, K/32]
+ *     row-major, one scale per 32 consecutive elements along K (OCP MX, 1x32 blocks).
+ *     Value of element (r, k) = E4M3(q[r,k]) * 2^(s[r, k/32] - 127).
+ *   - Sizes are int64 element counts; strides ("ld") are in elements.
+ *   - Host-detectable errors (bad sizes, misalignment, too small a workspace) return a
+ *     status and enqueue nothing. Errors only the device can see (a kv_len out of range,
+ *     a bounded in-kernel wait that ran out) are written to an optional device int32
+ *     `err_flag` (first error code wins; the caller zeroes it) -- no kernel ever traps.
+ *   - Launch failures return MXG_ELAUNCH.
+ *   - Alignment: every pointer 16-byte aligned; ld values multiples of 8 (bf16) / 16 (bytes).
+ */
+#ifndef MXG_H
+#define MXG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MXG_OK = 0,
+  MXG_EINVAL = 1,     /* null pointer or invalid scalar argument */
+  MXG_ESHAPE = 2,     /* sizes outside what the kernel supports */
+  MXG_EALIGN = 3,     /* pointer or stride misaligned */
+  MXG_EWORKSPACE = 4, /* workspace too small */
+  MXG_ELAUNCH = 5,    /* a CUDA launch failed */
+  MXG_ETIMEOUT = 6,   /* device: a bounded wait ran out */
+  MXG_EDEVICE = 7,    /* device: an input value out of range (e.g. kv_len) */
+  MXG_ENOTSUP = 8     /* no kernel for this device / configuration */
+} mxg_status;
+
+/* Static string for a status code (never NULL). */
+const char* mxg_status_str(int status);
+/* Library ABI version (major*10000 + minor*100 + patch). */
+int mxg_version(void);
+
+/*
+ * mxfp8_quantize -- fused activation quantisation + UE8M0 scale pack in one launch
+ * ([S2.1] "Kernel Benchmark Results": the fused kernel that quantises activations and
+ * packs the UE8M0 scales; "FP8 Quantization Strategy": mxfp8 = 1x32 blocks, OCP UE8M0).
+ *   x      bf16 [M, K], row stride ld_x (>= K)
+ *   q      E4M3 [M, K] (row-major, dense), s UE8M0 [M, K/32]
+ * Per 32-block: s = clamp(floor(log2 max|x|) - 8, -127, 127), q = E4M3_rne_satfinite(x/2^s);
+ * an all-zero block gets s = -127. Requires K % 32 == 0.  Bit-exact with the oracle.
+ */
+mxg_status mxfp8_quantize(const void* x, int64_t M, int64_t K, int64_t ld_x, uint8_t* q, uint8_t* s,
+                          void* stream);
+
+/*
+ * rmsnorm_mxfp8_quantize -- RMSNorm fused into the activation quantiser (decoder-layer
+ * step: RMSNorm -> attention -> RMSNorm -> MLP).
+ *   y = bf16( (x * r) * gamma ), r = fp32( 1 / sqrt( mean_fp64(x^2) + eps ) ), products
+ *   in fp32, then the MX rule above on y.  x bf16 [M, K] (row stride ld_x), gamma bf16 [K].
+ * Requires K % 32 == 0 and K <= 16384.
+ */
+mxg_status rmsnorm_mxfp8_quantize(const void* x, const void* gamma, float eps, int64_t M, int64_t K, int64_t ld_x,
+                                  uint8_t* q, uint8_t* s, void* stream);
+
+/*
+ * mxfp8_gemm -- C = A' B'^T (+ residual), both operands MXFP8 along K, fp32 accumulation,
+ * bf16 output ([S2.1] "FP8 Quantization Strategy" / "Kernel Benchmark Results": the MXFP8
+ * GEMM, square 1024^3..16384^3 and decode shapes).
+ *   aq [M, K], as [M, K/32]; bq [N, K], bs [N, K/32] (weights: N = output features)
+ *   residual bf16 [M, N] or NULL; c bf16 [M, N]. K % 32 == 0, N % 8 == 0.
+ *   workspace: device scratch of mxfp8_gemm_workspace(M, N, K) bytes (may be NULL if 0).
+ */
+size_t mxfp8_gemm_workspace(int64_t M, int64_t N, int64_t K);
+mxg_status mxfp8_gemm(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs, int64_t M,
+                      int64_t N, int64_t K, const void* residual, void* c, void* workspace, size_t ws_bytes,
+                      void* stream);
+
+/*
+ * mlp_gate_up_swiglu_mxfp8 -- the gate/up GEMM with the SwiGLU + re-quantisation epilogue
+ * ([S2.1] "Kernel Benchmark Results": SwiGLU fused into the down-GEMM's activation
+ * quantisation, so no bf16 intermediate is written): g = X' Wg'^T, u = X' Wu'^T (fp32),
+ * h = silu(g) * u (fp32), (hq, hs) = MX(h) along d_ff.
+ *   xq [M, d_model], xs [M, d_model/32]
+ *   w13q [2*d_ff, d_model], w13s [2*d_ff, d_model/32]: rows 0..d_ff-1 = gate, d_ff.. = up
+ *   hq [M, d_ff], hs [M, d_ff/32] (outputs).  d_model % 32 == 0, d_ff % 128 == 0.
+ */
+mxg_status mlp_gate_up_swiglu_mxfp8(const uint8_t* xq, const uint8_t* xs, int64_t M, int64_t d_model, int64_t d_ff,
+                                    const uint8_t* w13q, const uint8_t* w13s, uint8_t* hq, uint8_t* hs,
+                                    void* stream);
+
+/*
+ * mlp_swiglu_mxfp8 -- the whole Qwen3-4B-shaped SwiGLU MLP ([S2.1] "Kernel Benchmark
+ * Results": quantise -> gate/up -> SwiGLU -> quantise -> down): the call above into the
+ * workspace, then y = H' W2'^T (+ residual) in bf16.
+ *   w2q [d_model, d_ff], w2s [d_model, d_ff/32]; residual bf16 [M, d_model] or NULL;
+ *   y bf16 [M, d_model].
+ *   workspace: mlp_swiglu_mxfp8_workspace(M, d_model, d_ff) bytes; it holds hq at offset 0
+ *   (M*d_ff bytes) and hs right after (M*d_ff/32 bytes), then the down GEMM's scratch.
+ */
+size_t mlp_swiglu_mxfp8_workspace(int64_t M, int64_t d_model, int64_t d_ff);
+mxg_status mlp_swiglu_mxfp8(const uint8_t* xq, const uint8_t* xs, int64_t M, int64_t d_model, int64_t d_ff,
+                            const uint8_t* w13q, const uint8_t* w13s, const uint8_t* w2q, const uint8_t* w2s,
+                            const void* residual, void* y, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * gqa_decode_attn -- decode attention with grouped KV heads over the active prefix of a
+ * preallocated cache ([FSKV] §5: the cache keeps its capacity; attention reads only
+ * K[:, :, :kv_len] / V[:, :, :kv_len]; query head h reads KV head h / (Hq/Hkv) with no
+ * head expansion -- [S2.1] "What's Open Source": native GQA by stride-0 K/V broadcast).
+ *   q        bf16 [bs, Hq, D] with row stride ld_q elements between sequences (>= Hq*D)
+ *   k_cache, v_cache  bf16 [bs, Hkv, cap, D] (contiguous)
+ *   kv_len   int32 [bs] on the device: filled prefix length (the decode query is the last
+ *            position, so nothing inside the prefix is masked). Positions >= kv_len are
+ *            never used and may hold any finite values.
+ *   out      bf16 [bs, Hq, D]
+ *   max_kv_len  host-side bound on every kv_len (sets the grid; keeps the call capturable)
+ *   scale    softmax scale (e.g. 1/sqrt(D))
+ *   err_flag device int32 or NULL: MXG_EDEVICE if some kv_len is outside [1, min(cap,
+ *            max_kv_len)] (that sequence's output is zeroed), MXG_ETIMEOUT on a wait limit.
+ *   workspace gqa_decode_attn_workspace(bs, Hq, Hkv, D, max_kv_len) bytes (split-KV partials).
+ * Supported: D in {64, 128}, Hq % Hkv == 0, Hq/Hkv <= 8, cap < 2^31.
+ */
+size_t gqa_decode_attn_workspace(int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t max_kv_len);
+mxg_status gqa_decode_attn(const void* q, int64_t ld_q, const void* k_cache, const void* v_cache,
+                           const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t cap,
+                           int64_t max_kv_len, float scale, void* out, int32_t* err_flag, void* workspace,
+                           size_t ws_bytes, void* stream);
+
+/*
+ * kv_append -- in-place cache update of this step's K/V rows at position kv_len[b]-1
+ * ([FSKV] §5, kv_cache.update; kv_len counts the new row: prefill T, i-th decode T+i+1).
+ *   k_new, v_new bf16 [bs, Hkv, D] with row stride ld_new elements between sequences.
+ *   err_flag as above (MXG_EDEVICE if kv_len[b] is outside [1, cap]; that row is skipped).
+ */
+mxg_status kv_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new, int64_t ld_new,
+                     const int32_t* kv_len, int64_t bs, int64_t Hkv, int64_t D, int64_t cap, int32_t* err_flag,
+                     void* stream);
+
+/*
+ * prev_tokens_shift -- in-place slide of the Dual-AR previous-tokens window ([S2.1]
+ * "DualAR: S2-Specific Batching Constraints": prev int32 [bs, W, cw], next_tokens int32
+ * [bs, cw], strict shape/dtype contract). prev[b, w] <- prev[b, w+1] for w < W-1 and
+ * prev[b, W-1] <- next[b]; frame 0 is the oldest. Bit-exact. W*cw <= 12288.
+ */
+mxg_status prev_tokens_shift(int32_t* prev, const int32_t* next_tokens, int64_t bs, int64_t W, int64_t cw,
+                             void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MXG_H */

@@ -1,0 +1,264 @@
+"""Python binding of libmxg (ctypes): the same entry points as ``include/mxg.h``.
+
+Argument marshalling only: every step runs in the library's CUDA kernels. PyTorch
+provides device memory and the current CUDA stream. Inputs are checked strictly
+(dtype, rank, shape, contiguity, device); nothing is reshaped, unsqueezed or
+promoted on the caller's behalf (the prev-window contract of [S2.1] "DualAR:
+S2-Specific Batching Constraints"). Outputs may be passed in (stable addresses
+for CUDA-graph capture) or are allocated with ``torch.empty``.
+
+If the shared library is missing or cannot be loaded, every call raises: there
+is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+from . import build as _build
+
+_LIB = None
+
+c_i64, c_f32, c_vp, c_sz = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+
+_SIGS = {
+    "mxg_status_str": (ctypes.c_char_p, [ctypes.c_int]),
+    "mxg_version": (ctypes.c_int, []),
+    "mxfp8_quantize": (ctypes.c_int, [c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_vp]),
+    "rmsnorm_mxfp8_quantize": (ctypes.c_int, [c_vp, c_vp, c_f32, c_i64, c_i64, c_i64, c_vp, c_vp, c_vp]),
+    "mxfp8_gemm_workspace": (c_sz, [c_i64, c_i64, c_i64]),
+    "mxfp8_gemm": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_vp, c_sz, c_vp]),
+    "mlp_gate_up_swiglu_mxfp8": (ctypes.c_int, [c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_vp, c_vp, c_vp]),
+    "mlp_swiglu_mxfp8_workspace": (c_sz, [c_i64, c_i64, c_i64]),
+    "mlp_swiglu_mxfp8": (ctypes.c_int, [c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                        c_vp, c_sz, c_vp]),
+    "gqa_decode_attn_workspace": (c_sz, [c_i64, c_i64, c_i64, c_i64, c_i64]),
+    "gqa_decode_attn": (ctypes.c_int, [c_vp, c_i64, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_i64, c_i64, c_i64,
+                                       c_f32, c_vp, c_vp, c_vp, c_sz, c_vp]),
+    "kv_append": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_i64, c_vp, c_i64, c_i64, c_i64, c_i64, c_vp, c_vp]),
+    "prev_tokens_shift": (ctypes.c_int, [c_vp, c_vp, c_i64, c_i64, c_i64, c_vp]),
+}
+
+
+class MxgError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn}: {lib().mxg_status_str(status).decode()} (status {status})")
+
+
+def header_functions() -> list:
+    """Entry points declared in include/mxg.h."""
+    src = open(os.path.join(_build.INCLUDE, "mxg.h")).read()
+    return re.findall(r"^\s*(?:const char\*|int|size_t|mxg_status)\s+(\w+)\(", src, re.M)
+
+
+def lib(path: str | None = None):
+    """Load libmxg.so (once). Raises if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        p = path or _build.LIB
+        if not os.path.exists(p):
+            raise RuntimeError(f"libmxg.so not built at {p}: run __graft_entry__.build() first")
+        L = ctypes.CDLL(p)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def _call(name, *args):
+    st = getattr(lib(), name)(*args)
+    if st != 0:
+        raise MxgError(name, st)
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(t, name, dtype, shape=None, ndim=None, contiguous=True):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype} (no implicit promotion)")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name}: rank {t.dim()}, expected {ndim} (no implicit reshaping)")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    return t
+
+
+def _rows_view(t, name, dtype):
+    """2-D tensor whose rows may be strided (last dim contiguous): returns the row stride."""
+    _check(t, name, dtype, ndim=2, contiguous=False)
+    if t.stride(1) != 1:
+        raise ValueError(f"{name}: the last dimension must be contiguous")
+    return t.stride(0)
+
+
+def _out(t, name, dtype, shape, device):
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    return _check(t, name, dtype, shape)
+
+
+# ------------------------------------------------------------------ quantisation
+def mxfp8_quantize(x, q=None, s=None):
+    """bf16 [M, K] -> (E4M3 bytes [M, K], UE8M0 scales [M, K/32])."""
+    ld = _rows_view(x, "x", torch.bfloat16)
+    M, K = x.shape
+    q = _out(q, "q", torch.uint8, (M, K), x.device)
+    s = _out(s, "s", torch.uint8, (M, K // 32), x.device)
+    _call("mxfp8_quantize", _ptr(x), M, K, ld, _ptr(q), _ptr(s), _stream())
+    return q, s
+
+
+def rmsnorm_mxfp8_quantize(x, gamma, eps, q=None, s=None):
+    ld = _rows_view(x, "x", torch.bfloat16)
+    M, K = x.shape
+    _check(gamma, "gamma", torch.bfloat16, (K,))
+    q = _out(q, "q", torch.uint8, (M, K), x.device)
+    s = _out(s, "s", torch.uint8, (M, K // 32), x.device)
+    _call("rmsnorm_mxfp8_quantize", _ptr(x), _ptr(gamma), float(eps), M, K, ld, _ptr(q), _ptr(s), _stream())
+    return q, s
+
+
+# ------------------------------------------------------------------ GEMM / MLP
+def mxfp8_gemm(aq, as_, bq, bs, residual=None, c=None, workspace=None):
+    """C[M, N] = A' B'^T (+ residual) in bf16; A = (aq [M,K], as_ [M,K/32]), B = (bq [N,K], bs [N,K/32])."""
+    _check(aq, "aq", torch.uint8, ndim=2)
+    M, K = aq.shape
+    _check(as_, "as", torch.uint8, (M, K // 32))
+    _check(bq, "bq", torch.uint8, ndim=2)
+    N = bq.shape[0]
+    _check(bq, "bq", torch.uint8, (N, K))
+    _check(bs, "bs", torch.uint8, (N, K // 32))
+    if residual is not None:
+        _check(residual, "residual", torch.bfloat16, (M, N))
+    c = _out(c, "c", torch.bfloat16, (M, N), aq.device)
+    need = lib().mxfp8_gemm_workspace(M, N, K)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=aq.device)
+    ws_bytes = 0 if workspace is None else workspace.numel()
+    _call("mxfp8_gemm", _ptr(aq), _ptr(as_), _ptr(bq), _ptr(bs), M, N, K, _ptr(residual), _ptr(c),
+          _ptr(workspace), ws_bytes, _stream())
+    return c
+
+
+def mlp_gate_up_swiglu_mxfp8(xq, xs, w13q, w13s, hq=None, hs=None):
+    _check(xq, "xq", torch.uint8, ndim=2)
+    M, d_model = xq.shape
+    _check(xs, "xs", torch.uint8, (M, d_model // 32))
+    _check(w13q, "w13q", torch.uint8, ndim=2)
+    d_ff = w13q.shape[0] // 2
+    _check(w13q, "w13q", torch.uint8, (2 * d_ff, d_model))
+    _check(w13s, "w13s", torch.uint8, (2 * d_ff, d_model // 32))
+    hq = _out(hq, "hq", torch.uint8, (M, d_ff), xq.device)
+    hs = _out(hs, "hs", torch.uint8, (M, d_ff // 32), xq.device)
+    _call("mlp_gate_up_swiglu_mxfp8", _ptr(xq), _ptr(xs), M, d_model, d_ff, _ptr(w13q), _ptr(w13s), _ptr(hq),
+          _ptr(hs), _stream())
+    return hq, hs
+
+
+def mlp_swiglu_mxfp8_workspace(M, d_model, d_ff) -> int:
+    return int(lib().mlp_swiglu_mxfp8_workspace(M, d_model, d_ff))
+
+
+def mlp_swiglu_mxfp8(xq, xs, w13q, w13s, w2q, w2s, residual=None, y=None, workspace=None):
+    _check(xq, "xq", torch.uint8, ndim=2)
+    M, d_model = xq.shape
+    _check(xs, "xs", torch.uint8, (M, d_model // 32))
+    d_ff = w13q.shape[0] // 2
+    _check(w13q, "w13q", torch.uint8, (2 * d_ff, d_model))
+    _check(w13s, "w13s", torch.uint8, (2 * d_ff, d_model // 32))
+    _check(w2q, "w2q", torch.uint8, (d_model, d_ff))
+    _check(w2s, "w2s", torch.uint8, (d_model, d_ff // 32))
+    if residual is not None:
+        _check(residual, "residual", torch.bfloat16, (M, d_model))
+    y = _out(y, "y", torch.bfloat16, (M, d_model), xq.device)
+    need = mlp_swiglu_mxfp8_workspace(M, d_model, d_ff)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=xq.device)
+    _check(workspace, "workspace", torch.uint8, ndim=1)
+    _call("mlp_swiglu_mxfp8", _ptr(xq), _ptr(xs), M, d_model, d_ff, _ptr(w13q), _ptr(w13s), _ptr(w2q), _ptr(w2s),
+          _ptr(residual), _ptr(y), _ptr(workspace), workspace.numel(), _stream())
+    return y
+
+
+# ------------------------------------------------------------------ attention / cache / window
+def gqa_decode_attn_workspace(bs, Hq, Hkv, D, max_kv_len) -> int:
+    return int(lib().gqa_decode_attn_workspace(bs, Hq, Hkv, D, max_kv_len))
+
+
+def gqa_decode_attn(q, k_cache, v_cache, kv_len, max_kv_len, scale, out=None, err=None, workspace=None):
+    """q bf16 [bs, Hq, D] (or a row-strided [bs, Hq*D] view), caches bf16 [bs, Hkv, cap, D],
+    kv_len int32 [bs] on the device -> out bf16 [bs, Hq, D]."""
+    _check(k_cache, "k_cache", torch.bfloat16, ndim=4)
+    bs, Hkv, cap, D = k_cache.shape
+    _check(v_cache, "v_cache", torch.bfloat16, (bs, Hkv, cap, D))
+    _check(kv_len, "kv_len", torch.int32, (bs,))
+    if q.dim() == 3:
+        _check(q, "q", torch.bfloat16, ndim=3)
+        Hq = q.shape[1]
+        _check(q, "q", torch.bfloat16, (bs, Hq, D))
+        ld_q = Hq * D
+    else:
+        ld_q = _rows_view(q, "q", torch.bfloat16)
+        if q.shape[0] != bs or q.shape[1] % D:
+            raise ValueError("q: expected [bs, Hq*D]")
+        Hq = q.shape[1] // D
+    out = _out(out, "out", torch.bfloat16, (bs, Hq, D), k_cache.device)
+    if err is not None:
+        _check(err, "err", torch.int32, (1,))
+    need = gqa_decode_attn_workspace(bs, Hq, Hkv, D, max_kv_len)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=k_cache.device)
+    ws_bytes = 0 if workspace is None else workspace.numel()
+    _call("gqa_decode_attn", _ptr(q), ld_q, _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), bs, Hq, Hkv, D, cap,
+          int(max_kv_len), float(scale), _ptr(out), _ptr(err), _ptr(workspace), ws_bytes, _stream())
+    return out
+
+
+def kv_append(k_cache, v_cache, k_new, v_new, kv_len, err=None):
+    """k_new/v_new: bf16 [bs, Hkv, D] or row-strided [bs, Hkv*D] views (e.g. slices of a fused QKV)."""
+    _check(k_cache, "k_cache", torch.bfloat16, ndim=4)
+    bs, Hkv, cap, D = k_cache.shape
+    _check(v_cache, "v_cache", torch.bfloat16, (bs, Hkv, cap, D))
+    _check(kv_len, "kv_len", torch.int32, (bs,))
+    lds = []
+    for t, name in ((k_new, "k_new"), (v_new, "v_new")):
+        if t.dim() == 3:
+            _check(t, name, torch.bfloat16, (bs, Hkv, D))
+            lds.append(Hkv * D)
+        else:
+            lds.append(_rows_view(t, name, torch.bfloat16))
+            if tuple(t.shape) != (bs, Hkv * D):
+                raise ValueError(f"{name}: expected [bs, Hkv*D]")
+    if lds[0] != lds[1]:
+        raise ValueError("k_new and v_new must share a row stride")
+    if err is not None:
+        _check(err, "err", torch.int32, (1,))
+    _call("kv_append", _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), lds[0], _ptr(kv_len), bs, Hkv, D,
+          cap, _ptr(err), _stream())
+
+
+def prev_tokens_shift(prev, next_tokens):
+    """In place: prev int32 [bs, W, cw], next_tokens int32 [bs, cw] (exact shapes, no promotion)."""
+    _check(prev, "prev", torch.int32, ndim=3)
+    bs, W, cw = prev.shape
+    _check(next_tokens, "next_tokens", torch.int32, (bs, cw))
+    _call("prev_tokens_shift", _ptr(prev), _ptr(next_tokens), bs, W, cw, _stream())
+    return prev

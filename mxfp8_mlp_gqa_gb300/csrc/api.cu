@@ -1,0 +1,193 @@
+// C ABI of libmxg: argument checks, workspace sizing and kernel dispatch. Nothing here
+// allocates, frees or synchronises; each entry point only enqueues work on `stream`.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mxg {
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline mxg_status launched(cudaError_t e) { return e == cudaSuccess ? MXG_OK : MXG_ELAUNCH; }
+
+}  // namespace
+
+bool make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+  auto fn = encode_tiled_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace mxg
+
+using namespace mxg;
+
+extern "C" {
+
+const char* mxg_status_str(int s) {
+  switch (s) {
+    case MXG_OK: return "ok";
+    case MXG_EINVAL: return "invalid argument";
+    case MXG_ESHAPE: return "unsupported shape";
+    case MXG_EALIGN: return "misaligned pointer or stride";
+    case MXG_EWORKSPACE: return "workspace too small";
+    case MXG_ELAUNCH: return "kernel launch failed";
+    case MXG_ETIMEOUT: return "device wait timed out";
+    case MXG_EDEVICE: return "device-side input out of range";
+    case MXG_ENOTSUP: return "not supported on this device/configuration";
+    default: return "unknown status";
+  }
+}
+
+int mxg_version(void) { return 100; }
+
+mxg_status mxfp8_quantize(const void* x, int64_t M, int64_t K, int64_t ld_x, uint8_t* q, uint8_t* s, void* stream) {
+  if (!x || !q || !s) return MXG_EINVAL;
+  if (M < 0 || K <= 0 || K % 32 || ld_x < K) return MXG_ESHAPE;
+  if (!aligned16(x) || !aligned16(q) || ld_x % 8) return MXG_EALIGN;
+  if (M == 0) return MXG_OK;
+  return launched(launch_mxfp8_quantize(static_cast<const uint16_t*>(x), M, K, ld_x, q, s, (cudaStream_t)stream));
+}
+
+mxg_status rmsnorm_mxfp8_quantize(const void* x, const void* gamma, float eps, int64_t M, int64_t K, int64_t ld_x,
+                                  uint8_t* q, uint8_t* s, void* stream) {
+  if (!x || !gamma || !q || !s) return MXG_EINVAL;
+  if (!(eps >= 0.f)) return MXG_EINVAL;
+  if (M < 0 || K <= 0 || K % 32 || K > 16384 || ld_x < K || M > 0x7fffffff) return MXG_ESHAPE;
+  if (!aligned16(x) || !aligned16(gamma) || !aligned16(q) || ld_x % 8) return MXG_EALIGN;
+  if (M == 0) return MXG_OK;
+  return launched(launch_rmsnorm_mxfp8_quantize(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(gamma),
+                                                eps, M, K, ld_x, q, s, (cudaStream_t)stream));
+}
+
+size_t mxfp8_gemm_workspace(int64_t M, int64_t N, int64_t K) {
+  (void)M; (void)N; (void)K;
+  return 0;
+}
+
+mxg_status mxfp8_gemm(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs, int64_t M,
+                      int64_t N, int64_t K, const void* residual, void* c, void* workspace, size_t ws_bytes,
+                      void* stream) {
+  (void)workspace;
+  if (!aq || !as || !bq || !bs || !c) return MXG_EINVAL;
+  if (M < 0 || N <= 0 || K <= 0 || K % 32 || N % 8 || M > 0x7fffffff || N > 0x7fffffff || K > 0x7fffffff)
+    return MXG_ESHAPE;
+  if (!aligned16(aq) || !aligned16(bq) || !aligned16(c) || (residual && !aligned16(residual))) return MXG_EALIGN;
+  if (ws_bytes < mxfp8_gemm_workspace(M, N, K)) return MXG_EWORKSPACE;
+  if (M == 0) return MXG_OK;
+  return launched(launch_mx_gemm_simt(aq, as, bq, bs, M, N, K, static_cast<const uint16_t*>(residual),
+                                      static_cast<uint16_t*>(c), (cudaStream_t)stream));
+}
+
+mxg_status mlp_gate_up_swiglu_mxfp8(const uint8_t* xq, const uint8_t* xs, int64_t M, int64_t d_model, int64_t d_ff,
+                                    const uint8_t* w13q, const uint8_t* w13s, uint8_t* hq, uint8_t* hs,
+                                    void* stream) {
+  if (!xq || !xs || !w13q || !w13s || !hq || !hs) return MXG_EINVAL;
+  if (M < 0 || d_model <= 0 || d_ff <= 0 || d_model % 32 || d_ff % 128 || M > 0x7fffffff) return MXG_ESHAPE;
+  if (!aligned16(xq) || !aligned16(w13q) || !aligned16(hq)) return MXG_EALIGN;
+  if (M == 0) return MXG_OK;
+  return launched(launch_gate_up_swiglu_simt(xq, xs, M, d_model, d_ff, w13q, w13s, hq, hs, (cudaStream_t)stream));
+}
+
+size_t mlp_swiglu_mxfp8_workspace(int64_t M, int64_t d_model, int64_t d_ff) {
+  const size_t h = (size_t)M * (size_t)d_ff;
+  size_t off = (h + h / 32 + 255) / 256 * 256;
+  return off + mxfp8_gemm_workspace(M, d_model, d_ff);
+}
+
+mxg_status mlp_swiglu_mxfp8(const uint8_t* xq, const uint8_t* xs, int64_t M, int64_t d_model, int64_t d_ff,
+                            const uint8_t* w13q, const uint8_t* w13s, const uint8_t* w2q, const uint8_t* w2s,
+                            const void* residual, void* y, void* workspace, size_t ws_bytes, void* stream) {
+  if (!xq || !xs || !w13q || !w13s || !w2q || !w2s || !y) return MXG_EINVAL;
+  if (M < 0 || d_model <= 0 || d_ff <= 0 || d_model % 32 || d_ff % 128 || M > 0x7fffffff) return MXG_ESHAPE;
+  if (M == 0) return MXG_OK;
+  if (!workspace || ws_bytes < mlp_swiglu_mxfp8_workspace(M, d_model, d_ff)) return MXG_EWORKSPACE;
+  if (!aligned16(workspace)) return MXG_EALIGN;
+  uint8_t* hq = static_cast<uint8_t*>(workspace);
+  uint8_t* hs = hq + M * d_ff;
+  const size_t off = ((size_t)M * d_ff + (size_t)M * d_ff / 32 + 255) / 256 * 256;
+  mxg_status st = mlp_gate_up_swiglu_mxfp8(xq, xs, M, d_model, d_ff, w13q, w13s, hq, hs, stream);
+  if (st != MXG_OK) return st;
+  return mxfp8_gemm(hq, hs, w2q, w2s, M, d_model, d_ff, residual, y, static_cast<uint8_t*>(workspace) + off,
+                    ws_bytes - off, stream);
+}
+
+size_t gqa_decode_attn_workspace(int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t max_kv_len) {
+  if (bs <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || max_kv_len <= 0) return 0;
+  return attn_workspace_bytes(bs, Hq, Hkv, D, max_kv_len);
+}
+
+mxg_status gqa_decode_attn(const void* q, int64_t ld_q, const void* k_cache, const void* v_cache,
+                           const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t cap,
+                           int64_t max_kv_len, float scale, void* out, int32_t* err_flag, void* workspace,
+                           size_t ws_bytes, void* stream) {
+  if (!q || !k_cache || !v_cache || !kv_len || !out) return MXG_EINVAL;
+  if (!(scale > 0.f) || !(scale < 1e30f)) return MXG_EINVAL;
+  if (bs < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || Hq / Hkv > 8 || (D != 64 && D != 128) || cap <= 0 ||
+      max_kv_len <= 0 || ld_q < Hq * D)
+    return MXG_ESHAPE;
+  if (bs * Hkv * cap >= ((int64_t)1 << 31) || bs * Hkv > 65535 || max_kv_len > ((int64_t)1 << 30)) return MXG_ESHAPE;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || ld_q % 8) return MXG_EALIGN;
+  if (bs == 0) return MXG_OK;
+  const size_t need = attn_workspace_bytes(bs, Hq, Hkv, D, max_kv_len);
+  if (need && (!workspace || ws_bytes < need)) return MXG_EWORKSPACE;
+  if (need && !aligned16(workspace)) return MXG_EALIGN;
+  CUtensorMap tk, tv;
+  const uint64_t rows = (uint64_t)(bs * Hkv * cap);
+  if (!make_tensor_map_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_cache, (uint64_t)D, rows, (uint64_t)D * 2, 64, 64,
+                          CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tensor_map_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v_cache, (uint64_t)D, rows, (uint64_t)D * 2, 64, 64,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+    return MXG_ENOTSUP;
+  return launched(launch_gqa_decode_attn(tk, tv, static_cast<const uint16_t*>(q), ld_q, kv_len, bs, Hq, Hkv, D, cap,
+                                         max_kv_len, scale, static_cast<uint16_t*>(out), err_flag, workspace,
+                                         (cudaStream_t)stream));
+}
+
+mxg_status kv_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new, int64_t ld_new,
+                     const int32_t* kv_len, int64_t bs, int64_t Hkv, int64_t D, int64_t cap, int32_t* err_flag,
+                     void* stream) {
+  if (!k_cache || !v_cache || !k_new || !v_new || !kv_len) return MXG_EINVAL;
+  if (bs < 0 || Hkv <= 0 || D <= 0 || D % 8 || D > 256 || cap <= 0 || ld_new < Hkv * D || bs * Hkv > (1 << 26))
+    return MXG_ESHAPE;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new) || ld_new % 8)
+    return MXG_EALIGN;
+  if (bs == 0) return MXG_OK;
+  return launched(launch_kv_append(static_cast<uint16_t*>(k_cache), static_cast<uint16_t*>(v_cache),
+                                   static_cast<const uint16_t*>(k_new), static_cast<const uint16_t*>(v_new), ld_new,
+                                   kv_len, bs, Hkv, D, cap, err_flag, (cudaStream_t)stream));
+}
+
+mxg_status prev_tokens_shift(int32_t* prev, const int32_t* next_tokens, int64_t bs, int64_t W, int64_t cw,
+                             void* stream) {
+  if (!prev || !next_tokens) return MXG_EINVAL;
+  if (bs < 0 || W <= 0 || cw <= 0 || W * cw > 12288 || bs > 0x7fffffff) return MXG_ESHAPE;
+  if (bs == 0) return MXG_OK;
+  return launched(launch_prev_tokens_shift(prev, next_tokens, bs, W, cw, (cudaStream_t)stream));
+}
+
+}  // extern "C"

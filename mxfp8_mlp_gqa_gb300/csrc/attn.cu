@@ -1,0 +1,380 @@
+// GQA decode attention over the active prefix of a preallocated KV cache.
+//
+// [FSKV] §5: the cache keeps its full capacity and attention reads only the filled prefix
+// K[:, :, :kv_len], V[:, :, :kv_len]; §4: expanding the KV heads (repeat_interleave) before
+// attention multiplies the bytes touched. [S2.1] "What's Open Source": decode with native
+// GQA (a stride-0 broadcast of K/V over the query heads of a group).
+//
+// Design (HBM-bound: 4 flop per byte of K/V at group 4):
+//  * split-KV ("flash-decoding"): CTA = (kv split, sequence b, kv head g). Each CTA streams
+//    its slice of K and V exactly once and serves all Hq/Hkv query heads of the group, so
+//    K/V bytes are read once per KV head, never per query head.
+//  * one producer warp drives TMA (2-D tiled, 128-byte swizzle) into a 3-4 stage ring of
+//    64-token K and V tiles, with mbarrier full/empty handshakes (bounded waits);
+//  * four consumer warps, 16 tokens each per tile, compute S^T = K Q^T and O^T += V^T P^T
+//    with m16n8k16 bf16 tensor-core tiles (tokens x heads, heads padded to 8), fp32
+//    online softmax in base 2, P rounded to bf16 and l summed from the rounded P;
+//  * the CTA merges its 4 warps and writes (O/l, log2-sum-exp) per head; a small combine
+//    kernel merges the splits of each (b, h). With a single split the CTA writes bf16 out.
+// Grid size is fixed by a host bound on kv_len, so the call is graph-capturable; CTAs whose
+// split starts past kv_len exit at once.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mxg {
+
+namespace {
+
+constexpr int kTileTok = 64;     // tokens per pipeline stage
+constexpr int kConsumers = 4;    // consumer warps (16 tokens each per tile)
+constexpr int kThreads = (kConsumers + 1) * 32;
+
+template <int D>
+struct AttnShape {
+  static constexpr int kHalves = D / 64;                // 128-byte TMA boxes per row
+  static constexpr int kTileBytes = kTileTok * D * 2;   // one K (or V) tile
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kStages = D == 128 ? 3 : 4;
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kMergeBytes = kConsumers * 8 * D * 4 + kConsumers * 8 * 2 * 4;
+  static constexpr int kBodyBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
+  static constexpr int kPBytes = kConsumers * 8 * 16 * 2;  // per-warp P^T staging (bf16 [8][16])
+  static constexpr int kSmemBytes = 1024 + kBodyBytes + kPBytes + 2 * kStages * 8;
+};
+
+// Byte address (shared space) of element (row, col) of a [64, D] bf16 tile stored as D/64
+// column boxes of 64 rows x 128 bytes with the 128-byte swizzle (16-byte chunk ^= row % 8).
+__device__ __forceinline__ uint32_t tile_addr(uint32_t base, int row, int col) {
+  const int half = col >> 6;
+  const int chunk = (col & 63) >> 3;
+  return base + half * (kTileTok * 128) + row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+struct SplitParams {
+  const uint16_t* q;
+  int64_t ld_q;
+  const int32_t* kv_len;
+  int Hq, Hkv, group;
+  int64_t cap;
+  int chunk, max_splits, max_kv_len;
+  float scale_log2;  // softmax scale * log2(e)
+  float* o_part;     // [bs, Hq, max_splits, D]
+  float* lse;        // [bs, Hq, max_splits]
+  uint16_t* out;     // written directly when max_splits == 1
+  int32_t* err;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+}  // namespace
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                             const __grid_constant__ CUtensorMap tmV,
+                                                             const SplitParams p) {
+  using S = AttnShape<D>;
+  constexpr int KS = D / 16;  // k-steps of the QK^T product / m-tiles of O^T
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  uint16_t* pstage = reinterpret_cast<uint16_t*>(smem + S::kBodyBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBodyBytes + S::kPBytes);
+  uint64_t* empty = full + S::kStages;
+
+  const int split = blockIdx.x;
+  const int bg = blockIdx.y;
+  const int b = bg / p.Hkv, g = bg - b * p.Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = p.kv_len[b];
+  if (n < 1 || (int64_t)n > p.cap || n > p.max_kv_len) {
+    if (split == 0 && g == 0 && threadIdx.x == 0) set_error(p.err, MXG_EDEVICE);
+    if (p.max_splits == 1 && warp < kConsumers) {  // single-split mode: no combine pass, zero here
+      for (int i = threadIdx.x; i < p.group * D; i += kConsumers * 32)
+        p.out[((int64_t)b * p.Hq + g * p.group) * D + i] = 0;
+    }
+    return;
+  }
+  const int t0 = split * p.chunk;
+  if (t0 >= n) return;
+  const int t1 = min(n, t0 + p.chunk);
+  const int ntiles = (t1 - t0 + kTileTok - 1) / kTileTok;
+  const int row0 = (int)((int64_t)bg * p.cap + t0);  // host guarantees bs*Hkv*cap < 2^31
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumers);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumers) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+      const uint64_t pol = l2_policy_evict_first();
+      for (int i = 0; i < ntiles; ++i) {
+        const int s = i % S::kStages;
+        if (i >= S::kStages && !mbar_wait(&empty[s], ((i / S::kStages) - 1) & 1, p.err)) break;
+        mbar_arrive_expect_tx(&full[s], S::kStageBytes);
+        uint8_t* kt = ring + s * S::kStageBytes;
+        uint8_t* vt = kt + S::kTileBytes;
+#pragma unroll
+        for (int h = 0; h < S::kHalves; ++h) {
+          tma_load_2d_hint(kt + h * kTileTok * 128, &tmK, &full[s], h * 64, row0 + i * kTileTok, pol);
+          tma_load_2d_hint(vt + h * kTileTok * 128, &tmV, &full[s], h * 64, row0 + i * kTileTok, pol);
+        }
+      }
+    }
+    return;
+  }
+
+  // --------------------------------------------------------------- consumers
+  const int c4 = lane & 3, r4 = lane >> 2;
+  const int h0 = g * p.group;
+  // B fragments of Q^T (k = dim, n = head): lane holds head r4, dims 2*c4 (+1) and +8 (+9)
+  uint32_t qb[KS][2];
+  {
+    const bool hv = r4 < p.group;
+    const uint16_t* qh = p.q + (int64_t)b * p.ld_q + (int64_t)(h0 + (hv ? r4 : 0)) * D;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qb[ks][0] = hv ? *reinterpret_cast<const uint32_t*>(qh + ks * 16 + 2 * c4) : 0u;
+      qb[ks][1] = hv ? *reinterpret_cast<const uint32_t*>(qh + ks * 16 + 8 + 2 * c4) : 0u;
+    }
+  }
+  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+  float o[KS][4];
+#pragma unroll
+  for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+  uint16_t* ps = pstage + warp * (8 * 16);  // P^T staging: [8 heads][16 tokens]
+  const int r0 = warp * 16;
+  bool ok = true;
+  for (int i = 0; i < ntiles; ++i) {
+    const int s = i % S::kStages;
+    if (!mbar_wait(&full[s], (i / S::kStages) & 1, p.err)) { ok = false; break; }
+    const uint32_t kbase = smem_u32(ring + s * S::kStageBytes);
+    const uint32_t vbase = kbase + S::kTileBytes;
+    const int tb = t0 + i * kTileTok + r0;  // first token of this warp's 16 rows
+
+    // S^T[16 tok x 8 heads] = K[16 x D] Q^T[D x 8]
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t a0, a1, a2, a3;
+      ldmatrix_x4(tile_addr(kbase, r0 + (lane & 7) + 8 * ((lane >> 3) & 1), ks * 16 + 8 * (lane >> 4)), a0, a1, a2,
+                  a3);
+      mma_bf16_16816(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+    }
+    const bool va = tb + r4 < t1, vb = tb + r4 + 8 < t1;
+    const float x0 = va ? sc[0] * p.scale_log2 : -INFINITY;  // token r4,   head 2c4
+    const float x1 = va ? sc[1] * p.scale_log2 : -INFINITY;  // token r4,   head 2c4+1
+    const float x2 = vb ? sc[2] * p.scale_log2 : -INFINITY;  // token r4+8, head 2c4
+    const float x3 = vb ? sc[3] * p.scale_log2 : -INFINITY;  // token r4+8, head 2c4+1
+    float ma = fmaxf(x0, x2), mb = fmaxf(x1, x3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      ma = fmaxf(ma, __shfl_xor_sync(MXG_FULL_MASK, ma, off));
+      mb = fmaxf(mb, __shfl_xor_sync(MXG_FULL_MASK, mb, off));
+    }
+    const float na = fmaxf(m_a, ma), nb = fmaxf(m_b, mb);
+    const float ua = na == -INFINITY ? 0.f : na, ub = nb == -INFINITY ? 0.f : nb;
+    const float alpha_a = exp2f(m_a - ua), alpha_b = exp2f(m_b - ub);
+    m_a = na;
+    m_b = nb;
+    const __nv_bfloat16 p0 = __float2bfloat16_rn(exp2f(x0 - ua));
+    const __nv_bfloat16 p1 = __float2bfloat16_rn(exp2f(x1 - ub));
+    const __nv_bfloat16 p2 = __float2bfloat16_rn(exp2f(x2 - ua));
+    const __nv_bfloat16 p3 = __float2bfloat16_rn(exp2f(x3 - ub));
+    l_a = l_a * alpha_a + (__bfloat162float(p0) + __bfloat162float(p2));
+    l_b = l_b * alpha_b + (__bfloat162float(p1) + __bfloat162float(p3));
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      o[mt][0] *= alpha_a;
+      o[mt][1] *= alpha_b;
+      o[mt][2] *= alpha_a;
+      o[mt][3] *= alpha_b;
+    }
+    ps[(2 * c4) * 16 + r4] = __bfloat16_as_ushort(p0);
+    ps[(2 * c4 + 1) * 16 + r4] = __bfloat16_as_ushort(p1);
+    ps[(2 * c4) * 16 + r4 + 8] = __bfloat16_as_ushort(p2);
+    ps[(2 * c4 + 1) * 16 + r4 + 8] = __bfloat16_as_ushort(p3);
+    // rows past the split end may hold anything; P is 0 there, and V is zeroed so that a
+    // non-finite value cannot turn 0 * V into NaN
+    if (tb + 16 > t1) {
+      for (int rr = lane >> 4; rr < 16; rr += 2) {
+        if (tb + rr >= t1) {
+          const int row = r0 + rr;
+          const int cb = (lane & 15) * 16;  // 16 lanes x 16 bytes cover 256 bytes (two 128-byte halves)
+          if (cb < D * 2) {
+            const int half = cb >> 7;
+            uint8_t* dst = ring + s * S::kStageBytes + S::kTileBytes + half * (kTileTok * 128) + row * 128 + (cb & 127);
+            *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+    }
+    __syncwarp();
+    const uint32_t b0 = *reinterpret_cast<const uint32_t*>(ps + r4 * 16 + 2 * c4);
+    const uint32_t b1 = *reinterpret_cast<const uint32_t*>(ps + r4 * 16 + 8 + 2 * c4);
+    // O^T[D x 8] += V^T[D x 16 tok] P^T[16 tok x 8]
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      uint32_t a0, a1, a2, a3;
+      ldmatrix_x4_trans(tile_addr(vbase, r0 + (lane & 7) + 8 * (lane >> 4), mt * 16 + 8 * ((lane >> 3) & 1)), a0, a1,
+                        a2, a3);
+      mma_bf16_16816(o[mt], a0, a1, a2, a3, b0, b1);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+  if (!ok) return;
+
+  // l partial sums: reduce over the 8 lanes that share a head pair
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    l_a += __shfl_xor_sync(MXG_FULL_MASK, l_a, off);
+    l_b += __shfl_xor_sync(MXG_FULL_MASK, l_b, off);
+  }
+  // merge the consumer warps through shared memory (the ring is idle now: every issued tile
+  // was consumed before the named barrier below)
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+  float* os = reinterpret_cast<float*>(ring);                 // [warp][8 heads][D]
+  float* ml = os + kConsumers * 8 * D;                         // [warp][8 heads][m, l]
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt) {
+    const int d = mt * 16 + r4;
+    os[(warp * 8 + 2 * c4) * D + d] = o[mt][0];
+    os[(warp * 8 + 2 * c4 + 1) * D + d] = o[mt][1];
+    os[(warp * 8 + 2 * c4) * D + d + 8] = o[mt][2];
+    os[(warp * 8 + 2 * c4 + 1) * D + d + 8] = o[mt][3];
+  }
+  if (r4 == 0) {
+    ml[(warp * 8 + 2 * c4) * 2] = m_a;
+    ml[(warp * 8 + 2 * c4) * 2 + 1] = l_a;
+    ml[(warp * 8 + 2 * c4 + 1) * 2] = m_b;
+    ml[(warp * 8 + 2 * c4 + 1) * 2 + 1] = l_b;
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+  for (int idx = threadIdx.x; idx < p.group * D; idx += kConsumers * 32) {
+    const int h = idx / D, d = idx - h * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, ml[(w * 8 + h) * 2]);
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumers; ++w) {
+      const float mw = ml[(w * 8 + h) * 2];
+      const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
+      L += ml[(w * 8 + h) * 2 + 1] * f;
+      O += os[(w * 8 + h) * D + d] * f;
+    }
+    const int64_t bh = (int64_t)b * p.Hq + h0 + h;
+    if (p.max_splits == 1) {
+      p.out[bh * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(O / L));
+    } else {
+      p.o_part[(bh * p.max_splits + split) * D + d] = O / L;
+      if (d == 0) p.lse[bh * p.max_splits + split] = M + log2f(L);
+    }
+  }
+}
+
+// Merge the splits of each (b, h): weights 2^(lse_i - max lse).
+template <int D>
+__global__ void __launch_bounds__(D) gqa_combine_kernel(const float* __restrict__ o_part,
+                                                        const float* __restrict__ lse,
+                                                        const int32_t* __restrict__ kv_len, int Hq, int64_t cap,
+                                                        int chunk, int max_splits, int max_kv_len,
+                                                        uint16_t* __restrict__ out) {
+  const int64_t bh = blockIdx.x;
+  const int b = (int)(bh / Hq);
+  const int d = threadIdx.x;
+  const int n = kv_len[b];
+  if (n < 1 || (int64_t)n > cap || n > max_kv_len) {
+    out[bh * D + d] = 0;
+    return;
+  }
+  const int ns = (n + chunk - 1) / chunk;
+  const float* l = lse + bh * max_splits;
+  float M = -INFINITY;
+  for (int i = 0; i < ns; ++i) M = fmaxf(M, l[i]);
+  float W = 0.f, acc = 0.f;
+  for (int i = 0; i < ns; ++i) {
+    const float w = exp2f(l[i] - M);
+    W += w;
+    acc += w * o_part[(bh * max_splits + i) * D + d];
+  }
+  out[bh * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(acc / W));
+}
+
+// ---------------------------------------------------------------------------------- host
+int attn_chunk(int64_t bs, int64_t Hkv, int64_t max_kv_len) {
+  // aim for ~3000 (b, g, split) work items at the bound, 64..1024 tokens per split
+  int64_t c = (bs * Hkv * max_kv_len + 2999) / 3000;
+  c = (c + kTileTok - 1) / kTileTok * kTileTok;
+  if (c < kTileTok) c = kTileTok;
+  if (c > 1024) c = 1024;
+  return (int)c;
+}
+
+size_t attn_workspace_bytes(int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t max_kv_len) {
+  const int chunk = attn_chunk(bs, Hkv, max_kv_len);
+  const int64_t ms = (max_kv_len + chunk - 1) / chunk;
+  if (ms <= 1) return 0;
+  return (size_t)(bs * Hq * ms * (D + 1)) * sizeof(float);
+}
+
+cudaError_t launch_gqa_decode_attn(const CUtensorMap& tmK, const CUtensorMap& tmV, const uint16_t* q, int64_t ld_q,
+                                   const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t cap,
+                                   int64_t max_kv_len, float scale, uint16_t* out, int32_t* err, void* ws,
+                                   cudaStream_t st) {
+  const int chunk = attn_chunk(bs, Hkv, max_kv_len);
+  const int ms = (int)((max_kv_len + chunk - 1) / chunk);
+  SplitParams p;
+  p.q = q;
+  p.ld_q = ld_q;
+  p.kv_len = kv_len;
+  p.Hq = (int)Hq;
+  p.Hkv = (int)Hkv;
+  p.group = (int)(Hq / Hkv);
+  p.cap = cap;
+  p.chunk = chunk;
+  p.max_splits = ms;
+  p.max_kv_len = (int)max_kv_len;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.o_part = reinterpret_cast<float*>(ws);
+  p.lse = ms > 1 ? p.o_part + bs * Hq * ms * D : nullptr;
+  p.out = out;
+  p.err = err;
+  dim3 grid((unsigned)ms, (unsigned)(bs * Hkv));
+  cudaError_t e;
+  if (D == 128) {
+    const int smem = AttnShape<128>::kSmemBytes;
+    e = cudaFuncSetAttribute(gqa_split_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    gqa_split_kernel<128><<<grid, kThreads, smem, st>>>(tmK, tmV, p);
+  } else {
+    const int smem = AttnShape<64>::kSmemBytes;
+    e = cudaFuncSetAttribute(gqa_split_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    gqa_split_kernel<64><<<grid, kThreads, smem, st>>>(tmK, tmV, p);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess || ms == 1) return e;
+  if (D == 128)
+    gqa_combine_kernel<128><<<(unsigned)(bs * Hq), 128, 0, st>>>(p.o_part, p.lse, kv_len, (int)Hq, cap, chunk, ms,
+                                                                 (int)max_kv_len, out);
+  else
+    gqa_combine_kernel<64><<<(unsigned)(bs * Hq), 64, 0, st>>>(p.o_part, p.lse, kv_len, (int)Hq, cap, chunk, ms,
+                                                               (int)max_kv_len, out);
+  return cudaGetLastError();
+}
+
+}  // namespace mxg

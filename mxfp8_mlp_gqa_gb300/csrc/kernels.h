@@ -1,0 +1,38 @@
+// Internal launchers shared between the kernel translation units and the C ABI layer.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mxg {
+
+cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ld_x, uint8_t* q, uint8_t* s,
+                                  cudaStream_t st);
+cudaError_t launch_rmsnorm_mxfp8_quantize(const uint16_t* x, const uint16_t* gamma, float eps, int64_t M, int64_t K,
+                                          int64_t ld_x, uint8_t* q, uint8_t* s, cudaStream_t st);
+
+cudaError_t launch_prev_tokens_shift(int32_t* prev, const int32_t* next, int64_t bs, int64_t W, int64_t cw,
+                                     cudaStream_t st);
+cudaError_t launch_kv_append(uint16_t* kc, uint16_t* vc, const uint16_t* kn, const uint16_t* vn, int64_t ld_new,
+                             const int32_t* kv_len, int64_t bs, int64_t Hkv, int64_t D, int64_t cap, int32_t* err,
+                             cudaStream_t st);
+
+int attn_chunk(int64_t bs, int64_t Hkv, int64_t max_kv_len);
+size_t attn_workspace_bytes(int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t max_kv_len);
+cudaError_t launch_gqa_decode_attn(const CUtensorMap& tmK, const CUtensorMap& tmV, const uint16_t* q, int64_t ld_q,
+                                   const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t cap,
+                                   int64_t max_kv_len, float scale, uint16_t* out, int32_t* err, void* ws,
+                                   cudaStream_t st);
+
+cudaError_t launch_mx_gemm_simt(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs,
+                                int64_t M, int64_t N, int64_t K, const uint16_t* res, uint16_t* c, cudaStream_t st);
+cudaError_t launch_gate_up_swiglu_simt(const uint8_t* xq, const uint8_t* xs, int64_t M, int64_t d_model,
+                                       int64_t d_ff, const uint8_t* w13q, const uint8_t* w13s, uint8_t* hq,
+                                       uint8_t* hs, cudaStream_t st);
+
+// 2-D row-major tensor map (inner dimension first) for TMA; false if the driver refused it.
+bool make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz);
+
+}  // namespace mxg

@@ -1,0 +1,148 @@
+// MXFP8 activation quantisation (optionally fused with RMSNorm).
+//
+// [S2.1] "Kernel Benchmark Results": one launch quantises bf16 activations to E4M3 and packs
+// the UE8M0 scales; "FP8 Quantization Strategy": 1x32 blocks along K, OCP UE8M0 exponents.
+//
+// Work split: one thread owns 8 consecutive elements (one 16-byte load), four adjacent lanes
+// own one 32-element block and combine their |max| with two xor-shuffles. Loads are 128-bit
+// and coalesced; each lane stores 8 E4M3 bytes, lane 0 of each quad stores the scale byte.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mxg {
+
+// Quantise the 8 values this lane holds as part of a 4-lane 32-element block.
+// Every lane of the warp must call this (the shuffles use the full mask).
+__device__ __forceinline__ void mx_quant8(const float (&v)[8], uint2& packed, uint8_t& sbyte) {
+  float a = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[i]));
+  a = fmaxf(a, __shfl_xor_sync(MXG_FULL_MASK, a, 1));
+  a = fmaxf(a, __shfl_xor_sync(MXG_FULL_MASK, a, 2));
+  const int s = mx_shared_exp(a);
+  const float inv = mx_inv_scale(s);
+  const uint32_t p0 = cvt_e4m3x2(v[0] * inv, v[1] * inv);
+  const uint32_t p1 = cvt_e4m3x2(v[2] * inv, v[3] * inv);
+  const uint32_t p2 = cvt_e4m3x2(v[4] * inv, v[5] * inv);
+  const uint32_t p3 = cvt_e4m3x2(v[6] * inv, v[7] * inv);
+  packed.x = p0 | (p1 << 16);
+  packed.y = p2 | (p3 << 16);
+  sbyte = (uint8_t)(s + 127);
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4& w, float (&v)[8]) {
+  v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x);
+  v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+  v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z);
+  v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+}
+
+__global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
+                                                             int64_t ld_x, uint8_t* __restrict__ q,
+                                                             uint8_t* __restrict__ s) {
+  const int64_t cpr = K >> 3;  // 8-element chunks per row (a multiple of 4)
+  const int64_t total = M * cpr;
+  const int64_t step = (int64_t)gridDim.x * blockDim.x;
+  // the trip count is uniform per block, so whole warps reach the shuffles together
+  for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < total; base += step) {
+    const int64_t c = base + threadIdx.x;
+    const bool act = c < total;
+    int64_t row = 0, col = 0;
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (act) {
+      row = c / cpr;
+      col = (c - row * cpr) << 3;
+      w = __ldg(reinterpret_cast<const uint4*>(x + row * ld_x + col));
+    }
+    float v[8];
+    unpack_bf16x8(w, v);
+    uint2 packed;
+    uint8_t sb;
+    mx_quant8(v, packed, sb);
+    if (act) {
+      *reinterpret_cast<uint2*>(q + row * K + col) = packed;
+      if ((threadIdx.x & 3) == 0) s[row * (K >> 5) + (col >> 5)] = sb;
+    }
+  }
+}
+
+// One CTA per row. Pass 1: sum of squares in fp64 (each square is exact in fp64). Pass 2:
+// y = bf16((x * r) * gamma) with r rounded to fp32 once, then the MX rule on y.
+__global__ void __launch_bounds__(256) rmsnorm_mxfp8_quantize_kernel(const uint16_t* __restrict__ x,
+                                                                     const uint16_t* __restrict__ gamma, float eps,
+                                                                     int64_t K, int64_t ld_x,
+                                                                     uint8_t* __restrict__ q,
+                                                                     uint8_t* __restrict__ s) {
+  const int64_t row = blockIdx.x;
+  const uint16_t* xr = x + row * ld_x;
+  const int cpr = (int)(K >> 3);
+  double acc = 0.0;
+  for (int c = threadIdx.x; c < cpr; c += blockDim.x) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(xr + ((int64_t)c << 3)));
+    float v[8];
+    unpack_bf16x8(w, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc += (double)v[i] * (double)v[i];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(MXG_FULL_MASK, acc, o);
+  __shared__ double red[32];
+  __shared__ float r_sh;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t += red[i];
+    const double ms = t / (double)K;
+    r_sh = (float)(1.0 / sqrt(ms + (double)eps));
+  }
+  __syncthreads();
+  const float r = r_sh;
+  for (int base = 0; base < cpr; base += blockDim.x) {
+    const int c = base + threadIdx.x;
+    const bool act = c < cpr;
+    float v[8];
+    if (act) {
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(xr + ((int64_t)c << 3)));
+      const uint4 g = __ldg(reinterpret_cast<const uint4*>(gamma + ((int64_t)c << 3)));
+      float xv[8], gv[8];
+      unpack_bf16x8(w, xv);
+      unpack_bf16x8(g, gv);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float y = __fmul_rn(__fmul_rn(xv[i], r), gv[i]);
+        v[i] = __bfloat162float(__float2bfloat16_rn(y));
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    }
+    uint2 packed;
+    uint8_t sb;
+    mx_quant8(v, packed, sb);
+    if (act) {
+      *reinterpret_cast<uint2*>(q + row * K + ((int64_t)c << 3)) = packed;
+      if ((lane & 3) == 0) s[row * (K >> 5) + (c >> 2)] = sb;
+    }
+  }
+}
+
+cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ld_x, uint8_t* q, uint8_t* s,
+                                  cudaStream_t st) {
+  const int64_t total = M * (K >> 3);
+  const int threads = 256;
+  int64_t blocks = (total + threads - 1) / threads;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks < 1) blocks = 1;
+  mxfp8_quantize_kernel<<<(unsigned)blocks, threads, 0, st>>>(x, M, K, ld_x, q, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm_mxfp8_quantize(const uint16_t* x, const uint16_t* gamma, float eps, int64_t M, int64_t K,
+                                          int64_t ld_x, uint8_t* q, uint8_t* s, cudaStream_t st) {
+  rmsnorm_mxfp8_quantize_kernel<<<(unsigned)M, 256, 0, st>>>(x, gamma, eps, K, ld_x, q, s);
+  return cudaGetLastError();
+}
+
+}  // namespace mxg

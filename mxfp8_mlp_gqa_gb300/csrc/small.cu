@@ -1,0 +1,65 @@
+// Small per-step data-movement kernels: the Dual-AR prev-tokens window shift and the KV
+// cache append.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mxg {
+
+// [S2.1] "DualAR: S2-Specific Batching Constraints": prev int32 [bs, W, cw] slides by one
+// frame and next_tokens int32 [bs, cw] becomes the newest frame. One CTA per sequence: the
+// whole window is read into shared memory before any element is written, so the in-place
+// update never reads a value it has already overwritten.
+__global__ void __launch_bounds__(256) prev_tokens_shift_kernel(int32_t* __restrict__ prev,
+                                                                const int32_t* __restrict__ next, int W, int cw) {
+  extern __shared__ int32_t win[];
+  const int n = W * cw;
+  int32_t* p = prev + (int64_t)blockIdx.x * n;
+  const int32_t* nx = next + (int64_t)blockIdx.x * cw;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) win[i] = p[i];
+  __syncthreads();
+  const int keep = n - cw;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) p[i] = i < keep ? win[i + cw] : nx[i - keep];
+}
+
+// [FSKV] §5 (kv_cache.update, in place): K/V rows of this step land at position kv_len-1.
+// One warp per (sequence, kv head); each lane moves 16 bytes of K and of V.
+__global__ void __launch_bounds__(256) kv_append_kernel(uint16_t* __restrict__ kc, uint16_t* __restrict__ vc,
+                                                        const uint16_t* __restrict__ kn,
+                                                        const uint16_t* __restrict__ vn, int64_t ld_new,
+                                                        const int32_t* __restrict__ kv_len, int bs, int Hkv, int D,
+                                                        int64_t cap, int32_t* err) {
+  const int gw = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (gw >= bs * Hkv) return;
+  const int b = gw / Hkv, g = gw - b * Hkv;
+  const int n = kv_len[b];
+  if (n < 1 || (int64_t)n > cap) {
+    if (lane == 0 && g == 0) set_error(err, MXG_EDEVICE);
+    return;
+  }
+  const int64_t dst = (((int64_t)b * Hkv + g) * cap + (n - 1)) * D;
+  const int64_t src = (int64_t)b * ld_new + (int64_t)g * D;
+  for (int i = lane * 8; i < D; i += 256) {
+    *reinterpret_cast<uint4*>(kc + dst + i) = *reinterpret_cast<const uint4*>(kn + src + i);
+    *reinterpret_cast<uint4*>(vc + dst + i) = *reinterpret_cast<const uint4*>(vn + src + i);
+  }
+}
+
+cudaError_t launch_prev_tokens_shift(int32_t* prev, const int32_t* next, int64_t bs, int64_t W, int64_t cw,
+                                     cudaStream_t st) {
+  const size_t smem = (size_t)W * cw * sizeof(int32_t);
+  prev_tokens_shift_kernel<<<(unsigned)bs, 256, smem, st>>>(prev, next, (int)W, (int)cw);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_append(uint16_t* kc, uint16_t* vc, const uint16_t* kn, const uint16_t* vn, int64_t ld_new,
+                             const int32_t* kv_len, int64_t bs, int64_t Hkv, int64_t D, int64_t cap, int32_t* err,
+                             cudaStream_t st) {
+  const int64_t warps = bs * Hkv;
+  const int64_t blocks = (warps * 32 + 255) / 256;
+  kv_append_kernel<<<(unsigned)blocks, 256, 0, st>>>(kc, vc, kn, vn, ld_new, kv_len, (int)bs, (int)Hkv, (int)D, cap,
+                                                     err);
+  return cudaGetLastError();
+}
+
+}  // namespace mxg

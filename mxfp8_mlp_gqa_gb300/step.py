@@ -1,0 +1,101 @@
+"""One slow-AR decoder-layer step under continuous batching, composed from the library's
+entry points (every step runs in libmxg kernels; this module only owns buffers and the
+call order):
+
+    RMSNorm+MX-quantise -> QKV projection (MXFP8 GEMM) -> KV append -> GQA decode
+    attention -> MX-quantise -> O projection + residual -> RMSNorm+MX-quantise ->
+    SwiGLU MLP (gate/up + SwiGLU + requant, down + residual) -> prev-window shift
+
+The pages list the layer as RMSNorm -> attention -> RMSNorm -> MLP (Qwen3-style, [S2.1]
+"The Real Reason Voice AI Costs Money" / "Kernel Benchmark Results", [FSKV] §2). The QKV
+and O projections are the plainest way to join a 32x128-wide attention to a 2560-wide
+residual stream; RoPE and QK-norm are not on the pages and are left out.
+
+All buffers have stable addresses, so ``capture()`` records the step in a CUDA graph and
+``replay()`` re-launches it; ``kv_len`` / ``next_tokens`` / ``x`` are updated in place
+between replays.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import api
+
+
+class DecodeLayer:
+    def __init__(self, bs, d_model, d_ff, Hq, Hkv, D, cap, max_kv_len, W, cw, eps=1e-6, device="cuda"):
+        self.bs, self.d_model, self.d_ff = bs, d_model, d_ff
+        self.Hq, self.Hkv, self.D, self.cap = Hq, Hkv, D, cap
+        self.max_kv_len, self.eps, self.scale = max_kv_len, eps, 1.0 / math.sqrt(D)
+        dev = torch.device(device)
+        u8, bf, i32 = torch.uint8, torch.bfloat16, torch.int32
+        nqkv = (Hq + 2 * Hkv) * D
+        self.nqkv = nqkv
+        e = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)  # noqa: E731
+        # caller-visible state / inputs
+        self.x = e((bs, d_model), bf)
+        self.kv_len = e((bs,), i32)
+        self.prev = e((bs, W, cw), i32)
+        self.next_tokens = e((bs, cw), i32)
+        self.k_cache = e((bs, Hkv, cap, D), bf)
+        self.v_cache = e((bs, Hkv, cap, D), bf)
+        self.err = torch.zeros((1,), dtype=i32, device=dev)
+        # weights (MXFP8, set by load_weights)
+        self.wqkv = (e((nqkv, d_model), u8), e((nqkv, d_model // 32), u8))
+        self.wo = (e((d_model, Hq * D), u8), e((d_model, Hq * D // 32), u8))
+        self.w13 = (e((2 * d_ff, d_model), u8), e((2 * d_ff, d_model // 32), u8))
+        self.w2 = (e((d_model, d_ff), u8), e((d_model, d_ff // 32), u8))
+        self.gamma1 = e((d_model,), bf)
+        self.gamma2 = e((d_model,), bf)
+        # intermediates
+        self.xq, self.xs = e((bs, d_model), u8), e((bs, d_model // 32), u8)
+        self.qkv = e((bs, nqkv), bf)
+        self.o = e((bs, Hq, D), bf)
+        self.oq, self.os = e((bs, Hq * D), u8), e((bs, Hq * D // 32), u8)
+        self.x1 = e((bs, d_model), bf)
+        self.hq_in, self.hs_in = e((bs, d_model), u8), e((bs, d_model // 32), u8)
+        self.y = e((bs, d_model), bf)
+        self.ws_attn = e((max(1, api.gqa_decode_attn_workspace(bs, Hq, Hkv, D, max_kv_len)),), u8)
+        self.ws_mlp = e((api.mlp_swiglu_mxfp8_workspace(bs, d_model, d_ff),), u8)
+        self.graph = None
+
+    def load_weights(self, wqkv_bf16, wo_bf16, w13_bf16, w2_bf16, gamma1, gamma2):
+        """bf16 weights on the device -> MXFP8 once (weight prep, not part of a step)."""
+        for src, dst in ((wqkv_bf16, self.wqkv), (wo_bf16, self.wo), (w13_bf16, self.w13), (w2_bf16, self.w2)):
+            api.mxfp8_quantize(src, q=dst[0], s=dst[1])
+        self.gamma1.copy_(gamma1)
+        self.gamma2.copy_(gamma2)
+
+    def step(self):
+        Hq, Hkv, D = self.Hq, self.Hkv, self.D
+        api.rmsnorm_mxfp8_quantize(self.x, self.gamma1, self.eps, q=self.xq, s=self.xs)
+        api.mxfp8_gemm(self.xq, self.xs, *self.wqkv, c=self.qkv)
+        qd, kd = Hq * D, Hkv * D
+        api.kv_append(self.k_cache, self.v_cache, self.qkv[:, qd:qd + kd], self.qkv[:, qd + kd:], self.kv_len,
+                      err=self.err)
+        api.gqa_decode_attn(self.qkv[:, :qd], self.k_cache, self.v_cache, self.kv_len, self.max_kv_len, self.scale,
+                            out=self.o, err=self.err, workspace=self.ws_attn)
+        api.mxfp8_quantize(self.o.view(self.bs, qd), q=self.oq, s=self.os)
+        api.mxfp8_gemm(self.oq, self.os, *self.wo, residual=self.x, c=self.x1)
+        api.rmsnorm_mxfp8_quantize(self.x1, self.gamma2, self.eps, q=self.hq_in, s=self.hs_in)
+        api.mlp_swiglu_mxfp8(self.hq_in, self.hs_in, *self.w13, *self.w2, residual=self.x1, y=self.y,
+                             workspace=self.ws_mlp)
+        api.prev_tokens_shift(self.prev, self.next_tokens)
+        return self.y
+
+    def capture(self):
+        """Record one step in a CUDA graph (run once eagerly first so lazy init is done)."""
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.graph, stream=s):
+                self.step()
+        torch.cuda.current_stream().wait_stream(s)
+        return self.graph
+
+    def replay(self):
+        self.graph.replay()
+        return self.y

@@ -38,9 +38,9 @@ def rng(seed: int, tid: int) -> np.random.Generator:
 def f32_to_bf16_bits(a) -> np.ndarray:
     """Round float32 values to bf16 (round to nearest, ties to even); NaN kept quiet."""
     a = np.ascontiguousarray(a, dtype=np.float32)
-    u = a.view(np.uint32).astype(np.uint64)
-    lsb = (u >> 16) & 1
-    r = ((u + 0x7FFF + lsb) >> 16).astype(np.uint16)
+    u = a.view(np.uint32)
+    # finite values are <= 0xFF7FFFFF, so adding at most 0x8000 cannot wrap a uint32
+    r = ((u + (np.uint32(0x7FFF) + ((u >> 16) & np.uint32(1)))) >> 16).astype(np.uint16)
     nan = np.isnan(a)
     if nan.any():
         r = np.where(nan, np.uint16(0x7FC0), r)
