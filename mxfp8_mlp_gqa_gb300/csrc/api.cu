@@ -66,20 +66,20 @@ const char* mxg_status_str(int s) {
 int mxg_version(void) { return 100; }
 
 mxg_status mxfp8_quantize(const void* x, int64_t M, int64_t K, int64_t ld_x, uint8_t* q, uint8_t* s, void* stream) {
-  if (!x || !q || !s) return MXG_EINVAL;
   if (M < 0 || K <= 0 || K % 32 || ld_x < K) return MXG_ESHAPE;
+  if (M == 0) return MXG_OK;  // nothing to read or write (empty tensors may carry null pointers)
+  if (!x || !q || !s) return MXG_EINVAL;
   if (!aligned16(x) || !aligned16(q) || ld_x % 8) return MXG_EALIGN;
-  if (M == 0) return MXG_OK;
   return launched(launch_mxfp8_quantize(static_cast<const uint16_t*>(x), M, K, ld_x, q, s, (cudaStream_t)stream));
 }
 
 mxg_status rmsnorm_mxfp8_quantize(const void* x, const void* gamma, float eps, int64_t M, int64_t K, int64_t ld_x,
                                   uint8_t* q, uint8_t* s, void* stream) {
-  if (!x || !gamma || !q || !s) return MXG_EINVAL;
   if (!(eps >= 0.f)) return MXG_EINVAL;
   if (M < 0 || K <= 0 || K % 32 || K > 16384 || ld_x < K || M > 0x7fffffff) return MXG_ESHAPE;
-  if (!aligned16(x) || !aligned16(gamma) || !aligned16(q) || ld_x % 8) return MXG_EALIGN;
   if (M == 0) return MXG_OK;
+  if (!x || !gamma || !q || !s) return MXG_EINVAL;
+  if (!aligned16(x) || !aligned16(gamma) || !aligned16(q) || ld_x % 8) return MXG_EALIGN;
   return launched(launch_rmsnorm_mxfp8_quantize(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(gamma),
                                                 eps, M, K, ld_x, q, s, (cudaStream_t)stream));
 }
@@ -93,12 +93,12 @@ mxg_status mxfp8_gemm(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, c
                       int64_t N, int64_t K, const void* residual, void* c, void* workspace, size_t ws_bytes,
                       void* stream) {
   (void)workspace;
-  if (!aq || !as || !bq || !bs || !c) return MXG_EINVAL;
   if (M < 0 || N <= 0 || K <= 0 || K % 32 || N % 8 || M > 0x7fffffff || N > 0x7fffffff || K > 0x7fffffff)
     return MXG_ESHAPE;
+  if (M == 0) return MXG_OK;
+  if (!aq || !as || !bq || !bs || !c) return MXG_EINVAL;
   if (!aligned16(aq) || !aligned16(bq) || !aligned16(c) || (residual && !aligned16(residual))) return MXG_EALIGN;
   if (ws_bytes < mxfp8_gemm_workspace(M, N, K)) return MXG_EWORKSPACE;
-  if (M == 0) return MXG_OK;
   return launched(launch_mx_gemm_simt(aq, as, bq, bs, M, N, K, static_cast<const uint16_t*>(residual),
                                       static_cast<uint16_t*>(c), (cudaStream_t)stream));
 }
@@ -106,10 +106,10 @@ mxg_status mxfp8_gemm(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, c
 mxg_status mlp_gate_up_swiglu_mxfp8(const uint8_t* xq, const uint8_t* xs, int64_t M, int64_t d_model, int64_t d_ff,
                                     const uint8_t* w13q, const uint8_t* w13s, uint8_t* hq, uint8_t* hs,
                                     void* stream) {
-  if (!xq || !xs || !w13q || !w13s || !hq || !hs) return MXG_EINVAL;
   if (M < 0 || d_model <= 0 || d_ff <= 0 || d_model % 32 || d_ff % 128 || M > 0x7fffffff) return MXG_ESHAPE;
-  if (!aligned16(xq) || !aligned16(w13q) || !aligned16(hq)) return MXG_EALIGN;
   if (M == 0) return MXG_OK;
+  if (!xq || !xs || !w13q || !w13s || !hq || !hs) return MXG_EINVAL;
+  if (!aligned16(xq) || !aligned16(w13q) || !aligned16(hq)) return MXG_EALIGN;
   return launched(launch_gate_up_swiglu_simt(xq, xs, M, d_model, d_ff, w13q, w13s, hq, hs, (cudaStream_t)stream));
 }
 
@@ -122,9 +122,9 @@ size_t mlp_swiglu_mxfp8_workspace(int64_t M, int64_t d_model, int64_t d_ff) {
 mxg_status mlp_swiglu_mxfp8(const uint8_t* xq, const uint8_t* xs, int64_t M, int64_t d_model, int64_t d_ff,
                             const uint8_t* w13q, const uint8_t* w13s, const uint8_t* w2q, const uint8_t* w2s,
                             const void* residual, void* y, void* workspace, size_t ws_bytes, void* stream) {
-  if (!xq || !xs || !w13q || !w13s || !w2q || !w2s || !y) return MXG_EINVAL;
   if (M < 0 || d_model <= 0 || d_ff <= 0 || d_model % 32 || d_ff % 128 || M > 0x7fffffff) return MXG_ESHAPE;
   if (M == 0) return MXG_OK;
+  if (!xq || !xs || !w13q || !w13s || !w2q || !w2s || !y) return MXG_EINVAL;
   if (!workspace || ws_bytes < mlp_swiglu_mxfp8_workspace(M, d_model, d_ff)) return MXG_EWORKSPACE;
   if (!aligned16(workspace)) return MXG_EALIGN;
   uint8_t* hq = static_cast<uint8_t*>(workspace);

@@ -67,3 +67,21 @@ def assert_requant_close(hq_g, hs_g, hq_o, hs_o, frac=1e-3):
         step = np.exp2(np.maximum(hs_g, hs_o)[flip].astype(np.float64) - 127.0)[:, None] * 2.0 ** (8 - 3)
         assert np.all(np.abs(vg - vo) <= step)
     return float(flip.mean()), float((d > 0).mean())
+
+
+def bf16_ulp(x):
+    """Spacing of bf16 numbers at |x| (2^(floor(log2|x|) - 7)); 2^-133 at zero."""
+    a = np.maximum(np.abs(np.asarray(x, np.float64)), 2.0 ** -126)
+    return np.exp2(np.floor(np.log2(a)) - 7)
+
+
+def assert_attn_close(got, ref, floor_ulp=False):
+    """Attention acceptance: max |err| <= 2e-3 against the fp64 oracle. With floor_ulp, the
+    bound per element is max(2e-3, one bf16 step at |ref|): outputs of magnitude above 0.5
+    (short prefixes, where o is close to a single V row) cannot be stored in bf16 closer
+    than half a step, so 2e-3 alone is below the output format's resolution there."""
+    err = np.abs(np.asarray(got, np.float64) - ref)
+    tol = np.maximum(2e-3, bf16_ulp(ref)) if floor_ulp else 2e-3
+    bad = err > tol
+    assert not bad.any(), f"max err {err.max():.3e}; {bad.sum()} elements above the bound"
+    return float(err.max())
