@@ -208,7 +208,7 @@ def timed_ops(L, ev):
     ev[0].record()
     api.rmsnorm_mxfp8_quantize(L.x, L.gamma1, L.eps, q=L.xq, s=L.xs)
     ev[1].record()
-    api.mxfp8_gemm(L.xq, L.xs, *L.wqkv, c=L.qkv)
+    api.mxfp8_gemm(L.xq, L.xs, *L.wqkv, c=L.qkv, workspace=L.ws_qkv)
     ev[2].record()
     api.kv_append(L.k_cache, L.v_cache, L.qkv[:, qd:qd + kd], L.qkv[:, qd + kd:], L.kv_len, err=L.err)
     ev[3].record()
@@ -217,7 +217,7 @@ def timed_ops(L, ev):
     ev[4].record()
     api.mxfp8_quantize(L.o.view(L.bs, qd), q=L.oq, s=L.os)
     ev[5].record()
-    api.mxfp8_gemm(L.oq, L.os, *L.wo, residual=L.x, c=L.x1)
+    api.mxfp8_gemm(L.oq, L.os, *L.wo, residual=L.x, c=L.x1, workspace=L.ws_o)
     ev[6].record()
     api.rmsnorm_mxfp8_quantize(L.x1, L.gamma2, L.eps, q=L.hq_in, s=L.hs_in)
     ev[7].record()

@@ -54,6 +54,11 @@ typedef enum {
 const char* mxg_status_str(int status);
 /* Library ABI version (major*10000 + minor*100 + patch). */
 int mxg_version(void);
+/* Kernel-path switch for diagnostics and cross-checks: enable != 0 (the default) lets the
+ * GEMM / MLP entry points use the tcgen05 tensor-core kernels wherever the shape allows
+ * (K % 128 == 0); enable == 0 forces the CUDA-core kernels. Process-wide, not thread-safe;
+ * returns the previous setting. */
+int mxg_set_tensor_core_path(int enable);
 
 /*
  * mxfp8_quantize -- fused activation quantisation + UE8M0 scale pack in one launch

@@ -27,6 +27,7 @@ c_i64, c_f32, c_vp, c_sz = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctyp
 _SIGS = {
     "mxg_status_str": (ctypes.c_char_p, [ctypes.c_int]),
     "mxg_version": (ctypes.c_int, []),
+    "mxg_set_tensor_core_path": (ctypes.c_int, [ctypes.c_int]),
     "mxfp8_quantize": (ctypes.c_int, [c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_vp]),
     "rmsnorm_mxfp8_quantize": (ctypes.c_int, [c_vp, c_vp, c_f32, c_i64, c_i64, c_i64, c_vp, c_vp, c_vp]),
     "mxfp8_gemm_workspace": (c_sz, [c_i64, c_i64, c_i64]),
@@ -69,6 +70,11 @@ def lib(path: str | None = None):
             f.argtypes = args
         _LIB = L
     return _LIB
+
+
+def set_tensor_core_path(enable: bool) -> bool:
+    """Force (False) or allow (True, default) the tcgen05 GEMM kernels; returns the previous setting."""
+    return bool(lib().mxg_set_tensor_core_path(1 if enable else 0))
 
 
 def _call(name, *args):
@@ -151,11 +157,15 @@ def mxfp8_gemm(aq, as_, bq, bs, residual=None, c=None, workspace=None):
     c = _out(c, "c", torch.bfloat16, (M, N), aq.device)
     need = lib().mxfp8_gemm_workspace(M, N, K)
     if workspace is None and need:
-        workspace = torch.empty(need, dtype=torch.uint8, device=aq.device)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=aq.device)  # split-K counters start at 0
     ws_bytes = 0 if workspace is None else workspace.numel()
     _call("mxfp8_gemm", _ptr(aq), _ptr(as_), _ptr(bq), _ptr(bs), M, N, K, _ptr(residual), _ptr(c),
           _ptr(workspace), ws_bytes, _stream())
     return c
+
+
+def mxfp8_gemm_workspace(M, N, K) -> int:
+    return int(lib().mxfp8_gemm_workspace(M, N, K))
 
 
 def mlp_gate_up_swiglu_mxfp8(xq, xs, w13q, w13s, hq=None, hs=None):
@@ -191,7 +201,7 @@ def mlp_swiglu_mxfp8(xq, xs, w13q, w13s, w2q, w2s, residual=None, y=None, worksp
     y = _out(y, "y", torch.bfloat16, (M, d_model), xq.device)
     need = mlp_swiglu_mxfp8_workspace(M, d_model, d_ff)
     if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=xq.device)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=xq.device)  # split-K counters start at 0
     _check(workspace, "workspace", torch.uint8, ndim=1)
     _call("mlp_swiglu_mxfp8", _ptr(xq), _ptr(xs), M, d_model, d_ff, _ptr(w13q), _ptr(w13s), _ptr(w2q), _ptr(w2s),
           _ptr(residual), _ptr(y), _ptr(workspace), workspace.numel(), _stream())

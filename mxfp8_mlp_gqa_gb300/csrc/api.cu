@@ -28,7 +28,11 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 inline mxg_status launched(cudaError_t e) { return e == cudaSuccess ? MXG_OK : MXG_ELAUNCH; }
 
+int g_tc_path = 1;  // 1: tcgen05 kernels where the shape allows, 0: CUDA-core kernels only
+
 }  // namespace
+
+bool tensor_core_path_enabled() { return g_tc_path != 0; }
 
 bool make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
                         uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
@@ -65,6 +69,12 @@ const char* mxg_status_str(int s) {
 
 int mxg_version(void) { return 100; }
 
+int mxg_set_tensor_core_path(int enable) {
+  const int prev = g_tc_path;
+  g_tc_path = enable ? 1 : 0;
+  return prev;
+}
+
 mxg_status mxfp8_quantize(const void* x, int64_t M, int64_t K, int64_t ld_x, uint8_t* q, uint8_t* s, void* stream) {
   if (M < 0 || K <= 0 || K % 32 || ld_x < K) return MXG_ESHAPE;
   if (M == 0) return MXG_OK;  // nothing to read or write (empty tensors may carry null pointers)
@@ -85,8 +95,9 @@ mxg_status rmsnorm_mxfp8_quantize(const void* x, const void* gamma, float eps, i
 }
 
 size_t mxfp8_gemm_workspace(int64_t M, int64_t N, int64_t K) {
-  (void)M; (void)N; (void)K;
-  return 0;
+  // sized for the tensor-core plan even when the CUDA-core path is forced, so that a buffer
+  // sized once stays valid if the path changes
+  return tc_gemm_workspace(M, N, K);
 }
 
 mxg_status mxfp8_gemm(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs, int64_t M,
@@ -98,7 +109,15 @@ mxg_status mxfp8_gemm(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, c
   if (M == 0) return MXG_OK;
   if (!aq || !as || !bq || !bs || !c) return MXG_EINVAL;
   if (!aligned16(aq) || !aligned16(bq) || !aligned16(c) || (residual && !aligned16(residual))) return MXG_EALIGN;
-  if (ws_bytes < mxfp8_gemm_workspace(M, N, K)) return MXG_EWORKSPACE;
+  const size_t need = mxfp8_gemm_workspace(M, N, K);
+  if (ws_bytes < need || (need && !workspace)) return MXG_EWORKSPACE;
+  if (need && !aligned16(workspace)) return MXG_EALIGN;
+  if (tensor_core_path_enabled() && tc_gemm_supported(M, N, K)) {
+    bool unsupported = false;
+    cudaError_t e = launch_mx_gemm_tc(aq, as, bq, bs, M, N, K, static_cast<const uint16_t*>(residual),
+                                      static_cast<uint16_t*>(c), workspace, nullptr, (cudaStream_t)stream, &unsupported);
+    if (!unsupported) return launched(e);
+  }
   return launched(launch_mx_gemm_simt(aq, as, bq, bs, M, N, K, static_cast<const uint16_t*>(residual),
                                       static_cast<uint16_t*>(c), (cudaStream_t)stream));
 }
@@ -110,6 +129,12 @@ mxg_status mlp_gate_up_swiglu_mxfp8(const uint8_t* xq, const uint8_t* xs, int64_
   if (M == 0) return MXG_OK;
   if (!xq || !xs || !w13q || !w13s || !hq || !hs) return MXG_EINVAL;
   if (!aligned16(xq) || !aligned16(w13q) || !aligned16(hq)) return MXG_EALIGN;
+  if (tensor_core_path_enabled() && d_model % 128 == 0) {
+    bool unsupported = false;
+    cudaError_t e = launch_gate_up_swiglu_tc(xq, xs, M, d_model, d_ff, w13q, w13s, hq, hs, nullptr,
+                                             (cudaStream_t)stream, &unsupported);
+    if (!unsupported) return launched(e);
+  }
   return launched(launch_gate_up_swiglu_simt(xq, xs, M, d_model, d_ff, w13q, w13s, hq, hs, (cudaStream_t)stream));
 }
 

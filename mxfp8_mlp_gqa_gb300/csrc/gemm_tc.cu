@@ -1,0 +1,387 @@
+// MXFP8 block-scaled GEMM on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// out[m][n] = sum_k X'[m][k] W'[n][k] for MX operands (E4M3 + one UE8M0 scale per 32 along
+// K), [S2.1] "FP8 Quantization Strategy" / "Kernel Benchmark Results". Decode shapes have
+// few tokens (M <= 128) and many output features, so the MMA runs "swapped": the weight
+// tile is the 128-row MMA operand A, the tokens are the MMA N dimension (16..256), and the
+// fp32 accumulator D^T[128 features][N tokens] lives in tensor memory.
+//
+// Per CTA (192 threads):
+//   warp 0  producer: lane 0 issues TMA (128-byte swizzle) for the weight tile (two 64-row
+//           boxes) and the token tile of each 128-wide K group; all 32 lanes cp.async the
+//           UE8M0 words of that group (4 k-blocks per row) into the 32x4 atom layout
+//           (byte 16*(r%32) + 4*(r/32) + kb) that tcgen05.cp 32x128b.warpx4 expects;
+//   warp 1  TMEM owner; lane 0 issues per group: 2 scale copies to TMEM + 4 MMAs
+//           (kind::mxf8f6f4.block_scale, K=32 each, scale byte kb selected in the
+//           instruction descriptor), then tcgen05.commit frees the stage;
+//   warps 2-5 epilogue: read D^T from TMEM (each warp its lane quadrant) and
+//           * kEpiStore : write bf16 out (+ bf16 residual),
+//           * kEpiSplit : write fp32 partials of a K split; the last split of a tile sums
+//                         all splits in a fixed order (+ residual) and writes bf16,
+//           * kEpiSwiGLU: the weight tile is 64 gate rows + the matching 64 up rows; h =
+//                         silu(g) * u in fp32, re-quantised to MXFP8 along d_ff in the
+//                         epilogue (no bf16 h is ever written).
+// Every wait is bounded (MXG_ETIMEOUT in the error flag); TMEM is always released.
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace mxg {
+
+namespace {
+
+constexpr int kKG = 128;  // K elements per stage: one 4-block group of scales
+enum { kEpiStore = 0, kEpiSplit = 1, kEpiSwiGLU = 2 };
+
+template <int BN>
+struct TcShape {
+  static constexpr int kABytes = 128 * kKG;
+  static constexpr int kBBytes = BN * kKG;
+  static constexpr int kSfbAtoms = (BN + 127) / 128;
+  static constexpr int kSfBytes = 1024 * ((512 * (1 + kSfbAtoms) + 1023) / 1024);  // keeps stages 1024-aligned
+  static constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;
+  static constexpr int kStagesRaw = (BN >= 256 ? 200 * 1024 : 104 * 1024) / kStageBytes;
+  static constexpr int kStages = kStagesRaw > 8 ? 8 : (kStagesRaw < 2 ? 2 : kStagesRaw);
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kStagingBytes = 128 * (BN + 1) * 4;
+  static constexpr int kBodyBytes = kRingBytes > kStagingBytes ? kRingBytes : kStagingBytes;
+  static constexpr int kSmemBytes = 1024 + kBodyBytes + 8 * (2 * kStages + 1) + 16;
+  static constexpr uint32_t kTmemCols = BN + 4 * (1 + kSfbAtoms) <= 32    ? 32
+                                        : BN + 4 * (1 + kSfbAtoms) <= 64  ? 64
+                                        : BN + 4 * (1 + kSfbAtoms) <= 128 ? 128
+                                        : BN + 4 * (1 + kSfbAtoms) <= 256 ? 256
+                                                                          : 512;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+struct TcArgs {
+  int M, N, K;          // out[M tokens][N features]; N = 2*d_ff weight rows for SwiGLU
+  int groups, splits;   // K/128 groups, K splits (grid.z)
+  const uint8_t* ws;    // weight scales  [N rows][K/32]
+  const uint8_t* xs;    // token scales   [M][K/32]
+  int d_ff;
+  uint8_t* hq;
+  uint8_t* hs;
+  const uint16_t* residual;
+  uint16_t* out;
+  float* partial;       // [splits][M][N]
+  int* counters;        // one per (n tile, m tile); zero between calls
+  int32_t* err;
+};
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+}  // namespace
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(192, 1) mx_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                            const __grid_constant__ CUtensorMap tmX, const TcArgs a) {
+  using S = TcShape<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBodyBytes);
+  uint64_t* empty = full + S::kStages;
+  uint64_t* tmem_full = empty + S::kStages;
+  uint32_t* tmem_sh = reinterpret_cast<uint32_t*>(tmem_full + 1);
+  int* last_sh = reinterpret_cast<int*>(tmem_sh + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ntile = blockIdx.x, mtile = blockIdx.y, split = blockIdx.z;
+  const int m0 = mtile * BN;
+  const int n0 = EPI == kEpiSwiGLU ? ntile * 64 : ntile * 128;
+  const int a_lo = n0;                                         // weight rows of tile rows 0..63
+  const int a_hi = EPI == kEpiSwiGLU ? a.d_ff + n0 : n0 + 64;  // weight rows of tile rows 64..127
+  const int wrows = EPI == kEpiSwiGLU ? 2 * a.d_ff : a.N;
+  const int g0 = (int)((int64_t)split * a.groups / a.splits);
+  const int g1 = (int)((int64_t)(split + 1) * a.groups / a.splits);
+  const int ng = g1 - g0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S::kStages; ++s) {
+      mbar_init(&full[s], 1 + 32);  // TMA expect-tx arrive + one cp.async arrive per producer lane
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tmem_full, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_sh, S::kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_sh;
+  const uint32_t t_d = tmem, t_sfa = tmem + BN, t_sfb = tmem + BN + 4;
+
+  if (warp == 0) {
+    // ----------------------------------------------------------------- producer
+    if (lane == 0) {
+      prefetch_tensormap(&tmW);
+      prefetch_tensormap(&tmX);
+    }
+    const int64_t KB = a.K >> 5;
+    for (int i = 0; i < ng; ++i) {
+      const int s = i % S::kStages;
+      if (i >= S::kStages && !mbar_wait(&empty[s], ((i / S::kStages) - 1) & 1, a.err)) break;
+      uint8_t* st = ring + s * S::kStageBytes;
+      const int g = g0 + i;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&full[s], S::kABytes + S::kBBytes);
+        tma_load_2d(st, &tmW, &full[s], g * kKG, a_lo);
+        tma_load_2d(st + 64 * kKG, &tmW, &full[s], g * kKG, a_hi);
+        tma_load_2d(st + S::kABytes, &tmX, &full[s], g * kKG, m0);
+      }
+      uint32_t* sfa = reinterpret_cast<uint32_t*>(st + S::kABytes + S::kBBytes);
+#pragma unroll
+      for (int r1 = 0; r1 < 4; ++r1) {
+        const int r = lane + 32 * r1;
+        const int grow = r < 64 ? a_lo + r : a_hi + (r - 64);
+        if (grow < wrows) tc::cp_async4(&sfa[4 * lane + r1], a.ws + (int64_t)grow * KB + 4 * g);
+      }
+#pragma unroll
+      for (int at = 0; at < S::kSfbAtoms; ++at) {
+        uint32_t* sfb = sfa + 128 * (1 + at);
+#pragma unroll
+        for (int r1 = 0; r1 < 4; ++r1) {
+          const int r = 128 * at + lane + 32 * r1;
+          if (r < BN && m0 + r < a.M) tc::cp_async4(&sfb[4 * lane + r1], a.xs + (int64_t)(m0 + r) * KB + 4 * g);
+        }
+      }
+      tc::cp_async_arrive(&full[s]);
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      for (int i = 0; i < ng; ++i) {
+        const int s = i % S::kStages;
+        if (!mbar_wait(&full[s], (i / S::kStages) & 1, a.err)) break;
+        fence_proxy_async_smem();  // cp.async (generic proxy) scale words -> tcgen05.cp (async proxy)
+        tc::fence_after_sync();
+        uint8_t* st = ring + s * S::kStageBytes;
+        const uint32_t sa = smem_u32(st), sb = smem_u32(st + S::kABytes);
+        const uint32_t ssf = smem_u32(st + S::kABytes + S::kBBytes);
+        tc::cp_sf_atom(t_sfa, tc::desc_sf_atom(ssf));
+#pragma unroll
+        for (int at = 0; at < S::kSfbAtoms; ++at) tc::cp_sf_atom(t_sfb + 4 * at, tc::desc_sf_atom(ssf + 512 * (1 + at)));
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma_mxf8(t_d, tc::desc_k128_sw128(sa + kk * 32), tc::desc_k128_sw128(sb + kk * 32),
+                       tc::idesc_mxf8(BN, kk, kk), t_sfa, t_sfb, (i > 0 || kk > 0) ? 1u : 0u);
+        tc::commit(&empty[s]);
+      }
+      tc::commit(tmem_full);
+    }
+    __syncwarp();
+  } else {
+    // ----------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // the TMEM lane quadrant this warp may read
+    const int r = 32 * q + lane;
+    const bool ok = mbar_wait(tmem_full, 0, a.err);
+    tc::fence_after_sync();
+    const uint32_t trow = t_d + ((uint32_t)(32 * q) << 16);
+    if (EPI == kEpiStore || EPI == kEpiSplit) {
+      const int n = n0 + r;
+      const bool nv = n < a.N;
+      for (int c = 0; c < BN; c += 16) {
+        float v[16];
+        tc::ld16(trow + c, v);
+        tc::wait_ld();
+        if (!ok) continue;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int m = m0 + c + j;
+          if (m < a.M && nv) {
+            if (EPI == kEpiStore) {
+              float y = v[j];
+              if (a.residual) y += __bfloat162float(__ushort_as_bfloat16(a.residual[(int64_t)m * a.N + n]));
+              a.out[(int64_t)m * a.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+            } else {
+              a.partial[((int64_t)split * a.M + m) * a.N + n] = v[j];
+            }
+          }
+        }
+      }
+      if (EPI == kEpiSplit) {
+        __threadfence();
+        epi_bar();
+        const int tile = ntile + gridDim.x * mtile;
+        if (warp == 2 && lane == 0) *last_sh = atomicAdd(&a.counters[tile], 1) == a.splits - 1;
+        epi_bar();
+        if (*last_sh) {
+          __threadfence();
+          for (int c = 0; c < BN; ++c) {
+            const int m = m0 + c;
+            if (m >= a.M || !nv) continue;
+            float y = 0.f;
+            for (int z = 0; z < a.splits; ++z) y += __ldcg(&a.partial[((int64_t)z * a.M + m) * a.N + n]);
+            if (a.residual) y += __bfloat162float(__ushort_as_bfloat16(a.residual[(int64_t)m * a.N + n]));
+            a.out[(int64_t)m * a.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+          }
+          if (warp == 2 && lane == 0) a.counters[tile] = 0;
+        }
+      }
+    } else {
+      // SwiGLU + MXFP8 re-quantisation along d_ff
+      float* stg = reinterpret_cast<float*>(ring);  // [128 tile rows][BN + 1]
+      for (int c = 0; c < BN; c += 16) {
+        float v[16];
+        tc::ld16(trow + c, v);
+        tc::wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) stg[r * (BN + 1) + c + j] = v[j];
+      }
+      epi_bar();
+      if (ok) {
+        const int e = warp - 2, blk = e & 1, half = e >> 1;
+        const int j0 = n0 + 32 * blk;  // d_ff index of lane 0
+        const int tb = half * (BN / 2), te = tb + BN / 2;
+        for (int t = tb; t < te; ++t) {
+          const int m = m0 + t;
+          if (m >= a.M) break;
+          const float g = stg[(32 * blk + lane) * (BN + 1) + t];
+          const float u = stg[(64 + 32 * blk + lane) * (BN + 1) + t];
+          const float h = g / (1.f + expf(-g)) * u;
+          float am = fabsf(h);
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) am = fmaxf(am, __shfl_xor_sync(MXG_FULL_MASK, am, off));
+          const int se = mx_shared_exp(am);
+          a.hq[(int64_t)m * a.d_ff + j0 + lane] = (uint8_t)(cvt_e4m3x2(h * mx_inv_scale(se), 0.f) & 0xFF);
+          if (lane == 0) a.hs[(int64_t)m * (a.d_ff >> 5) + (j0 >> 5)] = (uint8_t)(se + 127);
+        }
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) tc::tmem_dealloc(tmem, S::kTmemCols);
+}
+
+// ---------------------------------------------------------------------------------- host
+namespace {
+
+int pick_bn(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
+
+struct Plan {
+  int bn, ntiles, mtiles, splits;
+};
+
+Plan plan_gemm(int64_t M, int64_t N, int64_t K) {
+  Plan p;
+  p.bn = M > 1024 ? 256 : pick_bn(M);
+  p.ntiles = (int)((N + 127) / 128);
+  p.mtiles = (int)((M + p.bn - 1) / p.bn);
+  const int groups = (int)(K / kKG);
+  const int64_t ctas = (int64_t)p.ntiles * p.mtiles;
+  p.splits = 1;
+  if (ctas < 120) {
+    int s = (int)((152 + ctas / 2) / ctas);
+    if (s > groups) s = groups;
+    if (s > 16) s = 16;
+    p.splits = s < 1 ? 1 : s;
+  }
+  return p;
+}
+
+template <int BN, int EPI>
+cudaError_t launch_tc(const CUtensorMap& tw, const CUtensorMap& tx, const TcArgs& a, dim3 grid, cudaStream_t st) {
+  using S = TcShape<BN>;
+  cudaError_t e = cudaFuncSetAttribute(mx_gemm_tc_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       S::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  mx_gemm_tc_kernel<BN, EPI><<<grid, 192, S::kSmemBytes, st>>>(tw, tx, a);
+  return cudaGetLastError();
+}
+
+template <int EPI>
+cudaError_t launch_tc_bn(int bn, const CUtensorMap& tw, const CUtensorMap& tx, const TcArgs& a, dim3 grid,
+                         cudaStream_t st) {
+  switch (bn) {
+    case 16: return launch_tc<16, EPI>(tw, tx, a, grid, st);
+    case 32: return launch_tc<32, EPI>(tw, tx, a, grid, st);
+    case 64: return launch_tc<64, EPI>(tw, tx, a, grid, st);
+    case 128: return launch_tc<128, EPI>(tw, tx, a, grid, st);
+    default: return launch_tc<256, EPI == kEpiSwiGLU ? kEpiStore : EPI>(tw, tx, a, grid, st);
+  }
+}
+
+bool maps(CUtensorMap* tw, CUtensorMap* tx, const uint8_t* wq, int64_t wrows, const uint8_t* xq, int64_t M, int64_t K,
+          int bn) {
+  return make_tensor_map_2d(tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)K, (uint64_t)wrows, (uint64_t)K, kKG, 64,
+                            CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_tensor_map_2d(tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, (uint64_t)K, (uint64_t)M, (uint64_t)K, kKG,
+                            (uint32_t)bn, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+}  // namespace
+
+bool tc_gemm_supported(int64_t M, int64_t N, int64_t K) {
+  return M > 0 && K % kKG == 0 && N % 8 == 0 && K / kKG >= 1 && M < (1ll << 31) && N < (1ll << 31);
+}
+
+size_t tc_gemm_workspace(int64_t M, int64_t N, int64_t K) {
+  if (!tc_gemm_supported(M, N, K)) return 0;
+  const Plan p = plan_gemm(M, N, K);
+  if (p.splits <= 1) return 0;
+  const size_t part = (size_t)p.splits * (size_t)M * (size_t)N * sizeof(float);
+  return (part + 255) / 256 * 256 + (size_t)p.ntiles * p.mtiles * sizeof(int);
+}
+
+cudaError_t launch_mx_gemm_tc(const uint8_t* xq, const uint8_t* xs, const uint8_t* wq, const uint8_t* ws, int64_t M,
+                              int64_t N, int64_t K, const uint16_t* residual, uint16_t* out, void* workspace,
+                              int32_t* err, cudaStream_t st, bool* unsupported) {
+  const Plan p = plan_gemm(M, N, K);
+  CUtensorMap tw, tx;
+  *unsupported = false;
+  if (!maps(&tw, &tx, wq, N, xq, M, K, p.bn)) {
+    *unsupported = true;
+    return cudaSuccess;
+  }
+  TcArgs a{};
+  a.M = (int)M;
+  a.N = (int)N;
+  a.K = (int)K;
+  a.groups = (int)(K / kKG);
+  a.splits = p.splits;
+  a.ws = ws;
+  a.xs = xs;
+  a.residual = residual;
+  a.out = out;
+  a.err = err;
+  dim3 grid((unsigned)p.ntiles, (unsigned)p.mtiles, (unsigned)p.splits);
+  if (p.splits > 1) {
+    const size_t part = (size_t)p.splits * (size_t)M * (size_t)N * sizeof(float);
+    a.partial = static_cast<float*>(workspace);
+    a.counters = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + (part + 255) / 256 * 256);
+    return launch_tc_bn<kEpiSplit>(p.bn, tw, tx, a, grid, st);
+  }
+  return launch_tc_bn<kEpiStore>(p.bn, tw, tx, a, grid, st);
+}
+
+cudaError_t launch_gate_up_swiglu_tc(const uint8_t* xq, const uint8_t* xs, int64_t M, int64_t d_model, int64_t d_ff,
+                                     const uint8_t* w13q, const uint8_t* w13s, uint8_t* hq, uint8_t* hs, int32_t* err,
+                                     cudaStream_t st, bool* unsupported) {
+  const int bn = pick_bn(M);
+  CUtensorMap tw, tx;
+  *unsupported = false;
+  if (d_model % kKG || d_ff % 64 || !maps(&tw, &tx, w13q, 2 * d_ff, xq, M, d_model, bn)) {
+    *unsupported = true;
+    return cudaSuccess;
+  }
+  TcArgs a{};
+  a.M = (int)M;
+  a.N = (int)(2 * d_ff);
+  a.K = (int)d_model;
+  a.groups = (int)(d_model / kKG);
+  a.splits = 1;
+  a.ws = w13s;
+  a.xs = xs;
+  a.d_ff = (int)d_ff;
+  a.hq = hq;
+  a.hs = hs;
+  a.err = err;
+  dim3 grid((unsigned)(d_ff / 64), (unsigned)((M + bn - 1) / bn), 1);
+  return launch_tc_bn<kEpiSwiGLU>(bn, tw, tx, a, grid, st);
+}
+
+}  // namespace mxg

@@ -31,6 +31,18 @@ cudaError_t launch_gate_up_swiglu_simt(const uint8_t* xq, const uint8_t* xs, int
                                        int64_t d_ff, const uint8_t* w13q, const uint8_t* w13s, uint8_t* hq,
                                        uint8_t* hs, cudaStream_t st);
 
+bool tc_gemm_supported(int64_t M, int64_t N, int64_t K);
+size_t tc_gemm_workspace(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_mx_gemm_tc(const uint8_t* xq, const uint8_t* xs, const uint8_t* wq, const uint8_t* ws, int64_t M,
+                              int64_t N, int64_t K, const uint16_t* residual, uint16_t* out, void* workspace,
+                              int32_t* err, cudaStream_t st, bool* unsupported);
+cudaError_t launch_gate_up_swiglu_tc(const uint8_t* xq, const uint8_t* xs, int64_t M, int64_t d_model, int64_t d_ff,
+                                     const uint8_t* w13q, const uint8_t* w13s, uint8_t* hq, uint8_t* hs, int32_t* err,
+                                     cudaStream_t st, bool* unsupported);
+
+// Kernel-path selection: true unless the caller forced the CUDA-core path.
+bool tensor_core_path_enabled();
+
 // 2-D row-major tensor map (inner dimension first) for TMA; false if the driver refused it.
 bool make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
                         uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz);

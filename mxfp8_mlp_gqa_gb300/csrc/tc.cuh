@@ -1,0 +1,104 @@
+// tcgen05 (5th-generation tensor core) helpers for sm_103a: TMEM allocation, UMMA shared
+// memory / instruction descriptors, block-scaled MMA issue, TMEM loads, scale-factor copies.
+#pragma once
+#include "common.cuh"
+
+namespace mxg {
+namespace tc {
+
+// ------------------------------------------------------------------ TMEM management
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// ------------------------------------------------------------------ descriptors
+// Shared-memory matrix descriptor (tcgen05 form): start address, leading / stride byte
+// offsets (all >> 4), descriptor version 1 at bits 46-47, layout type at bits 61-63
+// (0 = no swizzle, 2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)(layout & 7u) << 61;
+  return d;
+}
+
+// K-major operand tile of 8-bit elements stored by TMA with the 128-byte swizzle: rows of
+// 128 bytes, 8-row groups 1024 bytes apart. `saddr` may be advanced by k*32 bytes inside
+// the 128-byte row to select the k-th 32-element slice (one MMA-K of 8-bit data).
+__device__ __forceinline__ uint64_t desc_k128_sw128(uint32_t saddr) { return smem_desc(saddr, 0, 1024, 2); }
+
+// Scale-factor atom (32 rows x 16 bytes, contiguous, no swizzle) for tcgen05.cp 32x128b.
+__device__ __forceinline__ uint64_t desc_sf_atom(uint32_t saddr) { return smem_desc(saddr, 0, 128, 0); }
+
+// Instruction descriptor of kind::mxf8f6f4 with block scaling: E4M3 A and B (format 0),
+// both K-major, fp32 accumulation, UE8M0 scales (bit 23), M = 128 (M>>4 at bits 24-28),
+// N>>3 at bits 17-22, and the byte of the 32-bit scale word used by this MMA for A
+// (bits 29-30) and B (bits 4-5).
+__host__ __device__ constexpr uint32_t idesc_mxf8(int n, int sfa_id, int sfb_id) {
+  return ((uint32_t)sfb_id << 4) | ((uint32_t)(n >> 3) << 17) | (1u << 23) | ((uint32_t)(128 >> 4) << 24) |
+         ((uint32_t)sfa_id << 29);
+}
+
+// ------------------------------------------------------------------ MMA / copies / commit
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
+// 32 TMEM lanes x 128 bits from a 512-byte scale atom, replicated into all four lane
+// quadrants (warpx4).
+__device__ __forceinline__ void cp_sf_atom(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Arrive on an mbarrier once every tcgen05 operation this thread issued so far is complete.
+__device__ __forceinline__ void commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Each thread of the warp reads its TMEM lane (quadrant of the warp), 16 / 32 consecutive
+// 32-bit columns starting at the column of taddr.
+__device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// cp.async of 4 bytes global -> shared (generic proxy), tracked by a later mbarrier arrive.
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+// The mbarrier receives one arrival when all of this thread's prior cp.async are done
+// (the arrival is counted in the barrier's expected count, not added to it).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+}  // namespace tc
+}  // namespace mxg

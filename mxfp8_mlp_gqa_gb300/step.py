@@ -58,7 +58,10 @@ class DecodeLayer:
         self.hq_in, self.hs_in = e((bs, d_model), u8), e((bs, d_model // 32), u8)
         self.y = e((bs, d_model), bf)
         self.ws_attn = e((max(1, api.gqa_decode_attn_workspace(bs, Hq, Hkv, D, max_kv_len)),), u8)
-        self.ws_mlp = e((api.mlp_swiglu_mxfp8_workspace(bs, d_model, d_ff),), u8)
+        self.ws_mlp = torch.zeros((api.mlp_swiglu_mxfp8_workspace(bs, d_model, d_ff),), dtype=u8, device=dev)
+        nqkv_ws = api.mxfp8_gemm_workspace(bs, nqkv, d_model)
+        self.ws_qkv = torch.zeros((max(1, nqkv_ws),), dtype=u8, device=dev)
+        self.ws_o = torch.zeros((max(1, api.mxfp8_gemm_workspace(bs, d_model, Hq * D)),), dtype=u8, device=dev)
         self.graph = None
 
     def load_weights(self, wqkv_bf16, wo_bf16, w13_bf16, w2_bf16, gamma1, gamma2):
@@ -71,14 +74,14 @@ class DecodeLayer:
     def step(self):
         Hq, Hkv, D = self.Hq, self.Hkv, self.D
         api.rmsnorm_mxfp8_quantize(self.x, self.gamma1, self.eps, q=self.xq, s=self.xs)
-        api.mxfp8_gemm(self.xq, self.xs, *self.wqkv, c=self.qkv)
+        api.mxfp8_gemm(self.xq, self.xs, *self.wqkv, c=self.qkv, workspace=self.ws_qkv)
         qd, kd = Hq * D, Hkv * D
         api.kv_append(self.k_cache, self.v_cache, self.qkv[:, qd:qd + kd], self.qkv[:, qd + kd:], self.kv_len,
                       err=self.err)
         api.gqa_decode_attn(self.qkv[:, :qd], self.k_cache, self.v_cache, self.kv_len, self.max_kv_len, self.scale,
                             out=self.o, err=self.err, workspace=self.ws_attn)
         api.mxfp8_quantize(self.o.view(self.bs, qd), q=self.oq, s=self.os)
-        api.mxfp8_gemm(self.oq, self.os, *self.wo, residual=self.x, c=self.x1)
+        api.mxfp8_gemm(self.oq, self.os, *self.wo, residual=self.x, c=self.x1, workspace=self.ws_o)
         api.rmsnorm_mxfp8_quantize(self.x1, self.gamma2, self.eps, q=self.hq_in, s=self.hs_in)
         api.mlp_swiglu_mxfp8(self.hq_in, self.hs_in, *self.w13, *self.w2, residual=self.x1, y=self.y,
                              workspace=self.ws_mlp)
