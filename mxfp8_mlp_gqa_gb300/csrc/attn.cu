@@ -13,7 +13,8 @@
 //    64-token K and V tiles, with mbarrier full/empty handshakes (bounded waits);
 //  * four consumer warps, 16 tokens each per tile, compute S^T = K Q^T and O^T += V^T P^T
 //    with m16n8k16 bf16 tensor-core tiles (tokens x heads, heads padded to 8), fp32
-//    online softmax in base 2, P rounded to bf16 and l summed from the rounded P;
+//    online softmax in base 2; P enters the PV product as a bf16 pair hi + lo (two MMAs on
+//    the same V fragments), so the weights keep ~16 significant bits instead of 8;
 //  * the CTA merges its 4 warps and writes (O/l, log2-sum-exp) per head; a small combine
 //    kernel merges the splits of each (b, h). With a single split the CTA writes bf16 out.
 // Grid size is fixed by a host bound on kv_len, so the call is graph-capturable; CTAs whose
@@ -38,7 +39,7 @@ struct AttnShape {
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kMergeBytes = kConsumers * 8 * D * 4 + kConsumers * 8 * 2 * 4;
   static constexpr int kBodyBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
-  static constexpr int kPBytes = kConsumers * 8 * 16 * 2;  // per-warp P^T staging (bf16 [8][16])
+  static constexpr int kPBytes = kConsumers * 2 * 8 * 16 * 2;  // per-warp P^T staging, hi and lo (bf16 [8][16])
   static constexpr int kSmemBytes = 1024 + kBodyBytes + kPBytes + 2 * kStages * 8;
 };
 
@@ -153,7 +154,8 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
 #pragma unroll
   for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
-  uint16_t* ps = pstage + warp * (8 * 16);  // P^T staging: [8 heads][16 tokens]
+  uint16_t* ps = pstage + warp * (2 * 8 * 16);  // P^T staging: hi [8 heads][16 tokens], then lo
+  uint16_t* pl = ps + 8 * 16;
   const int r0 = warp * 16;
   bool ok = true;
   for (int i = 0; i < ntiles; ++i) {
@@ -188,12 +190,15 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
     const float alpha_a = exp2f(m_a - ua), alpha_b = exp2f(m_b - ub);
     m_a = na;
     m_b = nb;
-    const __nv_bfloat16 p0 = __float2bfloat16_rn(exp2f(x0 - ua));
-    const __nv_bfloat16 p1 = __float2bfloat16_rn(exp2f(x1 - ub));
-    const __nv_bfloat16 p2 = __float2bfloat16_rn(exp2f(x2 - ua));
-    const __nv_bfloat16 p3 = __float2bfloat16_rn(exp2f(x3 - ub));
-    l_a = l_a * alpha_a + (__bfloat162float(p0) + __bfloat162float(p2));
-    l_b = l_b * alpha_b + (__bfloat162float(p1) + __bfloat162float(p3));
+    const float f0 = exp2f(x0 - ua), f1 = exp2f(x1 - ub), f2 = exp2f(x2 - ua), f3 = exp2f(x3 - ub);
+    const __nv_bfloat16 p0 = __float2bfloat16_rn(f0), p1 = __float2bfloat16_rn(f1);
+    const __nv_bfloat16 p2 = __float2bfloat16_rn(f2), p3 = __float2bfloat16_rn(f3);
+    const __nv_bfloat16 q0 = __float2bfloat16_rn(f0 - __bfloat162float(p0));
+    const __nv_bfloat16 q1 = __float2bfloat16_rn(f1 - __bfloat162float(p1));
+    const __nv_bfloat16 q2 = __float2bfloat16_rn(f2 - __bfloat162float(p2));
+    const __nv_bfloat16 q3 = __float2bfloat16_rn(f3 - __bfloat162float(p3));
+    l_a = l_a * alpha_a + (f0 + f2);
+    l_b = l_b * alpha_b + (f1 + f3);
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) {
       o[mt][0] *= alpha_a;
@@ -205,6 +210,10 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
     ps[(2 * c4 + 1) * 16 + r4] = __bfloat16_as_ushort(p1);
     ps[(2 * c4) * 16 + r4 + 8] = __bfloat16_as_ushort(p2);
     ps[(2 * c4 + 1) * 16 + r4 + 8] = __bfloat16_as_ushort(p3);
+    pl[(2 * c4) * 16 + r4] = __bfloat16_as_ushort(q0);
+    pl[(2 * c4 + 1) * 16 + r4] = __bfloat16_as_ushort(q1);
+    pl[(2 * c4) * 16 + r4 + 8] = __bfloat16_as_ushort(q2);
+    pl[(2 * c4 + 1) * 16 + r4 + 8] = __bfloat16_as_ushort(q3);
     // rows past the split end may hold anything; P is 0 there, and V is zeroed so that a
     // non-finite value cannot turn 0 * V into NaN
     if (tb + 16 > t1) {
@@ -224,6 +233,8 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
     __syncwarp();
     const uint32_t b0 = *reinterpret_cast<const uint32_t*>(ps + r4 * 16 + 2 * c4);
     const uint32_t b1 = *reinterpret_cast<const uint32_t*>(ps + r4 * 16 + 8 + 2 * c4);
+    const uint32_t l0 = *reinterpret_cast<const uint32_t*>(pl + r4 * 16 + 2 * c4);
+    const uint32_t l1 = *reinterpret_cast<const uint32_t*>(pl + r4 * 16 + 8 + 2 * c4);
     // O^T[D x 8] += V^T[D x 16 tok] P^T[16 tok x 8]
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) {
@@ -231,6 +242,7 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
       ldmatrix_x4_trans(tile_addr(vbase, r0 + (lane & 7) + 8 * (lane >> 4), mt * 16 + 8 * ((lane >> 3) & 1)), a0, a1,
                         a2, a3);
       mma_bf16_16816(o[mt], a0, a1, a2, a3, b0, b1);
+      mma_bf16_16816(o[mt], a0, a1, a2, a3, l0, l1);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);

@@ -16,8 +16,11 @@
 //           instruction descriptor), then tcgen05.commit frees the stage;
 //   warps 2-5 epilogue: read D^T from TMEM (each warp its lane quadrant) and
 //           * kEpiStore : write bf16 out (+ bf16 residual),
-//           * kEpiSplit : write fp32 partials of a K split; the last split of a tile sums
-//                         all splits in a fixed order (+ residual) and writes bf16,
+//           * kEpiSplit : split-K over a thread-block cluster of S CTAs (grid.z = S): every
+//                         CTA stages its fp32 partial tile in shared memory, and after a
+//                         cluster barrier CTA z sums rows [z*128/S, (z+1)*128/S) of all S
+//                         partials through distributed shared memory in a fixed order
+//                         (+ residual) and writes bf16 -- deterministic, no global scratch,
 //           * kEpiSwiGLU: the weight tile is 64 gate rows + the matching 64 up rows; h =
 //                         silu(g) * u in fp32, re-quantised to MXFP8 along d_ff in the
 //                         epilogue (no bf16 h is ever written).
@@ -63,12 +66,24 @@ struct TcArgs {
   uint8_t* hs;
   const uint16_t* residual;
   uint16_t* out;
-  float* partial;       // [splits][M][N]
-  int* counters;        // one per (n tile, m tile); zero between calls
   int32_t* err;
 };
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// fp32 load from the shared memory of CTA `rank` of this cluster, at the offset that `local`
+// has in this CTA's shared memory.
+__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
+  uint32_t raddr;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(smem_u32(local)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(raddr) : "memory");
+  return v;
+}
 
 }  // namespace
 
@@ -83,7 +98,6 @@ __global__ void __launch_bounds__(192, 1) mx_gemm_tc_kernel(const __grid_constan
   uint64_t* empty = full + S::kStages;
   uint64_t* tmem_full = empty + S::kStages;
   uint32_t* tmem_sh = reinterpret_cast<uint32_t*>(tmem_full + 1);
-  int* last_sh = reinterpret_cast<int*>(tmem_sh + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntile = blockIdx.x, mtile = blockIdx.y, split = blockIdx.z;
@@ -180,7 +194,7 @@ __global__ void __launch_bounds__(192, 1) mx_gemm_tc_kernel(const __grid_constan
     const bool ok = mbar_wait(tmem_full, 0, a.err);
     tc::fence_after_sync();
     const uint32_t trow = t_d + ((uint32_t)(32 * q) << 16);
-    if (EPI == kEpiStore || EPI == kEpiSplit) {
+    if (EPI == kEpiStore) {
       const int n = n0 + r;
       const bool nv = n < a.N;
       for (int c = 0; c < BN; c += 16) {
@@ -192,34 +206,21 @@ __global__ void __launch_bounds__(192, 1) mx_gemm_tc_kernel(const __grid_constan
         for (int j = 0; j < 16; ++j) {
           const int m = m0 + c + j;
           if (m < a.M && nv) {
-            if (EPI == kEpiStore) {
-              float y = v[j];
-              if (a.residual) y += __bfloat162float(__ushort_as_bfloat16(a.residual[(int64_t)m * a.N + n]));
-              a.out[(int64_t)m * a.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
-            } else {
-              a.partial[((int64_t)split * a.M + m) * a.N + n] = v[j];
-            }
-          }
-        }
-      }
-      if (EPI == kEpiSplit) {
-        __threadfence();
-        epi_bar();
-        const int tile = ntile + gridDim.x * mtile;
-        if (warp == 2 && lane == 0) *last_sh = atomicAdd(&a.counters[tile], 1) == a.splits - 1;
-        epi_bar();
-        if (*last_sh) {
-          __threadfence();
-          for (int c = 0; c < BN; ++c) {
-            const int m = m0 + c;
-            if (m >= a.M || !nv) continue;
-            float y = 0.f;
-            for (int z = 0; z < a.splits; ++z) y += __ldcg(&a.partial[((int64_t)z * a.M + m) * a.N + n]);
+            float y = v[j];
             if (a.residual) y += __bfloat162float(__ushort_as_bfloat16(a.residual[(int64_t)m * a.N + n]));
             a.out[(int64_t)m * a.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
           }
-          if (warp == 2 && lane == 0) a.counters[tile] = 0;
         }
+      }
+    } else if (EPI == kEpiSplit) {
+      // stage this CTA's partial tile; the cluster reduction below reads it remotely
+      float* stg = reinterpret_cast<float*>(ring);  // [128 tile rows][BN + 1]
+      for (int c = 0; c < BN; c += 16) {
+        float v[16];
+        tc::ld16(trow + c, v);
+        tc::wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) stg[r * (BN + 1) + c + j] = v[j];
       }
     } else {
       // SwiGLU + MXFP8 re-quantisation along d_ff
@@ -252,6 +253,24 @@ __global__ void __launch_bounds__(192, 1) mx_gemm_tc_kernel(const __grid_constan
       }
     }
   }
+  if (EPI == kEpiSplit) {
+    cluster_sync_all();  // every CTA of the cluster has staged its partial tile
+    if (warp >= 2) {
+      const int S_ = a.splits;
+      const int rb = split * 128 / S_, re = (split + 1) * 128 / S_, nr = re - rb;
+      const float* stg = reinterpret_cast<const float*>(ring);
+      for (int e = threadIdx.x - 64; e < nr * BN; e += 128) {
+        const int rr = rb + e % nr, c = e / nr;
+        const int n = n0 + rr, m = m0 + c;
+        if (n >= a.N || m >= a.M) continue;
+        float y = 0.f;
+        for (int z = 0; z < S_; ++z) y += ld_dsmem_f32(&stg[rr * (BN + 1) + c], (uint32_t)z);
+        if (a.residual) y += __bfloat162float(__ushort_as_bfloat16(a.residual[(int64_t)m * a.N + n]));
+        a.out[(int64_t)m * a.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+      }
+    }
+    cluster_sync_all();  // keep this CTA's shared memory alive until every reader is done
+  }
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, S::kTmemCols);
@@ -277,7 +296,7 @@ Plan plan_gemm(int64_t M, int64_t N, int64_t K) {
   if (ctas < 120) {
     int s = (int)((152 + ctas / 2) / ctas);
     if (s > groups) s = groups;
-    if (s > 16) s = 16;
+    if (s > 8) s = 8;  // one thread-block cluster (portable size) per tile
     p.splits = s < 1 ? 1 : s;
   }
   return p;
@@ -289,6 +308,23 @@ cudaError_t launch_tc(const CUtensorMap& tw, const CUtensorMap& tx, const TcArgs
   cudaError_t e = cudaFuncSetAttribute(mx_gemm_tc_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        S::kSmemBytes);
   if (e != cudaSuccess) return e;
+  if (EPI == kEpiSplit) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(192, 1, 1);
+    cfg.dynamicSmemBytes = S::kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = grid.z;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, mx_gemm_tc_kernel<BN, EPI>, tw, tx, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
   mx_gemm_tc_kernel<BN, EPI><<<grid, 192, S::kSmemBytes, st>>>(tw, tx, a);
   return cudaGetLastError();
 }
@@ -320,11 +356,8 @@ bool tc_gemm_supported(int64_t M, int64_t N, int64_t K) {
 }
 
 size_t tc_gemm_workspace(int64_t M, int64_t N, int64_t K) {
-  if (!tc_gemm_supported(M, N, K)) return 0;
-  const Plan p = plan_gemm(M, N, K);
-  if (p.splits <= 1) return 0;
-  const size_t part = (size_t)p.splits * (size_t)M * (size_t)N * sizeof(float);
-  return (part + 255) / 256 * 256 + (size_t)p.ntiles * p.mtiles * sizeof(int);
+  (void)M; (void)N; (void)K;
+  return 0;  // split-K partials are reduced inside a cluster through distributed shared memory
 }
 
 cudaError_t launch_mx_gemm_tc(const uint8_t* xq, const uint8_t* xs, const uint8_t* wq, const uint8_t* ws, int64_t M,
@@ -349,12 +382,8 @@ cudaError_t launch_mx_gemm_tc(const uint8_t* xq, const uint8_t* xs, const uint8_
   a.out = out;
   a.err = err;
   dim3 grid((unsigned)p.ntiles, (unsigned)p.mtiles, (unsigned)p.splits);
-  if (p.splits > 1) {
-    const size_t part = (size_t)p.splits * (size_t)M * (size_t)N * sizeof(float);
-    a.partial = static_cast<float*>(workspace);
-    a.counters = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + (part + 255) / 256 * 256);
-    return launch_tc_bn<kEpiSplit>(p.bn, tw, tx, a, grid, st);
-  }
+  (void)workspace;
+  if (p.splits > 1) return launch_tc_bn<kEpiSplit>(p.bn, tw, tx, a, grid, st);
   return launch_tc_bn<kEpiStore>(p.bn, tw, tx, a, grid, st);
 }
 

@@ -57,7 +57,7 @@ def test_qwen3_4b_shape(M):
     assert_float_close(y, ref["y"])
 
 
-@pytest.mark.parametrize("M", [3, 77])
+@pytest.mark.parametrize("M", [3, 64, 77])
 def test_ragged_m_with_residual(M):
     hq, hs, y, ref = _mlp_case(M, 2560, 9728, residual=True, seed=1)
     assert_requant_close(hq, hs, ref["hq"], ref["hs"])

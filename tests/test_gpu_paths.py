@@ -37,7 +37,11 @@ def test_gemm_structured_scales(path, M, N, K):
     d = lambda a: torch.from_numpy(a).cuda()  # noqa: E731
     c = api.mxfp8_gemm(d(xq), d(xs), d(wq), d(ws), residual=dev_bf16(res))
     ref = ops.mx_gemm(xq, xs, wq, ws) + mx.bf16_to_f64(res)
-    assert_float_close(host_f64(c), ref)
+    # per-block scales spanning 2^-17..2^11 make the outputs heavy-tailed, so the bound on
+    # the largest error is taken against max |ref| (bf16 output rounding is 2^-9 of that)
+    got = host_f64(c)
+    assert np.linalg.norm(got - ref) <= 1e-2 * np.linalg.norm(ref)
+    assert np.abs(got - ref).max() <= 1e-2 * np.abs(ref).max()
 
 
 @pytest.mark.parametrize("M", [1, 5, 33, 128, 130])
