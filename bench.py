@@ -254,27 +254,44 @@ def run_ours(args, rank, local_rank, world):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     peak_gbs, peak_src = measured_peaks()
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(10)] for _ in range(args.steps)]
+    # one eager step (lazy initialisation), then the step is captured in a CUDA graph with a
+    # timing event between consecutive kernels, so that per-kernel times are device times
+    # without host enqueue gaps
+    L.kv_len.copy_(sched_d[0])
+    L.step()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(10)]
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            timed_ops(L, evs)
+    torch.cuda.current_stream().wait_stream(cap)
     for s in range(args.warmup):
         L.kv_len.copy_(sched_d[s])
-        L.step()
+        graph.replay()
     torch.cuda.synchronize()
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
+    per_op = {n: [] for n in OP_NAMES}
+    step_ms = []
     for i in range(args.steps):
         L.kv_len.copy_(sched_d[args.warmup + i])   # schedule advance (retire/refill), not timed
         flush.zero_()                               # L2 flush, not timed
-        timed_ops(L, ev[i])
+        graph.replay()
+        evs[9].synchronize()
+        for k, n in enumerate(OP_NAMES):
+            per_op[n].append(evs[k].elapsed_time(evs[k + 1]))
+        step_ms.append(evs[0].elapsed_time(evs[9]))
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
     assert int(L.err.item()) == 0, f"device error flag {int(L.err.item())}"
 
-    per_op = {n: [ev[i][k].elapsed_time(ev[i][k + 1]) for i in range(args.steps)] for k, n in enumerate(OP_NAMES)}
-    step_ms = [ev[i][0].elapsed_time(ev[i][9]) for i in range(args.steps)]
     tot_ms = max_over_ranks(sum(step_ms), world, dev)
     bytes_steps = [step_bytes(sched[args.warmup + i]) for i in range(args.steps)]
     tot_bytes = sum(sum(b.values()) for b in bytes_steps)
@@ -287,7 +304,8 @@ def run_ours(args, rank, local_rank, world):
         by = statistics.mean(b[n] for b in bytes_steps)
         breakdown[n] = {"us": round(ms * 1e3, 2), "GB_s": round(by / (ms * 1e-3) / 1e9, 1), "bytes": int(by)}
 
-    # e2e through the public API with host buffers: H2D inputs, the step, D2H of y
+    # e2e through the public API with host buffers: H2D of this step's inputs, the captured
+    # step, D2H of y, every step
     x_h = torch.empty((BS, D_MODEL), dtype=torch.bfloat16, pin_memory=True)
     x_h.copy_(L.x.cpu())
     nxt_h = torch.empty((BS, CW), dtype=torch.int32, pin_memory=True)
@@ -302,7 +320,7 @@ def run_ours(args, rank, local_rank, world):
         L.x.copy_(x_h, non_blocking=True)
         L.next_tokens.copy_(nxt_h, non_blocking=True)
         L.kv_len.copy_(lens_h[args.warmup + i], non_blocking=True)
-        L.step()
+        graph.replay()
         y_h.copy_(L.y, non_blocking=True)
         e1.record()
         e1.synchronize()
@@ -313,15 +331,13 @@ def run_ours(args, rank, local_rank, world):
     e2e = {"value": round(world * tot_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / args.steps, 4)}
 
-    # CUDA-graph replay of the same step (context: launch gaps removed)
-    L.kv_len.copy_(sched_d[0])
-    L.capture()
+    # eager (uncaptured) launches of the same step, for context: includes host enqueue time
     g_ms = []
     for i in range(args.steps):
         L.kv_len.copy_(sched_d[args.warmup + i])
         flush.zero_()
         e0.record()
-        L.replay()
+        L.step()
         e1.record()
         e1.synchronize()
         g_ms.append(e0.elapsed_time(e1))
@@ -329,7 +345,7 @@ def run_ours(args, rank, local_rank, world):
     sweeps = {} if args.no_sweeps else run_sweeps(dev, flush)
     return {
         "value": value, "ms_per_step": tot_ms / args.steps, "clocks": clk, "breakdown": breakdown, "e2e": e2e,
-        "graph_ms_per_step": statistics.mean(g_ms),
+        "eager_ms_per_step": statistics.mean(g_ms),
         "roofline": {"kernel": "gqa_split_kernel (+combine)", "bound": "hbm",
                      "achieved": round(attn_bytes_avg / (attn_ms * 1e-3) / 1e9, 1), "peak": peak_gbs,
                      "peak_source": peak_src, "unit": "GB/s",
@@ -393,6 +409,50 @@ def run_sweeps(dev, flush):
                       flush)
         attn[str(bs)] = {"us": round(ms * 1e3, 2), "GB_s": round(attn_bytes(lens) / (ms * 1e-3) / 1e9, 1)}
     return {"mlp_M": mlp, "attn_bs": attn}
+
+
+def run_profile(args):
+    """W + K launches of one entry point on synthetic device inputs (small ncu captures)."""
+    import torch
+
+    from mxfp8_mlp_gqa_gb300 import api, synth
+
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(2)
+    rn = lambda shape, std=1.0: (torch.randn(shape, generator=g, device=dev) * std).to(torch.bfloat16)  # noqa: E731
+    kind, _, arg = args.profile.partition(":")
+    if kind == "mlp":
+        M = int(arg)
+        w13 = api.mxfp8_quantize(rn((2 * D_FF, D_MODEL), 0.02))
+        w2 = api.mxfp8_quantize(rn((D_MODEL, D_FF), 0.02))
+        xq, xs = api.mxfp8_quantize(rn((M, D_MODEL)))
+        ws = torch.zeros(api.mlp_swiglu_mxfp8_workspace(M, D_MODEL, D_FF), dtype=torch.uint8, device=dev)
+        y = torch.empty((M, D_MODEL), dtype=torch.bfloat16, device=dev)
+        fn = lambda: api.mlp_swiglu_mxfp8(xq, xs, *w13, *w2, y=y, workspace=ws)  # noqa: E731
+    elif kind == "attn":
+        bs = int(arg)
+        K = torch.empty((bs, HKV, CAP, HD), dtype=torch.bfloat16, device=dev)
+        V = torch.empty_like(K)
+        for b in range(bs):
+            K[b].copy_(rn(K[b].shape))
+            V[b].copy_(rn(V[b].shape))
+        kl = torch.from_numpy(synth.kv_lens(bs, KV_LO, KV_HI, seed=0)).to(dev)
+        q = rn((bs, HQ, HD))
+        ws = torch.empty(max(1, api.gqa_decode_attn_workspace(bs, HQ, HKV, HD, KV_HI)), dtype=torch.uint8, device=dev)
+        out = torch.empty((bs, HQ, HD), dtype=torch.bfloat16, device=dev)
+        fn = lambda: api.gqa_decode_attn(q, K, V, kl, KV_HI, 1 / math.sqrt(HD), out=out, workspace=ws)  # noqa: E731
+    elif kind == "gemm":
+        M, N, K_ = (int(v) for v in arg.split("x"))
+        aq, as_ = api.mxfp8_quantize(rn((M, K_)))
+        bq, bs_ = api.mxfp8_quantize(rn((N, K_)))
+        c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        fn = lambda: api.mxfp8_gemm(aq, as_, bq, bs_, c=c)  # noqa: E731
+    else:
+        raise SystemExit(f"unknown --profile {args.profile}")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    ms = _time_op(fn, flush, reps=args.steps, warm=args.warmup)
+    return {"profile": args.profile, "median_us": round(ms * 1e3, 2)}
 
 
 # --------------------------------------------------------------------------- oracle (CPU) arm
@@ -501,6 +561,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sweeps", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", default=None,
+                    help="run one kernel family only (for ncu captures): mlp:<M> | attn:<bs> | gemm:<M>x<N>x<K>")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -514,6 +576,9 @@ def main(argv=None):
 
     import torch
 
+    if args.profile:
+        print(json.dumps(run_profile(args)))
+        return 0
     if world > 1:
         import torch.distributed as dist
 
@@ -530,9 +595,10 @@ def main(argv=None):
             "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8+bf16", "data": "synthetic",
             "config": {"workload": WORKLOAD, "global_batch": BS * world, "parallelism": f"replicas x{world}",
                        "l2": "flushed between timed steps (256 MiB write outside the events); step footprint "
-                             "~0.68 GB > 129 MB L2", "timing": "per-step CUDA events on the launching stream"},
+                             "~0.68 GB > 129 MB L2", "timing": "step captured in a CUDA graph with timing events between kernels (device times "
+                                           "on the launching stream); per-step replays"},
             "e2e": res["e2e"], "roofline": res["roofline"], "cpu_baseline": cpu, "clocks": res["clocks"],
-            "gpu_launches": res["gpu_launches"], "graph_ms_per_step": round(res["graph_ms_per_step"], 4),
+            "gpu_launches": res["gpu_launches"], "eager_ms_per_step": round(res["eager_ms_per_step"], 4),
             "breakdown": res["breakdown"], "sweeps": res["sweeps"],
         }
         print(json.dumps(line))

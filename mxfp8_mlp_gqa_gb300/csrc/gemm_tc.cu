@@ -45,7 +45,9 @@ struct TcShape {
   static constexpr int kStagesRaw = (BN >= 256 ? 200 * 1024 : 104 * 1024) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 8 ? 8 : (kStagesRaw < 2 ? 2 : kStagesRaw);
   static constexpr int kRingBytes = kStages * kStageBytes;
-  static constexpr int kStagingBytes = 128 * (BN + 1) * 4;
+  static constexpr int kRS = 128 + 4;  // split-K staging [BN][kRS] (column-major, 16-byte rows)
+  static constexpr int kStagingBytes =
+      128 * (BN + 1) * 4 > BN * kRS * 4 ? 128 * (BN + 1) * 4 : BN * kRS * 4;  // max(SwiGLU, split-K)
   static constexpr int kBodyBytes = kRingBytes > kStagingBytes ? kRingBytes : kStagingBytes;
   static constexpr int kSmemBytes = 1024 + kBodyBytes + 8 * (2 * kStages + 1) + 16;
   static constexpr uint32_t kTmemCols = BN + 4 * (1 + kSfbAtoms) <= 32    ? 32
@@ -75,13 +77,16 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// fp32 load from the shared memory of CTA `rank` of this cluster, at the offset that `local`
-// has in this CTA's shared memory.
-__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
+// 4 x fp32 from the shared memory of CTA `rank` of this cluster, at the offset that `local`
+// (16-byte aligned) has in this CTA's shared memory.
+__device__ __forceinline__ float4 ld_dsmem_f32x4(const float* local, uint32_t rank) {
   uint32_t raddr;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(smem_u32(local)), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(raddr) : "memory");
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(raddr)
+               : "memory");
   return v;
 }
 
@@ -213,14 +218,15 @@ __global__ void __launch_bounds__(192, 1) mx_gemm_tc_kernel(const __grid_constan
         }
       }
     } else if (EPI == kEpiSplit) {
-      // stage this CTA's partial tile; the cluster reduction below reads it remotely
-      float* stg = reinterpret_cast<float*>(ring);  // [128 tile rows][BN + 1]
+      // stage this CTA's partial tile (column-major: rows contiguous); the cluster reduction
+      // below reads it remotely
+      float* stg = reinterpret_cast<float*>(ring);  // [BN tokens][kRS]
       for (int c = 0; c < BN; c += 16) {
         float v[16];
         tc::ld16(trow + c, v);
         tc::wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) stg[r * (BN + 1) + c + j] = v[j];
+        for (int j = 0; j < 16; ++j) stg[(c + j) * S::kRS + r] = v[j];
       }
     } else {
       // SwiGLU + MXFP8 re-quantisation along d_ff
@@ -256,17 +262,41 @@ __global__ void __launch_bounds__(192, 1) mx_gemm_tc_kernel(const __grid_constan
   if (EPI == kEpiSplit) {
     cluster_sync_all();  // every CTA of the cluster has staged its partial tile
     if (warp >= 2) {
+      // CTA z of the cluster owns tile rows [z*128/S, (z+1)*128/S) (S is a power of two <= 8)
       const int S_ = a.splits;
-      const int rb = split * 128 / S_, re = (split + 1) * 128 / S_, nr = re - rb;
+      const int nr = 128 / S_, rb = split * nr, nq = nr / 4;
       const float* stg = reinterpret_cast<const float*>(ring);
-      for (int e = threadIdx.x - 64; e < nr * BN; e += 128) {
-        const int rr = rb + e % nr, c = e / nr;
-        const int n = n0 + rr, m = m0 + c;
-        if (n >= a.N || m >= a.M) continue;
-        float y = 0.f;
-        for (int z = 0; z < S_; ++z) y += ld_dsmem_f32(&stg[rr * (BN + 1) + c], (uint32_t)z);
-        if (a.residual) y += __bfloat162float(__ushort_as_bfloat16(a.residual[(int64_t)m * a.N + n]));
-        a.out[(int64_t)m * a.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+      for (int e = threadIdx.x - 64; e < BN * nq; e += 128) {
+        const int c = e / nq, rr = rb + 4 * (e - c * nq);
+        const int m = m0 + c, n = n0 + rr;
+        if (m >= a.M || n >= a.N) continue;
+        float4 part[8];
+#pragma unroll
+        for (int z = 0; z < 8; ++z)
+          if (z < S_) part[z] = ld_dsmem_f32x4(&stg[c * S::kRS + rr], (uint32_t)z);
+        float4 y = part[0];
+#pragma unroll
+        for (int z = 1; z < 8; ++z)
+          if (z < S_) {
+            y.x += part[z].x;
+            y.y += part[z].y;
+            y.z += part[z].z;
+            y.w += part[z].w;
+          }
+        const int64_t o = (int64_t)m * a.N + n;
+        if (a.residual) {
+          const uint2 rv = *reinterpret_cast<const uint2*>(a.residual + o);
+          y.x += bf16_lo(rv.x);
+          y.y += bf16_hi(rv.x);
+          y.z += bf16_lo(rv.y);
+          y.w += bf16_hi(rv.y);
+        }
+        uint2 ov;
+        ov.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.x)) |
+               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.y)) << 16);
+        ov.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.z)) |
+               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.w)) << 16);
+        *reinterpret_cast<uint2*>(a.out + o) = ov;
       }
     }
     cluster_sync_all();  // keep this CTA's shared memory alive until every reader is done
@@ -292,12 +322,14 @@ Plan plan_gemm(int64_t M, int64_t N, int64_t K) {
   p.mtiles = (int)((M + p.bn - 1) / p.bn);
   const int groups = (int)(K / kKG);
   const int64_t ctas = (int64_t)p.ntiles * p.mtiles;
+  // split K over a cluster (power of two <= 8, the portable cluster size) when the tiles
+  // alone cannot cover the 152 SMs; N % 4 == 0 keeps the 4-wide reduction stores aligned
   p.splits = 1;
-  if (ctas < 120) {
-    int s = (int)((152 + ctas / 2) / ctas);
-    if (s > groups) s = groups;
-    if (s > 8) s = 8;  // one thread-block cluster (portable size) per tile
-    p.splits = s < 1 ? 1 : s;
+  if (ctas < 120 && N % 4 == 0) {
+    const double want = 152.0 / (double)ctas;
+    int s = 1;
+    while (s < 8 && 2 * s <= groups && (double)(2 * s) <= 1.5 * want) s *= 2;
+    p.splits = s;
   }
   return p;
 }

@@ -60,17 +60,16 @@ def test_mlp_both_paths(path, M):
     assert_float_close(host_f64(y), ref["y"])
 
 
-def test_split_k_workspace_is_reusable():
-    # the split-K tile counters are reset by the kernel: back-to-back calls on one workspace agree
+def test_split_k_cluster_reduction_is_deterministic():
+    # split-K partials are summed inside a thread-block cluster in a fixed order: repeated
+    # calls give identical bits, and no workspace is needed
     M, N, K = 8, 1024, 4096
     g = synth.rng(3, 3)
     xq, wq = _codes((M, K), g), _codes((N, K), g)
     xs = np.full((M, K // 32), 124, np.uint8)
     ws = np.full((N, K // 32), 125, np.uint8)
     d = lambda a: torch.from_numpy(a).cuda()  # noqa: E731
-    need = api.mxfp8_gemm_workspace(M, N, K)
-    assert need > 0
-    wsb = torch.zeros(need, dtype=torch.uint8, device="cuda")
-    outs = [api.mxfp8_gemm(d(xq), d(xs), d(wq), d(ws), workspace=wsb).clone() for _ in range(3)]
+    assert api.mxfp8_gemm_workspace(M, N, K) == 0
+    outs = [api.mxfp8_gemm(d(xq), d(xs), d(wq), d(ws)).clone() for _ in range(3)]
     assert all(torch.equal(outs[0].view(torch.int16), o.view(torch.int16)) for o in outs[1:])
     assert_float_close(host_f64(outs[0]), ops.mx_gemm(xq, xs, wq, ws))
