@@ -21,6 +21,7 @@
 // split starts past kv_len exit at once.
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace mxg {
 
@@ -85,6 +86,8 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBodyBytes + S::kPBytes);
   uint64_t* empty = full + S::kStages;
 
+  pdl_trigger();
+  pdl_wait();
   const int split = blockIdx.x;
   const int bg = blockIdx.y;
   const int b = bg / p.Hkv, g = bg - b * p.Hkv;
@@ -305,6 +308,8 @@ __global__ void __launch_bounds__(D) gqa_combine_kernel(const float* __restrict_
                                                         const int32_t* __restrict__ kv_len, int Hq, int64_t cap,
                                                         int chunk, int max_splits, int max_kv_len,
                                                         uint16_t* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t bh = blockIdx.x;
   const int b = (int)(bh / Hq);
   const int d = threadIdx.x;
@@ -371,22 +376,21 @@ cudaError_t launch_gqa_decode_attn(const CUtensorMap& tmK, const CUtensorMap& tm
     const int smem = AttnShape<128>::kSmemBytes;
     e = cudaFuncSetAttribute(gqa_split_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    gqa_split_kernel<128><<<grid, kThreads, smem, st>>>(tmK, tmV, p);
+    e = launch_k(gqa_split_kernel<128>, grid, dim3(kThreads), smem, st, 1, tmK, tmV, p);
   } else {
     const int smem = AttnShape<64>::kSmemBytes;
     e = cudaFuncSetAttribute(gqa_split_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    gqa_split_kernel<64><<<grid, kThreads, smem, st>>>(tmK, tmV, p);
+    e = launch_k(gqa_split_kernel<64>, grid, dim3(kThreads), smem, st, 1, tmK, tmV, p);
   }
-  e = cudaGetLastError();
   if (e != cudaSuccess || ms == 1) return e;
   if (D == 128)
-    gqa_combine_kernel<128><<<(unsigned)(bs * Hq), 128, 0, st>>>(p.o_part, p.lse, kv_len, (int)Hq, cap, chunk, ms,
-                                                                 (int)max_kv_len, out);
-  else
-    gqa_combine_kernel<64><<<(unsigned)(bs * Hq), 64, 0, st>>>(p.o_part, p.lse, kv_len, (int)Hq, cap, chunk, ms,
-                                                               (int)max_kv_len, out);
-  return cudaGetLastError();
+    return launch_k(gqa_combine_kernel<128>, dim3((unsigned)(bs * Hq)), dim3(128), 0, st, 1,
+                    static_cast<const float*>(p.o_part), static_cast<const float*>(p.lse), kv_len, (int)Hq, cap, chunk,
+                    ms, (int)max_kv_len, out);
+  return launch_k(gqa_combine_kernel<64>, dim3((unsigned)(bs * Hq)), dim3(64), 0, st, 1,
+                  static_cast<const float*>(p.o_part), static_cast<const float*>(p.lse), kv_len, (int)Hq, cap, chunk, ms,
+                  (int)max_kv_len, out);
 }
 
 }  // namespace mxg

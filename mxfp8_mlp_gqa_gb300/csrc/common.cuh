@@ -49,6 +49,12 @@ __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t v) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// Let the next kernel on the stream be scheduled (it still waits for this one to finish).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Wait until the previous kernel on the stream has completed and its writes are visible.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ timers / bounded waits
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;

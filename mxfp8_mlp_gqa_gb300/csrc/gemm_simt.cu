@@ -11,6 +11,7 @@
 //    SwiGLU is fused into the down projection's activation quantisation; no bf16 h exists).
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace mxg {
 
@@ -49,6 +50,8 @@ __global__ void __launch_bounds__(256) mx_gemm_simt_kernel(const uint8_t* __rest
                                                            uint8_t* __restrict__ hq, uint8_t* __restrict__ hs) {
   __shared__ float As[kBK][kBM + 4];
   __shared__ float Bs[kBK][kBN + 4];
+  pdl_trigger();
+  pdl_wait();
   const int tid = threadIdx.x;
   const int m0 = blockIdx.y * kBM;
   const int n0 = blockIdx.x * kBN;
@@ -149,18 +152,16 @@ __global__ void __launch_bounds__(256) mx_gemm_simt_kernel(const uint8_t* __rest
 cudaError_t launch_mx_gemm_simt(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs,
                                 int64_t M, int64_t N, int64_t K, const uint16_t* res, uint16_t* c, cudaStream_t st) {
   dim3 grid((unsigned)((N + kBN - 1) / kBN), (unsigned)((M + kBM - 1) / kBM));
-  mx_gemm_simt_kernel<kStore><<<grid, 256, 0, st>>>(aq, as, bq, bs, (int)M, (int)N, (int)K, res, c, 0, nullptr,
-                                                     nullptr);
-  return cudaGetLastError();
+  return launch_k(mx_gemm_simt_kernel<kStore>, grid, dim3(256), 0, st, 1, aq, as, bq, bs, (int)M, (int)N, (int)K, res,
+                  c, 0, static_cast<uint8_t*>(nullptr), static_cast<uint8_t*>(nullptr));
 }
 
 cudaError_t launch_gate_up_swiglu_simt(const uint8_t* xq, const uint8_t* xs, int64_t M, int64_t d_model,
                                        int64_t d_ff, const uint8_t* w13q, const uint8_t* w13s, uint8_t* hq,
                                        uint8_t* hs, cudaStream_t st) {
   dim3 grid((unsigned)(d_ff / 32), (unsigned)((M + kBM - 1) / kBM));
-  mx_gemm_simt_kernel<kSwiGLU><<<grid, 256, 0, st>>>(xq, xs, w13q, w13s, (int)M, (int)(2 * d_ff), (int)d_model,
-                                                      nullptr, nullptr, (int)d_ff, hq, hs);
-  return cudaGetLastError();
+  return launch_k(mx_gemm_simt_kernel<kSwiGLU>, grid, dim3(256), 0, st, 1, xq, xs, w13q, w13s, (int)M, (int)(2 * d_ff),
+                  (int)d_model, static_cast<const uint16_t*>(nullptr), static_cast<uint16_t*>(nullptr), (int)d_ff, hq, hs);
 }
 
 }  // namespace mxg

@@ -26,6 +26,7 @@
 //                         epilogue (no bf16 h is ever written).
 // Every wait is bounded (MXG_ETIMEOUT in the error flag); TMEM is always released.
 #include "kernels.h"
+#include "launch.cuh"
 #include "tc.cuh"
 
 namespace mxg {
@@ -42,8 +43,9 @@ struct TcShape {
   static constexpr int kSfbAtoms = (BN + 127) / 128;
   static constexpr int kSfBytes = 1024 * ((512 * (1 + kSfbAtoms) + 1023) / 1024);  // keeps stages 1024-aligned
   static constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;
-  static constexpr int kStagesRaw = (BN >= 256 ? 200 * 1024 : 104 * 1024) / kStageBytes;
-  static constexpr int kStages = kStagesRaw > 8 ? 8 : (kStagesRaw < 2 ? 2 : kStagesRaw);
+  // one CTA per SM: the ring takes ~200 KB so that enough weight bytes are in flight per SM
+  static constexpr int kStagesRaw = (200 * 1024) / kStageBytes;
+  static constexpr int kStages = kStagesRaw > 12 ? 12 : (kStagesRaw < 2 ? 2 : kStagesRaw);
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kRS = 128 + 4;  // split-K staging [BN][kRS] (column-major, 16-byte rows)
   static constexpr int kStagingBytes =
@@ -133,6 +135,7 @@ __global__ void __launch_bounds__(192, 1) mx_gemm_tc_kernel(const __grid_constan
   const uint32_t tmem = *tmem_sh;
   const uint32_t t_d = tmem, t_sfa = tmem + BN, t_sfb = tmem + BN + 4;
 
+  pdl_trigger();
   if (warp == 0) {
     // ----------------------------------------------------------------- producer
     if (lane == 0) {
@@ -140,15 +143,29 @@ __global__ void __launch_bounds__(192, 1) mx_gemm_tc_kernel(const __grid_constan
       prefetch_tensormap(&tmX);
     }
     const int64_t KB = a.K >> 5;
+    // weight tiles of the first ring-full read nothing produced upstream: issue them before
+    // waiting for the previous kernel (programmatic dependent launch)
+    const int pre = ng < S::kStages ? ng : S::kStages;
+    if (lane == 0) {
+      for (int i = 0; i < pre; ++i) {
+        uint8_t* st = ring + i * S::kStageBytes;
+        mbar_arrive_expect_tx(&full[i], S::kABytes + S::kBBytes);
+        tma_load_2d(st, &tmW, &full[i], (g0 + i) * kKG, a_lo);
+        tma_load_2d(st + 64 * kKG, &tmW, &full[i], (g0 + i) * kKG, a_hi);
+      }
+    }
+    pdl_wait();
     for (int i = 0; i < ng; ++i) {
       const int s = i % S::kStages;
       if (i >= S::kStages && !mbar_wait(&empty[s], ((i / S::kStages) - 1) & 1, a.err)) break;
       uint8_t* st = ring + s * S::kStageBytes;
       const int g = g0 + i;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&full[s], S::kABytes + S::kBBytes);
-        tma_load_2d(st, &tmW, &full[s], g * kKG, a_lo);
-        tma_load_2d(st + 64 * kKG, &tmW, &full[s], g * kKG, a_hi);
+        if (i >= pre) {
+          mbar_arrive_expect_tx(&full[s], S::kABytes + S::kBBytes);
+          tma_load_2d(st, &tmW, &full[s], g * kKG, a_lo);
+          tma_load_2d(st + 64 * kKG, &tmW, &full[s], g * kKG, a_hi);
+        }
         tma_load_2d(st + S::kABytes, &tmX, &full[s], g * kKG, m0);
       }
       uint32_t* sfa = reinterpret_cast<uint32_t*>(st + S::kABytes + S::kBBytes);
@@ -196,6 +213,7 @@ __global__ void __launch_bounds__(192, 1) mx_gemm_tc_kernel(const __grid_constan
     // ----------------------------------------------------------------- epilogue
     const int q = warp & 3;  // the TMEM lane quadrant this warp may read
     const int r = 32 * q + lane;
+    pdl_wait();  // outputs and the residual are touched only after the previous kernel is done
     const bool ok = mbar_wait(tmem_full, 0, a.err);
     tc::fence_after_sync();
     const uint32_t trow = t_d + ((uint32_t)(32 * q) << 16);
@@ -262,9 +280,9 @@ __global__ void __launch_bounds__(192, 1) mx_gemm_tc_kernel(const __grid_constan
   if (EPI == kEpiSplit) {
     cluster_sync_all();  // every CTA of the cluster has staged its partial tile
     if (warp >= 2) {
-      // CTA z of the cluster owns tile rows [z*128/S, (z+1)*128/S) (S is a power of two <= 8)
+      // CTA z of the cluster owns the 4-row groups [z*32/S, (z+1)*32/S) of the 128-row tile
       const int S_ = a.splits;
-      const int nr = 128 / S_, rb = split * nr, nq = nr / 4;
+      const int rb = 4 * ((split * 32) / S_), nq = ((split + 1) * 32) / S_ - (split * 32) / S_;
       const float* stg = reinterpret_cast<const float*>(ring);
       for (int e = threadIdx.x - 64; e < BN * nq; e += 128) {
         const int c = e / nq, rr = rb + 4 * (e - c * nq);
@@ -322,14 +340,15 @@ Plan plan_gemm(int64_t M, int64_t N, int64_t K) {
   p.mtiles = (int)((M + p.bn - 1) / p.bn);
   const int groups = (int)(K / kKG);
   const int64_t ctas = (int64_t)p.ntiles * p.mtiles;
-  // split K over a cluster (power of two <= 8, the portable cluster size) when the tiles
-  // alone cannot cover the 152 SMs; N % 4 == 0 keeps the 4-wide reduction stores aligned
+  // split K over a cluster of S <= 8 CTAs (the portable cluster size) when the tiles alone
+  // cannot cover the 152 SMs, keeping the launch within one wave (one CTA per SM);
+  // N % 4 == 0 keeps the 4-wide reduction stores aligned
   p.splits = 1;
   if (ctas < 120 && N % 4 == 0) {
-    const double want = 152.0 / (double)ctas;
-    int s = 1;
-    while (s < 8 && 2 * s <= groups && (double)(2 * s) <= 1.5 * want) s *= 2;
-    p.splits = s;
+    int s = (int)(152 / ctas);
+    if (s > 8) s = 8;
+    if (s > groups) s = groups;
+    p.splits = s < 1 ? 1 : s;
   }
   return p;
 }
@@ -340,25 +359,8 @@ cudaError_t launch_tc(const CUtensorMap& tw, const CUtensorMap& tx, const TcArgs
   cudaError_t e = cudaFuncSetAttribute(mx_gemm_tc_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        S::kSmemBytes);
   if (e != cudaSuccess) return e;
-  if (EPI == kEpiSplit) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(192, 1, 1);
-    cfg.dynamicSmemBytes = S::kSmemBytes;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = grid.z;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, mx_gemm_tc_kernel<BN, EPI>, tw, tx, a);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
-  }
-  mx_gemm_tc_kernel<BN, EPI><<<grid, 192, S::kSmemBytes, st>>>(tw, tx, a);
-  return cudaGetLastError();
+  return launch_k(mx_gemm_tc_kernel<BN, EPI>, grid, dim3(192), S::kSmemBytes, st, EPI == kEpiSplit ? grid.z : 1u, tw,
+                  tx, a);
 }
 
 template <int EPI>

@@ -8,6 +8,7 @@
 // and coalesced; each lane stores 8 E4M3 bytes, lane 0 of each quad stores the scale byte.
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace mxg {
 
@@ -40,6 +41,8 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& w, float (&v)[8]) {
 __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
                                                              int64_t ld_x, uint8_t* __restrict__ q,
                                                              uint8_t* __restrict__ s) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t cpr = K >> 3;  // 8-element chunks per row (a multiple of 4)
   const int64_t total = M * cpr;
   const int64_t step = (int64_t)gridDim.x * blockDim.x;
@@ -73,6 +76,8 @@ __global__ void __launch_bounds__(256) rmsnorm_mxfp8_quantize_kernel(const uint1
                                                                      int64_t K, int64_t ld_x,
                                                                      uint8_t* __restrict__ q,
                                                                      uint8_t* __restrict__ s) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t row = blockIdx.x;
   const uint16_t* xr = x + row * ld_x;
   const int cpr = (int)(K >> 3);
@@ -135,14 +140,12 @@ cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t M, int64_t K, int64
   int64_t blocks = (total + threads - 1) / threads;
   if (blocks > 152 * 16) blocks = 152 * 16;
   if (blocks < 1) blocks = 1;
-  mxfp8_quantize_kernel<<<(unsigned)blocks, threads, 0, st>>>(x, M, K, ld_x, q, s);
-  return cudaGetLastError();
+  return launch_k(mxfp8_quantize_kernel, dim3((unsigned)blocks), dim3(threads), 0, st, 1, x, M, K, ld_x, q, s);
 }
 
 cudaError_t launch_rmsnorm_mxfp8_quantize(const uint16_t* x, const uint16_t* gamma, float eps, int64_t M, int64_t K,
                                           int64_t ld_x, uint8_t* q, uint8_t* s, cudaStream_t st) {
-  rmsnorm_mxfp8_quantize_kernel<<<(unsigned)M, 256, 0, st>>>(x, gamma, eps, K, ld_x, q, s);
-  return cudaGetLastError();
+  return launch_k(rmsnorm_mxfp8_quantize_kernel, dim3((unsigned)M), dim3(256), 0, st, 1, x, gamma, eps, K, ld_x, q, s);
 }
 
 }  // namespace mxg

@@ -2,6 +2,7 @@
 // cache append.
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace mxg {
 
@@ -12,6 +13,8 @@ namespace mxg {
 __global__ void __launch_bounds__(256) prev_tokens_shift_kernel(int32_t* __restrict__ prev,
                                                                 const int32_t* __restrict__ next, int W, int cw) {
   extern __shared__ int32_t win[];
+  pdl_trigger();
+  pdl_wait();
   const int n = W * cw;
   int32_t* p = prev + (int64_t)blockIdx.x * n;
   const int32_t* nx = next + (int64_t)blockIdx.x * cw;
@@ -28,6 +31,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint16_t* __restrict__ k
                                                         const uint16_t* __restrict__ vn, int64_t ld_new,
                                                         const int32_t* __restrict__ kv_len, int bs, int Hkv, int D,
                                                         int64_t cap, int32_t* err) {
+  pdl_trigger();
+  pdl_wait();
   const int gw = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (gw >= bs * Hkv) return;
@@ -48,8 +53,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint16_t* __restrict__ k
 cudaError_t launch_prev_tokens_shift(int32_t* prev, const int32_t* next, int64_t bs, int64_t W, int64_t cw,
                                      cudaStream_t st) {
   const size_t smem = (size_t)W * cw * sizeof(int32_t);
-  prev_tokens_shift_kernel<<<(unsigned)bs, 256, smem, st>>>(prev, next, (int)W, (int)cw);
-  return cudaGetLastError();
+  return launch_k(prev_tokens_shift_kernel, dim3((unsigned)bs), dim3(256), smem, st, 1, prev, next, (int)W, (int)cw);
 }
 
 cudaError_t launch_kv_append(uint16_t* kc, uint16_t* vc, const uint16_t* kn, const uint16_t* vn, int64_t ld_new,
@@ -57,9 +61,8 @@ cudaError_t launch_kv_append(uint16_t* kc, uint16_t* vc, const uint16_t* kn, con
                              cudaStream_t st) {
   const int64_t warps = bs * Hkv;
   const int64_t blocks = (warps * 32 + 255) / 256;
-  kv_append_kernel<<<(unsigned)blocks, 256, 0, st>>>(kc, vc, kn, vn, ld_new, kv_len, (int)bs, (int)Hkv, (int)D, cap,
-                                                     err);
-  return cudaGetLastError();
+  return launch_k(kv_append_kernel, dim3((unsigned)blocks), dim3(256), 0, st, 1, kc, vc, kn, vn, ld_new, kv_len,
+                  (int)bs, (int)Hkv, (int)D, cap, err);
 }
 
 }  // namespace mxg
