@@ -47,7 +47,8 @@ typedef enum {
   MXG_ELAUNCH = 5,    /* a CUDA launch failed */
   MXG_ETIMEOUT = 6,   /* device: a bounded wait ran out */
   MXG_EDEVICE = 7,    /* device: an input value out of range (e.g. kv_len) */
-  MXG_ENOTSUP = 8     /* no kernel for this device / configuration */
+  MXG_ENOTSUP = 8,    /* no kernel for this device / configuration */
+  MXG_ESCRATCH = 9    /* the problem needs more scratch than the library's fixed device array */
 } mxg_status;
 
 /* Static string for a status code (never NULL). */
@@ -145,6 +146,30 @@ mxg_status gqa_decode_attn(const void* q, int64_t ld_q, const void* k_cache, con
                            const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t cap,
                            int64_t max_kv_len, float scale, void* out, int32_t* err_flag, void* workspace,
                            size_t ws_bytes, void* stream);
+
+/*
+ * gqa_decode_attn_noalloc -- the same computation, kernels and arguments as gqa_decode_attn,
+ * minus the workspace: the split-KV scratch lives in a fixed device array owned by the
+ * library. (The pages have no counterpart of this entry point; it is an interface addition.)
+ *
+ * For callers that cannot allocate device memory where they run attention: code executing
+ * while a CUDA graph is being captured (cudaMalloc is not permitted there), real-time decode
+ * threads that must not block inside an allocator, and host applications that own the whole
+ * device-memory budget and do not let plugins allocate.
+ *   - Limit: gqa_decode_attn_noalloc_capacity() bytes (8 MiB) of scratch, i.e. problems with
+ *     gqa_decode_attn_workspace(bs, Hq, Hkv, D, max_kv_len) <= 8 MiB (e.g. bs 64, Hq 32, D 128,
+ *     max_kv_len up to ~4.2k tokens of split partials); larger problems return MXG_ESCRATCH
+ *     and launch nothing. Every GPU that loads the library holds the array until exit.
+ *   - Nothing is allocated or freed: no cudaMalloc/cudaFree or allocating library call.
+ *   - The first call on a device looks up that device's address of the array (with the device
+ *     current); make that first call before any stream capture on the device.
+ *   - All calls share the array and it keeps the last call's contents; calls whose kernels
+ *     overlap on the GPU (e.g. unordered streams) race on it -- order them on one stream.
+ */
+size_t gqa_decode_attn_noalloc_capacity(void);
+mxg_status gqa_decode_attn_noalloc(const void* q, int64_t ld_q, const void* k_cache, const void* v_cache,
+                                   const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t cap,
+                                   int64_t max_kv_len, float scale, void* out, int32_t* err_flag, void* stream);
 
 /*
  * kv_append -- in-place cache update of this step's K/V rows at position kv_len[b]-1

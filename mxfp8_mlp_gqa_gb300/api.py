@@ -39,6 +39,9 @@ _SIGS = {
     "gqa_decode_attn_workspace": (c_sz, [c_i64, c_i64, c_i64, c_i64, c_i64]),
     "gqa_decode_attn": (ctypes.c_int, [c_vp, c_i64, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_i64, c_i64, c_i64,
                                        c_f32, c_vp, c_vp, c_vp, c_sz, c_vp]),
+    "gqa_decode_attn_noalloc_capacity": (c_sz, []),
+    "gqa_decode_attn_noalloc": (ctypes.c_int, [c_vp, c_i64, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_i64, c_i64,
+                                               c_i64, c_f32, c_vp, c_vp, c_vp]),
     "kv_append": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_i64, c_vp, c_i64, c_i64, c_i64, c_i64, c_vp, c_vp]),
     "prev_tokens_shift": (ctypes.c_int, [c_vp, c_vp, c_i64, c_i64, c_i64, c_vp]),
 }
@@ -239,6 +242,24 @@ def gqa_decode_attn(q, k_cache, v_cache, kv_len, max_kv_len, scale, out=None, er
     ws_bytes = 0 if workspace is None else workspace.numel()
     _call("gqa_decode_attn", _ptr(q), ld_q, _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), bs, Hq, Hkv, D, cap,
           int(max_kv_len), float(scale), _ptr(out), _ptr(err), _ptr(workspace), ws_bytes, _stream())
+    return out
+
+
+def gqa_decode_attn_noalloc(q, k_cache, v_cache, kv_len, max_kv_len, scale, out):
+    """gqa_decode_attn without a workspace: for callers that cannot allocate device memory
+    (inside CUDA-graph capture, real-time threads, hosts that own the memory budget). Its
+    split-KV scratch is the library's fixed device array (gqa_decode_attn_noalloc_capacity()
+    bytes, shared by all calls); `out` must be passed in, so nothing is allocated here."""
+    _check(k_cache, "k_cache", torch.bfloat16, ndim=4)
+    bs, Hkv, cap, D = k_cache.shape
+    _check(v_cache, "v_cache", torch.bfloat16, (bs, Hkv, cap, D))
+    _check(kv_len, "kv_len", torch.int32, (bs,))
+    _check(q, "q", torch.bfloat16, ndim=3)
+    Hq = q.shape[1]
+    _check(q, "q", torch.bfloat16, (bs, Hq, D))
+    _check(out, "out", torch.bfloat16, (bs, Hq, D))
+    _call("gqa_decode_attn_noalloc", _ptr(q), Hq * D, _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), bs, Hq, Hkv, D,
+          cap, int(max_kv_len), float(scale), _ptr(out), None, _stream())
     return out
 
 

@@ -63,6 +63,7 @@ const char* mxg_status_str(int s) {
     case MXG_ETIMEOUT: return "device wait timed out";
     case MXG_EDEVICE: return "device-side input out of range";
     case MXG_ENOTSUP: return "not supported on this device/configuration";
+    case MXG_ESCRATCH: return "problem exceeds the fixed scratch of the allocation-free entry point";
     default: return "unknown status";
   }
 }
