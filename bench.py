@@ -65,14 +65,15 @@ def gemm_bytes(M, N, K, residual=False):
 
 
 def step_bytes(kv_lens, bs=BS):
+    """Algorithmic HBM bytes of one decode-layer step, per fused kernel of the step."""
     d, qd = D_MODEL, HQ * HD
     nqkv = (HQ + 2 * HKV) * HD
     parts = {
         "rmsnorm_quant_1": bs * d * 2 + d * 2 + bs * d * (1 + 1 / 32),
-        "qkv_gemm": gemm_bytes(bs, nqkv, d),
-        "kv_append": 2 * bs * HKV * HD * 2 * 2,
-        "attention": attn_bytes(kv_lens),
-        "quant_o": bs * qd * 2 + bs * qd * (1 + 1 / 32),
+        # weights + activations in; q written to the qkv buffer, K/V rows written to the cache
+        "qkv_gemm_kv_append": gemm_bytes(bs, nqkv, d),
+        # K/V prefixes + q in; o (bf16) and its MXFP8 copy out
+        "attention_quant": attn_bytes(kv_lens) + bs * qd * (1 + 1 / 32),
         "o_gemm": gemm_bytes(bs, d, qd, residual=True),
         "rmsnorm_quant_2": bs * d * 2 + d * 2 + bs * d * (1 + 1 / 32),
         "mlp": mlp_bytes(bs, residual=True),
@@ -200,42 +201,40 @@ def build_layer(dev, max_kv_len):
 
 
 def timed_ops(L, ev):
-    """One eager step with an event after every op (events on the current stream)."""
+    """The kernels of one step in order on one stream, with an event after each (the step
+    proper forks the prev-window shift onto a second stream; here it runs last)."""
     from mxfp8_mlp_gqa_gb300 import api
 
-    Hq, Hkv, D = L.Hq, L.Hkv, L.D
-    qd, kd = Hq * D, Hkv * D
+    qd = L.Hq * L.D
     ev[0].record()
     api.rmsnorm_mxfp8_quantize(L.x, L.gamma1, L.eps, q=L.xq, s=L.xs)
     ev[1].record()
-    api.mxfp8_gemm(L.xq, L.xs, *L.wqkv, c=L.qkv, workspace=L.ws_qkv)
+    api.mxfp8_gemm_qkv_kv_append(L.xq, L.xs, *L.wqkv, L.Hq, L.Hkv, L.k_cache, L.v_cache, L.kv_len, qkv=L.qkv,
+                                 err=L.err)
     ev[2].record()
-    api.kv_append(L.k_cache, L.v_cache, L.qkv[:, qd:qd + kd], L.qkv[:, qd + kd:], L.kv_len, err=L.err)
-    ev[3].record()
     api.gqa_decode_attn(L.qkv[:, :qd], L.k_cache, L.v_cache, L.kv_len, L.max_kv_len, L.scale, out=L.o, err=L.err,
-                        workspace=L.ws_attn)
-    ev[4].record()
-    api.mxfp8_quantize(L.o.view(L.bs, qd), q=L.oq, s=L.os)
-    ev[5].record()
+                        workspace=L.ws_attn, oq=L.oq, os=L.os)
+    ev[3].record()
     api.mxfp8_gemm(L.oq, L.os, *L.wo, residual=L.x, c=L.x1, workspace=L.ws_o)
-    ev[6].record()
+    ev[4].record()
     api.rmsnorm_mxfp8_quantize(L.x1, L.gamma2, L.eps, q=L.hq_in, s=L.hs_in)
-    ev[7].record()
+    ev[5].record()
     api.mlp_swiglu_mxfp8(L.hq_in, L.hs_in, *L.w13, *L.w2, residual=L.x1, y=L.y, workspace=L.ws_mlp)
-    ev[8].record()
+    ev[6].record()
     api.prev_tokens_shift(L.prev, L.next_tokens)
-    ev[9].record()
+    ev[7].record()
 
 
-OP_NAMES = ["rmsnorm_quant_1", "qkv_gemm", "kv_append", "attention", "quant_o", "o_gemm", "rmsnorm_quant_2", "mlp",
+OP_NAMES = ["rmsnorm_quant_1", "qkv_gemm_kv_append", "attention_quant", "o_gemm", "rmsnorm_quant_2", "mlp",
             "prev_shift"]
+NEV = len(OP_NAMES) + 1
 
 
 def launches_per_step(max_kv_len):
     from mxfp8_mlp_gqa_gb300 import api
 
     attn = 2 if api.gqa_decode_attn_workspace(BS, HQ, HKV, HD, max_kv_len) > 0 else 1
-    return 1 + 1 + 1 + attn + 1 + 1 + 1 + 2 + 1
+    return 1 + 1 + attn + 1 + 1 + 2 + 1  # rmsnorm, qkv+append, attention(+combine), o, rmsnorm, mlp, shift
 
 
 def run_ours(args, rank, local_rank, world):
@@ -260,7 +259,7 @@ def run_ours(args, rank, local_rank, world):
     L.kv_len.copy_(sched_d[0])
     L.step()
     torch.cuda.synchronize()
-    evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(10)]
+    evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(NEV)]
     graph = torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream()
     cap.wait_stream(torch.cuda.current_stream())
@@ -296,10 +295,10 @@ def run_ours(args, rank, local_rank, world):
         L.kv_len.copy_(sched_d[args.warmup + i])
         flush.zero_()
         graph.replay()
-        evs[9].synchronize()
+        evs[NEV - 1].synchronize()
         for k, n in enumerate(OP_NAMES):
             per_op[n].append(evs[k].elapsed_time(evs[k + 1]))
-        ev_step_ms.append(evs[0].elapsed_time(evs[9]))
+        ev_step_ms.append(evs[0].elapsed_time(evs[NEV - 1]))
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
@@ -309,8 +308,8 @@ def run_ours(args, rank, local_rank, world):
     bytes_steps = [step_bytes(sched[args.warmup + i]) for i in range(args.steps)]
     tot_bytes = sum(sum(b.values()) for b in bytes_steps)
     value = world * tot_bytes / (tot_ms * 1e-3) / 1e9
-    attn_bytes_avg = statistics.mean(b["attention"] for b in bytes_steps)
-    attn_ms = statistics.mean(per_op["attention"])
+    attn_bytes_avg = statistics.mean(b["attention_quant"] for b in bytes_steps)
+    attn_ms = statistics.mean(per_op["attention_quant"])
     breakdown = {}
     for n in OP_NAMES:
         ms = statistics.mean(per_op[n])
@@ -358,7 +357,8 @@ def run_ours(args, rank, local_rank, world):
     return {
         "value": value, "ms_per_step": tot_ms / args.steps, "clocks": clk, "breakdown": breakdown, "e2e": e2e,
         "eager_ms_per_step": statistics.mean(g_ms), "evented_ms_per_step": statistics.mean(ev_step_ms),
-        "roofline": {"kernel": "gqa_split_kernel (+combine)", "bound": "hbm",
+        "roofline": {"kernel": "gqa_split_kernel + gqa_combine_kernel (attention with fused MX quant)",
+                     "bound": "hbm",
                      "achieved": round(attn_bytes_avg / (attn_ms * 1e-3) / 1e9, 1), "peak": peak_gbs,
                      "peak_source": peak_src, "unit": "GB/s",
                      "frac": round(attn_bytes_avg / (attn_ms * 1e-3) / 1e9 / peak_gbs, 4), "traffic": None,

@@ -148,6 +148,17 @@ mxg_status gqa_decode_attn(const void* q, int64_t ld_q, const void* k_cache, con
                            size_t ws_bytes, void* stream);
 
 /*
+ * gqa_decode_attn_mxfp8 -- gqa_decode_attn that also writes its output MX-quantised for the
+ * O projection (decoder-layer step: attention -> quantise -> O projection), so that no
+ * separate quantise launch is needed: oq E4M3 [bs, Hq*D], os UE8M0 [bs, Hq*D/32], the MX
+ * rule of mxfp8_quantize applied to the bf16 output (bit-identical to mxfp8_quantize(out)).
+ */
+mxg_status gqa_decode_attn_mxfp8(const void* q, int64_t ld_q, const void* k_cache, const void* v_cache,
+                                 const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t cap,
+                                 int64_t max_kv_len, float scale, void* out, uint8_t* oq, uint8_t* os,
+                                 int32_t* err_flag, void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * gqa_decode_attn_noalloc -- the same computation, kernels and arguments as gqa_decode_attn,
  * minus the workspace: the split-KV scratch lives in a fixed device array owned by the
  * library. (The pages have no counterpart of this entry point; it is an interface addition.)
@@ -170,6 +181,19 @@ size_t gqa_decode_attn_noalloc_capacity(void);
 mxg_status gqa_decode_attn_noalloc(const void* q, int64_t ld_q, const void* k_cache, const void* v_cache,
                                    const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t cap,
                                    int64_t max_kv_len, float scale, void* out, int32_t* err_flag, void* stream);
+
+/*
+ * mxfp8_gemm_qkv_kv_append -- the QKV projection of a decoder-layer step fused with the KV
+ * append ([FSKV] §5, kv_cache.update): qkv = X' Wqkv'^T with X MXFP8 [M, K] and Wqkv MXFP8
+ * [(Hq + 2 Hkv) D, K]; columns [0, Hq D) (q) go to qkv bf16 [M, (Hq + 2 Hkv) D], columns of K
+ * and V go straight to row kv_len[m]-1 of k_cache / v_cache [M, Hkv, cap, D] (the K/V part of
+ * qkv is left unwritten). err_flag: MXG_EDEVICE if some kv_len is outside [1, cap] (that
+ * row is skipped). Requires K % 128 == 0, D % 8 == 0 (tensor-core path only).
+ */
+mxg_status mxfp8_gemm_qkv_kv_append(const uint8_t* xq, const uint8_t* xs, const uint8_t* wq, const uint8_t* ws,
+                                    int64_t M, int64_t K, int64_t Hq, int64_t Hkv, int64_t D, void* qkv,
+                                    void* k_cache, void* v_cache, const int32_t* kv_len, int64_t cap,
+                                    int32_t* err_flag, void* stream);
 
 /*
  * kv_append -- in-place cache update of this step's K/V rows at position kv_len[b]-1

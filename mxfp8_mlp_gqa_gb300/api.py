@@ -39,6 +39,10 @@ _SIGS = {
     "gqa_decode_attn_workspace": (c_sz, [c_i64, c_i64, c_i64, c_i64, c_i64]),
     "gqa_decode_attn": (ctypes.c_int, [c_vp, c_i64, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_i64, c_i64, c_i64,
                                        c_f32, c_vp, c_vp, c_vp, c_sz, c_vp]),
+    "gqa_decode_attn_mxfp8": (ctypes.c_int, [c_vp, c_i64, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_i64, c_i64,
+                                             c_i64, c_f32, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
+    "mxfp8_gemm_qkv_kv_append": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_i64, c_i64, c_vp,
+                                                c_vp, c_vp, c_vp, c_i64, c_vp, c_vp]),
     "gqa_decode_attn_noalloc_capacity": (c_sz, []),
     "gqa_decode_attn_noalloc": (ctypes.c_int, [c_vp, c_i64, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_i64, c_i64,
                                                c_i64, c_f32, c_vp, c_vp, c_vp]),
@@ -167,6 +171,29 @@ def mxfp8_gemm(aq, as_, bq, bs, residual=None, c=None, workspace=None):
     return c
 
 
+def mxfp8_gemm_qkv_kv_append(xq, xs, wq, ws, Hq, Hkv, k_cache, v_cache, kv_len, qkv=None, err=None):
+    """QKV projection with the KV append fused: q columns -> qkv bf16 [M, (Hq+2Hkv)D]; K/V
+    columns -> row kv_len[m]-1 of the caches [M, Hkv, cap, D]."""
+    _check(xq, "xq", torch.uint8, ndim=2)
+    M, K = xq.shape
+    _check(xs, "xs", torch.uint8, (M, K // 32))
+    _check(k_cache, "k_cache", torch.bfloat16, ndim=4)
+    bs, Hkv_, cap, D = k_cache.shape
+    if bs != M or Hkv_ != Hkv:
+        raise ValueError("k_cache: expected [M, Hkv, cap, D]")
+    _check(v_cache, "v_cache", torch.bfloat16, (M, Hkv, cap, D))
+    N = (Hq + 2 * Hkv) * D
+    _check(wq, "wq", torch.uint8, (N, K))
+    _check(ws, "ws", torch.uint8, (N, K // 32))
+    _check(kv_len, "kv_len", torch.int32, (M,))
+    qkv = _out(qkv, "qkv", torch.bfloat16, (M, N), xq.device)
+    if err is not None:
+        _check(err, "err", torch.int32, (1,))
+    _call("mxfp8_gemm_qkv_kv_append", _ptr(xq), _ptr(xs), _ptr(wq), _ptr(ws), M, K, Hq, Hkv, D, _ptr(qkv),
+          _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), cap, _ptr(err), _stream())
+    return qkv
+
+
 def mxfp8_gemm_workspace(M, N, K) -> int:
     return int(lib().mxfp8_gemm_workspace(M, N, K))
 
@@ -216,9 +243,11 @@ def gqa_decode_attn_workspace(bs, Hq, Hkv, D, max_kv_len) -> int:
     return int(lib().gqa_decode_attn_workspace(bs, Hq, Hkv, D, max_kv_len))
 
 
-def gqa_decode_attn(q, k_cache, v_cache, kv_len, max_kv_len, scale, out=None, err=None, workspace=None):
+def gqa_decode_attn(q, k_cache, v_cache, kv_len, max_kv_len, scale, out=None, err=None, workspace=None, oq=None,
+                    os=None):
     """q bf16 [bs, Hq, D] (or a row-strided [bs, Hq*D] view), caches bf16 [bs, Hkv, cap, D],
-    kv_len int32 [bs] on the device -> out bf16 [bs, Hq, D]."""
+    kv_len int32 [bs] on the device -> out bf16 [bs, Hq, D]. With oq/os given (uint8
+    [bs, Hq*D] and [bs, Hq*D/32]) the output is also written MX-quantised (gqa_decode_attn_mxfp8)."""
     _check(k_cache, "k_cache", torch.bfloat16, ndim=4)
     bs, Hkv, cap, D = k_cache.shape
     _check(v_cache, "v_cache", torch.bfloat16, (bs, Hkv, cap, D))
@@ -240,9 +269,16 @@ def gqa_decode_attn(q, k_cache, v_cache, kv_len, max_kv_len, scale, out=None, er
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=k_cache.device)
     ws_bytes = 0 if workspace is None else workspace.numel()
-    _call("gqa_decode_attn", _ptr(q), ld_q, _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), bs, Hq, Hkv, D, cap,
-          int(max_kv_len), float(scale), _ptr(out), _ptr(err), _ptr(workspace), ws_bytes, _stream())
-    return out
+    if oq is None and os is None:
+        _call("gqa_decode_attn", _ptr(q), ld_q, _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), bs, Hq, Hkv, D, cap,
+              int(max_kv_len), float(scale), _ptr(out), _ptr(err), _ptr(workspace), ws_bytes, _stream())
+        return out
+    _check(oq, "oq", torch.uint8, (bs, Hq * D))
+    _check(os, "os", torch.uint8, (bs, Hq * D // 32))
+    _call("gqa_decode_attn_mxfp8", _ptr(q), ld_q, _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), bs, Hq, Hkv, D, cap,
+          int(max_kv_len), float(scale), _ptr(out), _ptr(oq), _ptr(os), _ptr(err), _ptr(workspace), ws_bytes,
+          _stream())
+    return out, oq, os
 
 
 def gqa_decode_attn_noalloc(q, k_cache, v_cache, kv_len, max_kv_len, scale, out):

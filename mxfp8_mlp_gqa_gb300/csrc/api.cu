@@ -167,10 +167,12 @@ size_t gqa_decode_attn_workspace(int64_t bs, int64_t Hq, int64_t Hkv, int64_t D,
   return attn_workspace_bytes(bs, Hq, Hkv, D, max_kv_len);
 }
 
-mxg_status gqa_decode_attn(const void* q, int64_t ld_q, const void* k_cache, const void* v_cache,
-                           const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t cap,
-                           int64_t max_kv_len, float scale, void* out, int32_t* err_flag, void* workspace,
-                           size_t ws_bytes, void* stream) {
+namespace {
+
+mxg_status attn_call(const void* q, int64_t ld_q, const void* k_cache, const void* v_cache, const int32_t* kv_len,
+                     int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t cap, int64_t max_kv_len, float scale,
+                     void* out, uint8_t* oq, uint8_t* os, int32_t* err_flag, void* workspace, size_t ws_bytes,
+                     void* stream) {
   if (!q || !k_cache || !v_cache || !kv_len || !out) return MXG_EINVAL;
   if (!(scale > 0.f) || !(scale < 1e30f)) return MXG_EINVAL;
   if (bs < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || Hq / Hkv > 8 || (D != 64 && D != 128) || cap <= 0 ||
@@ -191,7 +193,54 @@ mxg_status gqa_decode_attn(const void* q, int64_t ld_q, const void* k_cache, con
     return MXG_ENOTSUP;
   return launched(launch_gqa_decode_attn(tk, tv, static_cast<const uint16_t*>(q), ld_q, kv_len, bs, Hq, Hkv, D, cap,
                                          max_kv_len, scale, static_cast<uint16_t*>(out), err_flag, workspace,
-                                         (cudaStream_t)stream));
+                                         (cudaStream_t)stream, oq, os));
+}
+
+}  // namespace
+
+mxg_status gqa_decode_attn(const void* q, int64_t ld_q, const void* k_cache, const void* v_cache,
+                           const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t cap,
+                           int64_t max_kv_len, float scale, void* out, int32_t* err_flag, void* workspace,
+                           size_t ws_bytes, void* stream) {
+  return attn_call(q, ld_q, k_cache, v_cache, kv_len, bs, Hq, Hkv, D, cap, max_kv_len, scale, out, nullptr, nullptr,
+                   err_flag, workspace, ws_bytes, stream);
+}
+
+mxg_status gqa_decode_attn_mxfp8(const void* q, int64_t ld_q, const void* k_cache, const void* v_cache,
+                                 const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t cap,
+                                 int64_t max_kv_len, float scale, void* out, uint8_t* oq, uint8_t* os,
+                                 int32_t* err_flag, void* workspace, size_t ws_bytes, void* stream) {
+  if (bs > 0 && (!oq || !os)) return MXG_EINVAL;
+  return attn_call(q, ld_q, k_cache, v_cache, kv_len, bs, Hq, Hkv, D, cap, max_kv_len, scale, out, oq, os, err_flag,
+                   workspace, ws_bytes, stream);
+}
+
+mxg_status mxfp8_gemm_qkv_kv_append(const uint8_t* xq, const uint8_t* xs, const uint8_t* wq, const uint8_t* ws,
+                                    int64_t M, int64_t K, int64_t Hq, int64_t Hkv, int64_t D, void* qkv,
+                                    void* k_cache, void* v_cache, const int32_t* kv_len, int64_t cap,
+                                    int32_t* err_flag, void* stream) {
+  const int64_t N = (Hq + 2 * Hkv) * D;
+  if (M < 0 || K <= 0 || K % 128 || Hq <= 0 || Hkv <= 0 || D <= 0 || D % 8 || cap <= 0 || M > 0x7fffffff ||
+      N > 0x7fffffff)
+    return MXG_ESHAPE;
+  if (M == 0) return MXG_OK;
+  if (!xq || !xs || !wq || !ws || !qkv || !k_cache || !v_cache || !kv_len) return MXG_EINVAL;
+  if (!aligned16(xq) || !aligned16(wq) || !aligned16(qkv) || !aligned16(k_cache) || !aligned16(v_cache))
+    return MXG_EALIGN;
+  if (!tc_gemm_supported(M, N, K)) return MXG_ENOTSUP;
+  KvScatter kv;
+  kv.q_cols = (int)(Hq * D);
+  kv.Hkv = (int)Hkv;
+  kv.D = (int)D;
+  kv.cap = cap;
+  kv.kc = static_cast<uint16_t*>(k_cache);
+  kv.vc = static_cast<uint16_t*>(v_cache);
+  kv.kv_len = kv_len;
+  bool unsupported = false;
+  const cudaError_t e = launch_mx_gemm_tc(xq, xs, wq, ws, M, N, K, nullptr, static_cast<uint16_t*>(qkv), nullptr,
+                                          err_flag, (cudaStream_t)stream, &unsupported, &kv);
+  if (unsupported) return MXG_ENOTSUP;
+  return launched(e);
 }
 
 mxg_status kv_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new, int64_t ld_new,

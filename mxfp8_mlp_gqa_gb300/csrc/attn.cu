@@ -63,6 +63,8 @@ struct SplitParams {
   float* o_part;     // [bs, Hq, max_splits, D]
   float* lse;        // [bs, Hq, max_splits]
   uint16_t* out;     // written directly when max_splits == 1
+  uint8_t* oq;       // optional MXFP8 copy of out ([bs, Hq*D] E4M3 + [bs, Hq*D/32] UE8M0)
+  uint8_t* os;
   int32_t* err;
 };
 
@@ -96,8 +98,14 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
   if (n < 1 || (int64_t)n > p.cap || n > p.max_kv_len) {
     if (split == 0 && g == 0 && threadIdx.x == 0) set_error(p.err, MXG_EDEVICE);
     if (p.max_splits == 1 && warp < kConsumers) {  // single-split mode: no combine pass, zero here
-      for (int i = threadIdx.x; i < p.group * D; i += kConsumers * 32)
-        p.out[((int64_t)b * p.Hq + g * p.group) * D + i] = 0;
+      for (int i = threadIdx.x; i < p.group * D; i += kConsumers * 32) {
+        const int64_t o = ((int64_t)b * p.Hq + g * p.group) * D + i;
+        p.out[o] = 0;
+        if (p.oq) {
+          p.oq[o] = 0;
+          if ((i & 31) == 0) p.os[o >> 5] = 0;
+        }
+      }
     }
     return;
   }
@@ -293,7 +301,10 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
     }
     const int64_t bh = (int64_t)b * p.Hq + h0 + h;
     if (p.max_splits == 1) {
-      p.out[bh * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(O / L));
+      const __nv_bfloat16 ob = __float2bfloat16_rn(O / L);
+      p.out[bh * D + d] = __bfloat16_as_ushort(ob);
+      // idx runs over whole warps of consecutive d (D is a multiple of 32): one MX block per warp
+      if (p.oq) mx_quant_warp_store(__bfloat162float(ob), p.oq + bh * D + d, p.os + ((bh * D + d) >> 5));
     } else {
       p.o_part[(bh * p.max_splits + split) * D + d] = O / L;
       if (d == 0) p.lse[bh * p.max_splits + split] = M + log2f(L);
@@ -307,7 +318,8 @@ __global__ void __launch_bounds__(D) gqa_combine_kernel(const float* __restrict_
                                                         const float* __restrict__ lse,
                                                         const int32_t* __restrict__ kv_len, int Hq, int64_t cap,
                                                         int chunk, int max_splits, int max_kv_len,
-                                                        uint16_t* __restrict__ out) {
+                                                        uint16_t* __restrict__ out, uint8_t* __restrict__ oq,
+                                                        uint8_t* __restrict__ os) {
   pdl_trigger();
   pdl_wait();
   const int64_t bh = blockIdx.x;
@@ -316,6 +328,10 @@ __global__ void __launch_bounds__(D) gqa_combine_kernel(const float* __restrict_
   const int n = kv_len[b];
   if (n < 1 || (int64_t)n > cap || n > max_kv_len) {
     out[bh * D + d] = 0;
+    if (oq) {
+      oq[bh * D + d] = 0;
+      if ((d & 31) == 0) os[(bh * D + d) >> 5] = 0;
+    }
     return;
   }
   const int ns = (n + chunk - 1) / chunk;
@@ -328,7 +344,9 @@ __global__ void __launch_bounds__(D) gqa_combine_kernel(const float* __restrict_
     W += w;
     acc += w * o_part[(bh * max_splits + i) * D + d];
   }
-  out[bh * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(acc / W));
+  const __nv_bfloat16 ob = __float2bfloat16_rn(acc / W);
+  out[bh * D + d] = __bfloat16_as_ushort(ob);
+  if (oq) mx_quant_warp_store(__bfloat162float(ob), oq + bh * D + d, os + ((bh * D + d) >> 5));
 }
 
 // ---------------------------------------------------------------------------------- host
@@ -351,7 +369,7 @@ size_t attn_workspace_bytes(int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int6
 cudaError_t launch_gqa_decode_attn(const CUtensorMap& tmK, const CUtensorMap& tmV, const uint16_t* q, int64_t ld_q,
                                    const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t cap,
                                    int64_t max_kv_len, float scale, uint16_t* out, int32_t* err, void* ws,
-                                   cudaStream_t st) {
+                                   cudaStream_t st, uint8_t* oq, uint8_t* os) {
   const int chunk = attn_chunk(bs, Hkv, max_kv_len);
   const int ms = (int)((max_kv_len + chunk - 1) / chunk);
   SplitParams p;
@@ -369,6 +387,8 @@ cudaError_t launch_gqa_decode_attn(const CUtensorMap& tmK, const CUtensorMap& tm
   p.o_part = reinterpret_cast<float*>(ws);
   p.lse = ms > 1 ? p.o_part + bs * Hq * ms * D : nullptr;
   p.out = out;
+  p.oq = oq;
+  p.os = os;
   p.err = err;
   dim3 grid((unsigned)ms, (unsigned)(bs * Hkv));
   cudaError_t e;
@@ -387,10 +407,10 @@ cudaError_t launch_gqa_decode_attn(const CUtensorMap& tmK, const CUtensorMap& tm
   if (D == 128)
     return launch_k(gqa_combine_kernel<128>, dim3((unsigned)(bs * Hq)), dim3(128), 0, st, 1,
                     static_cast<const float*>(p.o_part), static_cast<const float*>(p.lse), kv_len, (int)Hq, cap, chunk,
-                    ms, (int)max_kv_len, out);
+                    ms, (int)max_kv_len, out, oq, os);
   return launch_k(gqa_combine_kernel<64>, dim3((unsigned)(bs * Hq)), dim3(64), 0, st, 1,
                   static_cast<const float*>(p.o_part), static_cast<const float*>(p.lse), kv_len, (int)Hq, cap, chunk, ms,
-                  (int)max_kv_len, out);
+                  (int)max_kv_len, out, oq, os);
 }
 
 }  // namespace mxg

@@ -46,6 +46,17 @@ __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t v) {
   return __half22float2(hh);
 }
 
+// One 32-element MX block held one value per lane of a full warp: lane i stores the E4M3
+// byte of its value to q_dst, lane 0 stores the block's UE8M0 scale byte to s_dst.
+__device__ __forceinline__ void mx_quant_warp_store(float v, uint8_t* q_dst, uint8_t* s_dst) {
+  float am = fabsf(v);
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) am = fmaxf(am, __shfl_xor_sync(MXG_FULL_MASK, am, off));
+  const int s = mx_shared_exp(am);
+  *q_dst = (uint8_t)(cvt_e4m3x2(v * mx_inv_scale(s), 0.f) & 0xFF);
+  if ((threadIdx.x & 31) == 0) *s_dst = (uint8_t)(s + 127);
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

@@ -71,7 +71,29 @@ struct TcArgs {
   const uint16_t* residual;
   uint16_t* out;
   int32_t* err;
+  KvScatter kv;         // fused KV append of a QKV projection (kv.kc == nullptr: off)
 };
+
+// Destination of output element (m, n): `out`, or -- for the K/V columns of a fused QKV
+// projection -- row kv_len[m]-1 of KV head (c / D) in the K or V cache (nullptr, with the
+// error flag set, when that row is outside the cache).
+__device__ __forceinline__ uint16_t* out_ptr(const TcArgs& a, int m, int n) {
+  if (a.kv.kc == nullptr || n < a.kv.q_cols) return a.out + (int64_t)m * a.N + n;
+  const int kvd = a.kv.Hkv * a.kv.D;
+  int c = n - a.kv.q_cols;
+  uint16_t* base = a.kv.kc;
+  if (c >= kvd) {
+    c -= kvd;
+    base = a.kv.vc;
+  }
+  const int pos = a.kv.kv_len[m] - 1;
+  if (pos < 0 || (int64_t)pos >= a.kv.cap) {
+    set_error(a.err, MXG_EDEVICE);
+    return nullptr;
+  }
+  const int g = c / a.kv.D, d = c - g * a.kv.D;
+  return base + (((int64_t)m * a.kv.Hkv + g) * a.kv.cap + pos) * a.kv.D + d;
+}
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -231,7 +253,8 @@ __global__ void __launch_bounds__(192, 1) mx_gemm_tc_kernel(const __grid_constan
           if (m < a.M && nv) {
             float y = v[j];
             if (a.residual) y += __bfloat162float(__ushort_as_bfloat16(a.residual[(int64_t)m * a.N + n]));
-            a.out[(int64_t)m * a.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+            uint16_t* dst = out_ptr(a, m, n);
+            if (dst) *dst = __bfloat16_as_ushort(__float2bfloat16_rn(y));
           }
         }
       }
@@ -267,12 +290,7 @@ __global__ void __launch_bounds__(192, 1) mx_gemm_tc_kernel(const __grid_constan
           const float g = stg[(32 * blk + lane) * (BN + 1) + t];
           const float u = stg[(64 + 32 * blk + lane) * (BN + 1) + t];
           const float h = g / (1.f + expf(-g)) * u;
-          float am = fabsf(h);
-#pragma unroll
-          for (int off = 1; off < 32; off <<= 1) am = fmaxf(am, __shfl_xor_sync(MXG_FULL_MASK, am, off));
-          const int se = mx_shared_exp(am);
-          a.hq[(int64_t)m * a.d_ff + j0 + lane] = (uint8_t)(cvt_e4m3x2(h * mx_inv_scale(se), 0.f) & 0xFF);
-          if (lane == 0) a.hs[(int64_t)m * (a.d_ff >> 5) + (j0 >> 5)] = (uint8_t)(se + 127);
+          mx_quant_warp_store(h, a.hq + (int64_t)m * a.d_ff + j0 + lane, a.hs + (int64_t)m * (a.d_ff >> 5) + (j0 >> 5));
         }
       }
     }
@@ -314,7 +332,8 @@ __global__ void __launch_bounds__(192, 1) mx_gemm_tc_kernel(const __grid_constan
                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.y)) << 16);
         ov.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.z)) |
                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.w)) << 16);
-        *reinterpret_cast<uint2*>(a.out + o) = ov;
+        uint16_t* dst = out_ptr(a, m, n);  // 4 consecutive columns never straddle a head (D % 4 == 0)
+        if (dst) *reinterpret_cast<uint2*>(dst) = ov;
       }
     }
     cluster_sync_all();  // keep this CTA's shared memory alive until every reader is done
@@ -333,6 +352,43 @@ struct Plan {
   int bn, ntiles, mtiles, splits;
 };
 
+template <int BN>
+int max_clusters(int cs) {
+  // how many clusters of `cs` CTAs of the split-K kernel can be resident at once (1 CTA/SM)
+  static int cache[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+  if (cache[cs]) return cache[cs];
+  using S = TcShape<BN>;
+  cudaFuncSetAttribute(mx_gemm_tc_kernel<BN, kEpiSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, 1, cs);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = S::kSmemBytes;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 1;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = cs;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, mx_gemm_tc_kernel<BN, kEpiSplit>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 152 / cs;
+  }
+  cache[cs] = n > 0 ? n : 1;
+  return cache[cs];
+}
+
+int max_clusters_bn(int bn, int cs) {
+  switch (bn) {
+    case 16: return max_clusters<16>(cs);
+    case 32: return max_clusters<32>(cs);
+    case 64: return max_clusters<64>(cs);
+    case 128: return max_clusters<128>(cs);
+    default: return max_clusters<256>(cs);
+  }
+}
+
 Plan plan_gemm(int64_t M, int64_t N, int64_t K) {
   Plan p;
   p.bn = M > 1024 ? 256 : pick_bn(M);
@@ -343,11 +399,13 @@ Plan plan_gemm(int64_t M, int64_t N, int64_t K) {
   // split K over a cluster of S <= 8 CTAs (the portable cluster size) when the tiles alone
   // cannot cover the 152 SMs, keeping the launch within one wave (one CTA per SM);
   // N % 4 == 0 keeps the 4-wide reduction stores aligned
+  // (the largest S whose clusters are all resident together: no second wave)
   p.splits = 1;
   if (ctas < 120 && N % 4 == 0) {
     int s = (int)(152 / ctas);
     if (s > 8) s = 8;
     if (s > groups) s = groups;
+    while (s > 1 && (int64_t)max_clusters_bn(p.bn, s) < ctas) --s;
     p.splits = s < 1 ? 1 : s;
   }
   return p;
@@ -396,7 +454,7 @@ size_t tc_gemm_workspace(int64_t M, int64_t N, int64_t K) {
 
 cudaError_t launch_mx_gemm_tc(const uint8_t* xq, const uint8_t* xs, const uint8_t* wq, const uint8_t* ws, int64_t M,
                               int64_t N, int64_t K, const uint16_t* residual, uint16_t* out, void* workspace,
-                              int32_t* err, cudaStream_t st, bool* unsupported) {
+                              int32_t* err, cudaStream_t st, bool* unsupported, const KvScatter* kv) {
   const Plan p = plan_gemm(M, N, K);
   CUtensorMap tw, tx;
   *unsupported = false;
@@ -415,6 +473,7 @@ cudaError_t launch_mx_gemm_tc(const uint8_t* xq, const uint8_t* xs, const uint8_
   a.residual = residual;
   a.out = out;
   a.err = err;
+  if (kv) a.kv = *kv;
   dim3 grid((unsigned)p.ntiles, (unsigned)p.mtiles, (unsigned)p.splits);
   (void)workspace;
   if (p.splits > 1) return launch_tc_bn<kEpiSplit>(p.bn, tw, tx, a, grid, st);

@@ -23,7 +23,7 @@ size_t attn_workspace_bytes(int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int6
 cudaError_t launch_gqa_decode_attn(const CUtensorMap& tmK, const CUtensorMap& tmV, const uint16_t* q, int64_t ld_q,
                                    const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t cap,
                                    int64_t max_kv_len, float scale, uint16_t* out, int32_t* err, void* ws,
-                                   cudaStream_t st);
+                                   cudaStream_t st, uint8_t* oq = nullptr, uint8_t* os = nullptr);
 
 cudaError_t launch_mx_gemm_simt(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs,
                                 int64_t M, int64_t N, int64_t K, const uint16_t* res, uint16_t* c, cudaStream_t st);
@@ -33,9 +33,18 @@ cudaError_t launch_gate_up_swiglu_simt(const uint8_t* xq, const uint8_t* xs, int
 
 bool tc_gemm_supported(int64_t M, int64_t N, int64_t K);
 size_t tc_gemm_workspace(int64_t M, int64_t N, int64_t K);
+// Optional fused KV append of a QKV projection: output columns [q_cols, q_cols + Hkv*D) are K
+// and the next Hkv*D are V; they are written to the caches at row kv_len[m]-1 instead of `out`.
+struct KvScatter {
+  int q_cols = 0, Hkv = 0, D = 0;
+  int64_t cap = 0;
+  uint16_t* kc = nullptr;
+  uint16_t* vc = nullptr;
+  const int32_t* kv_len = nullptr;
+};
 cudaError_t launch_mx_gemm_tc(const uint8_t* xq, const uint8_t* xs, const uint8_t* wq, const uint8_t* ws, int64_t M,
                               int64_t N, int64_t K, const uint16_t* residual, uint16_t* out, void* workspace,
-                              int32_t* err, cudaStream_t st, bool* unsupported);
+                              int32_t* err, cudaStream_t st, bool* unsupported, const KvScatter* kv = nullptr);
 cudaError_t launch_gate_up_swiglu_tc(const uint8_t* xq, const uint8_t* xs, int64_t M, int64_t d_model, int64_t d_ff,
                                      const uint8_t* w13q, const uint8_t* w13s, uint8_t* hq, uint8_t* hs, int32_t* err,
                                      cudaStream_t st, bool* unsupported);

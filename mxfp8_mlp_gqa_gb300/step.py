@@ -2,9 +2,10 @@
 entry points (every step runs in libmxg kernels; this module only owns buffers and the
 call order):
 
-    RMSNorm+MX-quantise -> QKV projection (MXFP8 GEMM) -> KV append -> GQA decode
-    attention -> MX-quantise -> O projection + residual -> RMSNorm+MX-quantise ->
-    SwiGLU MLP (gate/up + SwiGLU + requant, down + residual) -> prev-window shift
+    RMSNorm+MX-quantise -> QKV projection with the KV append fused in its epilogue ->
+    GQA decode attention with the MX-quantised output fused in -> O projection + residual ->
+    RMSNorm+MX-quantise -> SwiGLU MLP (gate/up + SwiGLU + requant, down + residual);
+    the prev-window shift runs on a forked stream branch (it depends on nothing above)
 
 The pages list the layer as RMSNorm -> attention -> RMSNorm -> MLP (Qwen3-style, [S2.1]
 "The Real Reason Voice AI Costs Money" / "Kernel Benchmark Results", [FSKV] §2). The QKV
@@ -63,6 +64,7 @@ class DecodeLayer:
         self.ws_qkv = torch.zeros((max(1, nqkv_ws),), dtype=u8, device=dev)
         self.ws_o = torch.zeros((max(1, api.mxfp8_gemm_workspace(bs, d_model, Hq * D)),), dtype=u8, device=dev)
         self.graph = None
+        self.side = torch.cuda.Stream(device=dev)
 
     def load_weights(self, wqkv_bf16, wo_bf16, w13_bf16, w2_bf16, gamma1, gamma2):
         """bf16 weights on the device -> MXFP8 once (weight prep, not part of a step)."""
@@ -73,19 +75,21 @@ class DecodeLayer:
 
     def step(self):
         Hq, Hkv, D = self.Hq, self.Hkv, self.D
+        main = torch.cuda.current_stream()
+        self.side.wait_stream(main)
+        with torch.cuda.stream(self.side):
+            api.prev_tokens_shift(self.prev, self.next_tokens)
         api.rmsnorm_mxfp8_quantize(self.x, self.gamma1, self.eps, q=self.xq, s=self.xs)
-        api.mxfp8_gemm(self.xq, self.xs, *self.wqkv, c=self.qkv, workspace=self.ws_qkv)
-        qd, kd = Hq * D, Hkv * D
-        api.kv_append(self.k_cache, self.v_cache, self.qkv[:, qd:qd + kd], self.qkv[:, qd + kd:], self.kv_len,
-                      err=self.err)
+        api.mxfp8_gemm_qkv_kv_append(self.xq, self.xs, *self.wqkv, Hq, Hkv, self.k_cache, self.v_cache,
+                                     self.kv_len, qkv=self.qkv, err=self.err)
+        qd = Hq * D
         api.gqa_decode_attn(self.qkv[:, :qd], self.k_cache, self.v_cache, self.kv_len, self.max_kv_len, self.scale,
-                            out=self.o, err=self.err, workspace=self.ws_attn)
-        api.mxfp8_quantize(self.o.view(self.bs, qd), q=self.oq, s=self.os)
+                            out=self.o, err=self.err, workspace=self.ws_attn, oq=self.oq, os=self.os)
         api.mxfp8_gemm(self.oq, self.os, *self.wo, residual=self.x, c=self.x1, workspace=self.ws_o)
         api.rmsnorm_mxfp8_quantize(self.x1, self.gamma2, self.eps, q=self.hq_in, s=self.hs_in)
         api.mlp_swiglu_mxfp8(self.hq_in, self.hs_in, *self.w13, *self.w2, residual=self.x1, y=self.y,
                              workspace=self.ws_mlp)
-        api.prev_tokens_shift(self.prev, self.next_tokens)
+        main.wait_stream(self.side)
         return self.y
 
     def capture(self):
