@@ -78,7 +78,7 @@ mxg_status mxfp8_quantize(const void* x, int64_t M, int64_t K, int64_t ld_x, uin
  * step: RMSNorm -> attention -> RMSNorm -> MLP).
  *   y = bf16( (x * r) * gamma ), r = fp32( 1 / sqrt( mean_fp64(x^2) + eps ) ), products
  *   in fp32, then the MX rule above on y.  x bf16 [M, K] (row stride ld_x), gamma bf16 [K].
- * Requires K % 32 == 0 and K <= 16384.
+ * Requires K % 32 == 0 and K <= 17920.
  */
 mxg_status rmsnorm_mxfp8_quantize(const void* x, const void* gamma, float eps, int64_t M, int64_t K, int64_t ld_x,
                                   uint8_t* q, uint8_t* s, void* stream);

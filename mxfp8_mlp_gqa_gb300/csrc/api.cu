@@ -87,7 +87,7 @@ mxg_status mxfp8_quantize(const void* x, int64_t M, int64_t K, int64_t ld_x, uin
 mxg_status rmsnorm_mxfp8_quantize(const void* x, const void* gamma, float eps, int64_t M, int64_t K, int64_t ld_x,
                                   uint8_t* q, uint8_t* s, void* stream) {
   if (!(eps >= 0.f)) return MXG_EINVAL;
-  if (M < 0 || K <= 0 || K % 32 || K > 16384 || ld_x < K || M > 0x7fffffff) return MXG_ESHAPE;
+  if (M < 0 || K <= 0 || K % 32 || K > 17920 || ld_x < K || M > 0x7fffffff) return MXG_ESHAPE;
   if (M == 0) return MXG_OK;
   if (!x || !gamma || !q || !s) return MXG_EINVAL;
   if (!aligned16(x) || !aligned16(gamma) || !aligned16(q) || ld_x % 8) return MXG_EALIGN;

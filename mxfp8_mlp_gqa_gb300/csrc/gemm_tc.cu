@@ -43,9 +43,10 @@ struct TcShape {
   static constexpr int kSfbAtoms = (BN + 127) / 128;
   static constexpr int kSfBytes = 1024 * ((512 * (1 + kSfbAtoms) + 1023) / 1024);  // keeps stages 1024-aligned
   static constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;
-  // one CTA per SM: the ring takes ~200 KB so that enough weight bytes are in flight per SM
-  static constexpr int kStagesRaw = (200 * 1024) / kStageBytes;
-  static constexpr int kStages = kStagesRaw > 12 ? 12 : (kStagesRaw < 2 ? 2 : kStagesRaw);
+  // ~96 KB ring: two CTAs fit on an SM, so that the next kernel of the step (launched early
+  // by PDL) can start streaming its weights while this one drains
+  static constexpr int kStagesRaw = (BN >= 256 ? 200 * 1024 : 96 * 1024) / kStageBytes;
+  static constexpr int kStages = kStagesRaw > 8 ? 8 : (kStagesRaw < 2 ? 2 : kStagesRaw);
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kRS = 128 + 4;  // split-K staging [BN][kRS] (column-major, 16-byte rows)
   static constexpr int kStagingBytes =
@@ -117,7 +118,7 @@ __device__ __forceinline__ float4 ld_dsmem_f32x4(const float* local, uint32_t ra
 }  // namespace
 
 template <int BN, int EPI>
-__global__ void __launch_bounds__(192, 1) mx_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW,
+__global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW,
                                                             const __grid_constant__ CUtensorMap tmX, const TcArgs a) {
   using S = TcShape<BN>;
   extern __shared__ uint8_t smem_raw[];

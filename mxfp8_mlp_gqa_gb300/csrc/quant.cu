@@ -69,59 +69,70 @@ __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const uint16_t* __r
   }
 }
 
-// One CTA per row. Pass 1: sum of squares in fp64 (each square is exact in fp64). Pass 2:
-// y = bf16((x * r) * gamma) with r rounded to fp32 once, then the MX rule on y.
-__global__ void __launch_bounds__(256) rmsnorm_mxfp8_quantize_kernel(const uint16_t* __restrict__ x,
-                                                                     const uint16_t* __restrict__ gamma, float eps,
-                                                                     int64_t K, int64_t ld_x,
-                                                                     uint8_t* __restrict__ q,
-                                                                     uint8_t* __restrict__ s) {
+// One CTA per row; each thread keeps its 8-element chunks of x (and gamma) in registers, so
+// the row is read from memory once. Sum of squares in fp64 (each square is exact in fp64),
+// then y = bf16((x * r) * gamma) with r = fp32(1 / sqrt(mean + eps)), then the MX rule on y.
+constexpr int kRmsThreads = 320;  // = K/8 for K = 2560: one chunk per thread
+constexpr int kRmsChunks = 7;     // chunks per thread kept in registers: K <= 8 * 320 * 7 = 17920
+
+__global__ void __launch_bounds__(kRmsThreads) rmsnorm_mxfp8_quantize_kernel(const uint16_t* __restrict__ x,
+                                                                             const uint16_t* __restrict__ gamma,
+                                                                             float eps, int64_t K, int64_t ld_x,
+                                                                             uint8_t* __restrict__ q,
+                                                                             uint8_t* __restrict__ s) {
   pdl_trigger();
-  pdl_wait();
   const int64_t row = blockIdx.x;
   const uint16_t* xr = x + row * ld_x;
   const int cpr = (int)(K >> 3);
-  double acc = 0.0;
-  for (int c = threadIdx.x; c < cpr; c += blockDim.x) {
-    const uint4 w = __ldg(reinterpret_cast<const uint4*>(xr + ((int64_t)c << 3)));
-    float v[8];
-    unpack_bf16x8(w, v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint4 gw[kRmsChunks];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc += (double)v[i] * (double)v[i];
+  for (int i = 0; i < kRmsChunks; ++i) {  // gamma is a weight: read before waiting for upstream
+    const int c = threadIdx.x + i * kRmsThreads;
+    gw[i] = c < cpr ? __ldg(reinterpret_cast<const uint4*>(gamma + ((int64_t)c << 3))) : make_uint4(0, 0, 0, 0);
+  }
+  pdl_wait();
+  uint4 xw[kRmsChunks];
+  double acc = 0.0;
+#pragma unroll
+  for (int i = 0; i < kRmsChunks; ++i) {
+    const int c = threadIdx.x + i * kRmsThreads;
+    xw[i] = c < cpr ? __ldg(reinterpret_cast<const uint4*>(xr + ((int64_t)c << 3))) : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int i = 0; i < kRmsChunks; ++i) {
+    float v[8];
+    unpack_bf16x8(xw[i], v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc += (double)v[j] * (double)v[j];
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(MXG_FULL_MASK, acc, o);
-  __shared__ double red[32];
+  __shared__ double red[kRmsThreads / 32];
   __shared__ float r_sh;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) red[warp] = acc;
   __syncthreads();
   if (threadIdx.x == 0) {
     double t = 0.0;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t += red[i];
+    for (int i = 0; i < kRmsThreads / 32; ++i) t += red[i];
     const double ms = t / (double)K;
     r_sh = (float)(1.0 / sqrt(ms + (double)eps));
   }
   __syncthreads();
   const float r = r_sh;
-  for (int base = 0; base < cpr; base += blockDim.x) {
+#pragma unroll
+  for (int i = 0; i < kRmsChunks; ++i) {
+    const int base = i * kRmsThreads;
+    if (base >= cpr) break;  // uniform across the block
     const int c = base + threadIdx.x;
     const bool act = c < cpr;
-    float v[8];
-    if (act) {
-      const uint4 w = __ldg(reinterpret_cast<const uint4*>(xr + ((int64_t)c << 3)));
-      const uint4 g = __ldg(reinterpret_cast<const uint4*>(gamma + ((int64_t)c << 3)));
-      float xv[8], gv[8];
-      unpack_bf16x8(w, xv);
-      unpack_bf16x8(g, gv);
+    float xv[8], gv[8], v[8];
+    unpack_bf16x8(xw[i], xv);
+    unpack_bf16x8(gw[i], gv);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float y = __fmul_rn(__fmul_rn(xv[i], r), gv[i]);
-        v[i] = __bfloat162float(__float2bfloat16_rn(y));
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    for (int j = 0; j < 8; ++j) {
+      const float y = __fmul_rn(__fmul_rn(xv[j], r), gv[j]);
+      v[j] = act ? __bfloat162float(__float2bfloat16_rn(y)) : 0.f;
     }
     uint2 packed;
     uint8_t sb;
@@ -145,7 +156,8 @@ cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t M, int64_t K, int64
 
 cudaError_t launch_rmsnorm_mxfp8_quantize(const uint16_t* x, const uint16_t* gamma, float eps, int64_t M, int64_t K,
                                           int64_t ld_x, uint8_t* q, uint8_t* s, cudaStream_t st) {
-  return launch_k(rmsnorm_mxfp8_quantize_kernel, dim3((unsigned)M), dim3(256), 0, st, 1, x, gamma, eps, K, ld_x, q, s);
+  return launch_k(rmsnorm_mxfp8_quantize_kernel, dim3((unsigned)M), dim3(kRmsThreads), 0, st, 1, x, gamma, eps, K, ld_x,
+                  q, s);
 }
 
 }  // namespace mxg

@@ -52,7 +52,7 @@ def test_quantize_rejects_bad_shapes(lib):
     assert lib.mxfp8_quantize(FAKE, 1, 32, 36, FAKE, FAKE, None) == 3       # ld % 8
     assert lib.mxfp8_quantize(FAKE, 0, 32, 32, FAKE, FAKE, None) == 0       # empty: nothing enqueued
     assert lib.rmsnorm_mxfp8_quantize(FAKE, FAKE, -1.0, 1, 32, 32, FAKE, FAKE, None) == 1
-    assert lib.rmsnorm_mxfp8_quantize(FAKE, FAKE, 1e-6, 1, 32768, 32768, FAKE, FAKE, None) == 2
+    assert lib.rmsnorm_mxfp8_quantize(FAKE, FAKE, 1e-6, 1, 17952, 17952, FAKE, FAKE, None) == 2
 
 
 def test_gemm_and_mlp_reject_bad_shapes(lib):
