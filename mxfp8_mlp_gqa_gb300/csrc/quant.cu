@@ -69,9 +69,21 @@ __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const uint16_t* __r
   }
 }
 
+// Error-free addition (Knuth two-sum): hi + lo carries the running sum with ~48 significant
+// bits using fp32 arithmetic only (fp64 throughput on this part is a small fraction of fp32).
+__device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float x) {
+  const float s = __fadd_rn(hi, x);
+  const float bp = __fsub_rn(s, hi);
+  const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(x, bp));
+  hi = s;
+  lo = __fadd_rn(lo, e);
+}
+
 // One CTA per row; each thread keeps its 8-element chunks of x (and gamma) in registers, so
-// the row is read from memory once. Sum of squares in fp64 (each square is exact in fp64),
-// then y = bf16((x * r) * gamma) with r = fp32(1 / sqrt(mean + eps)), then the MX rule on y.
+// the row is read from memory once. Sum of squares: each square of a bf16 value is exact in
+// fp32; they are summed as a two-sum pair (~48-bit), and the ten warp partials in fp64, so the
+// fp64 mean agrees with an fp64 summation far below the fp32 rounding of r. Then
+// y = bf16((x * r) * gamma) with r = fp32(1 / sqrt(mean + eps)), then the MX rule on y.
 constexpr int kRmsThreads = 320;  // = K/8 for K = 2560: one chunk per thread
 constexpr int kRmsChunks = 7;     // chunks per thread kept in registers: K <= 8 * 320 * 7 = 17920
 
@@ -93,24 +105,30 @@ __global__ void __launch_bounds__(kRmsThreads) rmsnorm_mxfp8_quantize_kernel(con
   }
   pdl_wait();
   uint4 xw[kRmsChunks];
-  double acc = 0.0;
 #pragma unroll
   for (int i = 0; i < kRmsChunks; ++i) {
     const int c = threadIdx.x + i * kRmsThreads;
     xw[i] = c < cpr ? __ldg(reinterpret_cast<const uint4*>(xr + ((int64_t)c << 3))) : make_uint4(0, 0, 0, 0);
   }
+  float hi = 0.f, lo = 0.f;
 #pragma unroll
   for (int i = 0; i < kRmsChunks; ++i) {
+    if (i * kRmsThreads >= cpr) break;  // uniform: no work on chunk slots past the row
     float v[8];
     unpack_bf16x8(xw[i], v);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc += (double)v[j] * (double)v[j];
+    for (int j = 0; j < 8; ++j) two_sum_acc(hi, lo, __fmul_rn(v[j], v[j]));
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(MXG_FULL_MASK, acc, o);
+  for (int o = 16; o > 0; o >>= 1) {
+    const float h2 = __shfl_xor_sync(MXG_FULL_MASK, hi, o);
+    const float l2 = __shfl_xor_sync(MXG_FULL_MASK, lo, o);
+    two_sum_acc(hi, lo, h2);
+    lo = __fadd_rn(lo, l2);
+  }
   __shared__ double red[kRmsThreads / 32];
   __shared__ float r_sh;
-  if (lane == 0) red[warp] = acc;
+  if (lane == 0) red[warp] = (double)hi + (double)lo;
   __syncthreads();
   if (threadIdx.x == 0) {
     double t = 0.0;
