@@ -43,10 +43,12 @@ struct TcShape {
   static constexpr int kSfbAtoms = (BN + 127) / 128;
   static constexpr int kSfBytes = 1024 * ((512 * (1 + kSfbAtoms) + 1023) / 1024);  // keeps stages 1024-aligned
   static constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;
-  // ~96 KB ring: two CTAs fit on an SM, so that the next kernel of the step (launched early
-  // by PDL) can start streaming its weights while this one drains
+  // At least 5 stages (>= 80 KB of weights in flight per SM: the weight stream is latency-
+  // bound below that), otherwise as many as fit in ~96 KB so that small-BN kernels still fit
+  // two CTAs per SM (the next kernel, launched early by PDL, can then stream alongside).
   static constexpr int kStagesRaw = (BN >= 256 ? 200 * 1024 : 96 * 1024) / kStageBytes;
-  static constexpr int kStages = kStagesRaw > 8 ? 8 : (kStagesRaw < 2 ? 2 : kStagesRaw);
+  static constexpr int kStages = kStagesRaw > 8 ? 8 : (kStagesRaw < (BN >= 256 ? 2 : 5) ? (BN >= 256 ? 2 : 5)
+                                                                                       : kStagesRaw);
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kRS = 128 + 4;  // split-K staging [BN][kRS] (column-major, 16-byte rows)
   static constexpr int kStagingBytes =
@@ -286,16 +288,33 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
       }
       epi_bar();
       if (ok) {
+        // one lane per token: the lane holds all 32 d_ff values of its MX block, so the block
+        // max needs no shuffles and the 32 codes leave in two 16-byte stores
         const int e = warp - 2, blk = e & 1, half = e >> 1;
-        const int j0 = n0 + 32 * blk;  // d_ff index of lane 0
-        const int tb = half * (BN / 2), te = tb + BN / 2;
-        for (int t = tb; t < te; ++t) {
+        const int j0 = n0 + 32 * blk;  // first d_ff index of this warp's block
+        const float* gs = stg + (32 * blk) * (BN + 1);
+        const float* us = stg + (64 + 32 * blk) * (BN + 1);
+        for (int t = half * (BN / 2) + lane; t < (half + 1) * (BN / 2); t += 32) {
           const int m = m0 + t;
-          if (m >= a.M) break;
-          const float g = stg[(32 * blk + lane) * (BN + 1) + t];
-          const float u = stg[(64 + 32 * blk + lane) * (BN + 1) + t];
-          const float h = g / (1.f + expf(-g)) * u;
-          mx_quant_warp_store(h, a.hq + (int64_t)m * a.d_ff + j0 + lane, a.hs + (int64_t)m * (a.d_ff >> 5) + (j0 >> 5));
+          if (m >= a.M) continue;
+          float h[32];
+          float am = 0.f;
+#pragma unroll
+          for (int r = 0; r < 32; ++r) {
+            const float g = gs[r * (BN + 1) + t], u = us[r * (BN + 1) + t];
+            h[r] = g / (1.f + expf(-g)) * u;
+            am = fmaxf(am, fabsf(h[r]));
+          }
+          const int se = mx_shared_exp(am);
+          const float inv = mx_inv_scale(se);
+          uint32_t w[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            w[k] = cvt_e4m3x2(h[4 * k] * inv, h[4 * k + 1] * inv) | (cvt_e4m3x2(h[4 * k + 2] * inv, h[4 * k + 3] * inv) << 16);
+          uint4* dst = reinterpret_cast<uint4*>(a.hq + (int64_t)m * a.d_ff + j0);
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          a.hs[(int64_t)m * (a.d_ff >> 5) + (j0 >> 5)] = (uint8_t)(se + 127);
         }
       }
     }
