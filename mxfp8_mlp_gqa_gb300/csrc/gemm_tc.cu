@@ -287,7 +287,19 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
         for (int j = 0; j < 16; ++j) stg[r * (BN + 1) + c + j] = v[j];
       }
       epi_bar();
-      if (ok) {
+      if (ok && BN <= 16) {
+        // few tokens: the warp spreads one token's 32-value block over its lanes
+        const int e = warp - 2, blk = e & 1, half = e >> 1;
+        const int j0 = n0 + 32 * blk;
+        for (int t = half * (BN / 2); t < (half + 1) * (BN / 2); ++t) {
+          const int m = m0 + t;
+          if (m >= a.M) break;
+          const float g = stg[(32 * blk + lane) * (BN + 1) + t];
+          const float u = stg[(64 + 32 * blk + lane) * (BN + 1) + t];
+          const float h = g / (1.f + expf(-g)) * u;
+          mx_quant_warp_store(h, a.hq + (int64_t)m * a.d_ff + j0 + lane, a.hs + (int64_t)m * (a.d_ff >> 5) + (j0 >> 5));
+        }
+      } else if (ok) {
         // one lane per token: the lane holds all 32 d_ff values of its MX block, so the block
         // max needs no shuffles and the 32 codes leave in two 16-byte stores
         const int e = warp - 2, blk = e & 1, half = e >> 1;
