@@ -443,13 +443,15 @@ def run_profile(args):
         y = torch.empty((M, D_MODEL), dtype=torch.bfloat16, device=dev)
         fn = lambda: api.mlp_swiglu_mxfp8(xq, xs, *w13, *w2, y=y, workspace=ws)  # noqa: E731
     elif kind == "attn":
-        bs = int(arg)
-        K = torch.empty((bs, HKV, CAP, HD), dtype=torch.bfloat16, device=dev)
+        bs, _, capa = arg.partition(":")
+        bs, cap = int(bs), int(capa or CAP)
+        K = torch.empty((bs, HKV, cap, HD), dtype=torch.bfloat16, device=dev)
         V = torch.empty_like(K)
         for b in range(bs):
             K[b].copy_(rn(K[b].shape))
             V[b].copy_(rn(V[b].shape))
-        kl = torch.from_numpy(synth.kv_lens(bs, KV_LO, KV_HI, seed=0)).to(dev)
+        lens = synth.kv_lens(bs, KV_LO, min(KV_HI, cap), seed=0)
+        kl = torch.from_numpy(lens).to(dev)
         q = rn((bs, HQ, HD))
         ws = torch.empty(max(1, api.gqa_decode_attn_workspace(bs, HQ, HKV, HD, KV_HI)), dtype=torch.uint8, device=dev)
         out = torch.empty((bs, HQ, HD), dtype=torch.bfloat16, device=dev)
@@ -464,7 +466,11 @@ def run_profile(args):
         raise SystemExit(f"unknown --profile {args.profile}")
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     ms = _time_op(fn, flush, reps=args.steps, warm=args.warmup)
-    return {"profile": args.profile, "median_us": round(ms * 1e3, 2)}
+    out = {"profile": args.profile, "median_us": round(ms * 1e3, 2)}
+    if kind == "attn":
+        out["attn_bytes"] = attn_bytes(lens)
+        out["sum_kv_len"] = int(lens.sum())
+    return out
 
 
 # --------------------------------------------------------------------------- oracle (CPU) arm
@@ -574,7 +580,8 @@ def main(argv=None):
     ap.add_argument("--no-sweeps", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", default=None,
-                    help="run one kernel family only (for ncu captures): mlp:<M> | attn:<bs> | gemm:<M>x<N>x<K>")
+                    help="run one kernel family only (for ncu captures): mlp:<M> | attn:<bs>[:<cap>] | "
+                         "gemm:<M>x<N>x<K>")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
