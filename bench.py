@@ -163,6 +163,14 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# DRAM traffic of the attention split kernel per algorithmic byte, from one ncu capture of the
+# same kernel on a smaller cache (profiles/gqa_split_kernel_bs64_cap4096.md: 634.67 MB of
+# dram__bytes_read.sum + dram__bytes_write.sum for 622.54 MB of algorithmic bytes). Traffic
+# grows in proportion to the prefix tokens read, so it is scaled to the step's launch. Set to
+# None whenever the kernel changes until it is captured again.
+ATTN_TRAFFIC_PER_ALG_BYTE = 634.671104e6 / 622538752
+
+
 # --------------------------------------------------------------------------- measured peaks
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -361,7 +369,10 @@ def run_ours(args, rank, local_rank, world):
                      "bound": "hbm",
                      "achieved": round(attn_bytes_avg / (attn_ms * 1e-3) / 1e9, 1), "peak": peak_gbs,
                      "peak_source": peak_src, "unit": "GB/s",
-                     "frac": round(attn_bytes_avg / (attn_ms * 1e-3) / 1e9 / peak_gbs, 4), "traffic": None,
+                     "frac": round(attn_bytes_avg / (attn_ms * 1e-3) / 1e9 / peak_gbs, 4),
+                     "traffic": (None if ATTN_TRAFFIC_PER_ALG_BYTE is None
+                                 else int(attn_bytes_avg * ATTN_TRAFFIC_PER_ALG_BYTE)),
+                     "traffic_unit": "bytes per launch (ncu, scaled from a smaller capture)",
                      "bytes_per_launch": int(attn_bytes_avg), "us_per_launch": round(attn_ms * 1e3, 2)},
         "gpu_launches": launches_per_step(max_kv_len) * args.steps,
         "sweeps": sweeps,
