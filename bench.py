@@ -431,7 +431,58 @@ def run_sweeps(dev, flush):
         ms = _time_op(lambda: api.gqa_decode_attn(q, Kb, Vb, kl, KV_HI, 1 / math.sqrt(HD), out=out, workspace=ws),
                       flush)
         attn[str(bs)] = {"us": round(ms * 1e3, 2), "GB_s": round(attn_bytes(lens) / (ms * 1e-3) / 1e9, 1)}
-    return {"mlp_M": mlp, "attn_bs": attn}
+    del K, V
+    return {"mlp_M": mlp, "attn_bs": attn, "gemm_square": gemm_square_sweep(dev)}
+
+
+def gemm_square_sweep(dev, sizes=(1024, 2048, 4096, 8192, 16384)):
+    """Config-5 sweep: C = A' B'^T, A and B MXFP8 [N, N], bf16 C; TFLOP/s of 2 N^3 per call,
+    median of 5 timed calls after 2 warm-up calls. Alongside, cuBLAS's MXFP8 GEMM through
+    torch._scaled_mm with UE8M0 block scales where this torch build supports it (context:
+    a library kernel's practical peak on this part)."""
+    import torch
+
+    from mxfp8_mlp_gqa_gb300 import api
+
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    out = {}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timeit(fn, reps=5):
+        for _ in range(2):
+            fn()
+        ts = []
+        for _ in range(reps):
+            e0.record()
+            fn()
+            e1.record()
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    for n in sizes:
+        a = torch.randn((n, n), generator=g, device=dev).to(torch.bfloat16)
+        aq, as_ = api.mxfp8_quantize(a)
+        b = torch.randn((n, n), generator=g, device=dev).to(torch.bfloat16)
+        bq, bs_ = api.mxfp8_quantize(b)
+        del a, b
+        c = torch.empty((n, n), dtype=torch.bfloat16, device=dev)
+        ms = timeit(lambda: api.mxfp8_gemm(aq, as_, bq, bs_, c=c))
+        ent = {"us": round(ms * 1e3, 1), "TFLOP_s": round(2 * n ** 3 / (ms * 1e-3) / 1e12, 1)}
+        try:
+            fa = aq.view(torch.float8_e4m3fn)
+            fb = bq.view(torch.float8_e4m3fn)
+            sa = torch.full((((n + 127) // 128) * 128 * ((n // 32 + 3) // 4) * 4,), 127, dtype=torch.uint8,
+                            device=dev).view(torch.float8_e8m0fnu)
+            sb = sa.clone()
+            ms2 = timeit(lambda: torch._scaled_mm(fa, fb.t(), sa, sb, out_dtype=torch.bfloat16))
+            ent["cublas_mxfp8_TFLOP_s"] = round(2 * n ** 3 / (ms2 * 1e-3) / 1e12, 1)
+        except Exception as ex:  # noqa: BLE001 - context only
+            ent["cublas_mxfp8"] = f"unavailable: {type(ex).__name__}"
+        out[str(n)] = ent
+        del aq, bq, c
+    return out
 
 
 def run_profile(args):

@@ -141,9 +141,6 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
   const int g0 = (int)((int64_t)split * a.groups / a.splits);
   const int g1 = (int)((int64_t)(split + 1) * a.groups / a.splits);
   const int ng = g1 - g0;
-  // every CTA reads the same token tile; starting the K loop at a CTA-dependent group keeps the
-  // 152 CTAs on different slices of it (no L2 hot spot). The order is fixed per CTA.
-  const int rot = ng > 0 ? (int)(((unsigned)ntile * 7u + (unsigned)mtile * 3u) % (unsigned)ng) : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S::kStages; ++s) {
@@ -178,9 +175,8 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
       for (int i = 0; i < pre; ++i) {
         uint8_t* st = ring + i * S::kStageBytes;
         mbar_arrive_expect_tx(&full[i], S::kABytes + S::kBBytes);
-        const int gi = g0 + (i + rot) % ng;
-        tma_load_2d(st, &tmW, &full[i], gi * kKG, a_lo);
-        tma_load_2d(st + 64 * kKG, &tmW, &full[i], gi * kKG, a_hi);
+        tma_load_2d(st, &tmW, &full[i], (g0 + i) * kKG, a_lo);
+        tma_load_2d(st + 64 * kKG, &tmW, &full[i], (g0 + i) * kKG, a_hi);
       }
     }
     pdl_wait();
@@ -188,7 +184,7 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
       const int s = i % S::kStages;
       if (i >= S::kStages && !mbar_wait(&empty[s], ((i / S::kStages) - 1) & 1, a.err)) break;
       uint8_t* st = ring + s * S::kStageBytes;
-      const int g = g0 + (i + rot) % ng;
+      const int g = g0 + i;
       if (lane == 0) {
         if (i >= pre) {
           mbar_arrive_expect_tx(&full[s], S::kABytes + S::kBBytes);
