@@ -468,7 +468,8 @@ def gemm_square_sweep(dev, sizes=(1024, 2048, 4096, 8192, 16384)):
         bq, bs_ = api.mxfp8_quantize(b)
         del a, b
         c = torch.empty((n, n), dtype=torch.bfloat16, device=dev)
-        ms = timeit(lambda: api.mxfp8_gemm(aq, as_, bq, bs_, c=c))
+        ws = torch.zeros(max(1, api.mxfp8_gemm_workspace(n, n, n)), dtype=torch.uint8, device=dev)
+        ms = timeit(lambda: api.mxfp8_gemm(aq, as_, bq, bs_, c=c, workspace=ws))
         ent = {"us": round(ms * 1e3, 1), "TFLOP_s": round(2 * n ** 3 / (ms * 1e-3) / 1e12, 1)}
         try:
             fa = aq.view(torch.float8_e4m3fn)
@@ -523,7 +524,8 @@ def run_profile(args):
         aq, as_ = api.mxfp8_quantize(rn((M, K_)))
         bq, bs_ = api.mxfp8_quantize(rn((N, K_)))
         c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        fn = lambda: api.mxfp8_gemm(aq, as_, bq, bs_, c=c)  # noqa: E731
+        wsb = torch.zeros(max(1, api.mxfp8_gemm_workspace(M, N, K_)), dtype=torch.uint8, device=dev)
+        fn = lambda: api.mxfp8_gemm(aq, as_, bq, bs_, c=c, workspace=wsb)  # noqa: E731
     else:
         raise SystemExit(f"unknown --profile {args.profile}")
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)

@@ -75,7 +75,36 @@ struct TcArgs {
   uint16_t* out;
   int32_t* err;
   KvScatter kv;         // fused KV append of a QKV projection (kv.kc == nullptr: off)
+  // Pre-packed scales (large GEMMs): group-major 512-byte atoms [K/128][row tiles][512 B],
+  // one 1-D bulk copy per stage instead of per-lane gathers. nullptr: gather from ws / xs.
+  const uint32_t* wsp;
+  const uint32_t* xsp;
+  int rt_w, rt_x;       // 128-row tiles per group in wsp / xsp
 };
+
+// Scales [rows][K/32] (row-major) -> group-major atoms: word w of atom (g, rt) holds the four
+// k-blocks of group g of row rt*128 + (w >> 2) + 32 * (w & 3); rows past `rows` are zero.
+__global__ void __launch_bounds__(256) pack_scales_kernel(const uint8_t* __restrict__ s, int64_t rows, int64_t KB,
+                                                          int rt_pad, int groups, uint32_t* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
+  const int64_t total = (int64_t)groups * rt_pad * 128;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int w = (int)(idx & 127);
+    const int64_t t = idx >> 7;
+    const int rt = (int)(t % rt_pad), g = (int)(t / rt_pad);
+    const int64_t row = (int64_t)rt * 128 + (w >> 2) + 32 * (w & 3);
+    out[idx] = row < rows ? *reinterpret_cast<const uint32_t*>(s + row * KB + 4 * (int64_t)g) : 0u;
+  }
+}
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
 
 // Destination of output element (m, n): `out`, or -- for the K/V columns of a fused QKV
 // projection -- row kv_len[m]-1 of KV head (c / D) in the K or V cache (nullptr, with the
@@ -144,7 +173,8 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S::kStages; ++s) {
-      mbar_init(&full[s], 1 + 32);  // TMA expect-tx arrive + one cp.async arrive per producer lane
+      // TMA expect-tx arrive (+ one cp.async arrive per producer lane when scales are gathered)
+      mbar_init(&full[s], a.wsp ? 1 : 1 + 32);
       mbar_init(&empty[s], 1);
     }
     mbar_init(tmem_full, 1);
@@ -168,13 +198,14 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
       prefetch_tensormap(&tmX);
     }
     const int64_t KB = a.K >> 5;
+    const uint32_t tx = S::kABytes + S::kBBytes + (a.wsp ? 512u * (1 + S::kSfbAtoms) : 0u);
     // weight tiles of the first ring-full read nothing produced upstream: issue them before
     // waiting for the previous kernel (programmatic dependent launch)
     const int pre = ng < S::kStages ? ng : S::kStages;
     if (lane == 0) {
       for (int i = 0; i < pre; ++i) {
         uint8_t* st = ring + i * S::kStageBytes;
-        mbar_arrive_expect_tx(&full[i], S::kABytes + S::kBBytes);
+        mbar_arrive_expect_tx(&full[i], tx);
         tma_load_2d(st, &tmW, &full[i], (g0 + i) * kKG, a_lo);
         tma_load_2d(st + 64 * kKG, &tmW, &full[i], (g0 + i) * kKG, a_hi);
       }
@@ -187,13 +218,20 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
       const int g = g0 + i;
       if (lane == 0) {
         if (i >= pre) {
-          mbar_arrive_expect_tx(&full[s], S::kABytes + S::kBBytes);
+          mbar_arrive_expect_tx(&full[s], tx);
           tma_load_2d(st, &tmW, &full[s], g * kKG, a_lo);
           tma_load_2d(st + 64 * kKG, &tmW, &full[s], g * kKG, a_hi);
         }
         tma_load_2d(st + S::kABytes, &tmX, &full[s], g * kKG, m0);
       }
       uint32_t* sfa = reinterpret_cast<uint32_t*>(st + S::kABytes + S::kBBytes);
+      if (a.wsp) {
+        if (lane == 0) {
+          bulk_load(sfa, a.wsp + ((int64_t)g * a.rt_w + ntile) * 128, 512, &full[s]);
+          bulk_load(sfa + 128, a.xsp + ((int64_t)g * a.rt_x + (m0 >> 7)) * 128, 512 * S::kSfbAtoms, &full[s]);
+        }
+        continue;
+      }
 #pragma unroll
       for (int r1 = 0; r1 < 4; ++r1) {
         const int r = lane + 32 * r1;
@@ -479,9 +517,31 @@ bool tc_gemm_supported(int64_t M, int64_t N, int64_t K) {
   return M > 0 && K % kKG == 0 && N % 8 == 0 && K / kKG >= 1 && M < (1ll << 31) && N < (1ll << 31);
 }
 
+namespace {
+// Large GEMMs (256-token tiles) read pre-packed scale atoms: [K/128][rt_w][512 B] for the
+// weight operand, then [K/128][rt_x][512 B] for the token operand (rt_x padded to whole tiles).
+struct PackPlan {
+  int rt_w = 0, rt_x = 0, groups = 0;
+  size_t w_bytes = 0, bytes = 0;
+};
+PackPlan pack_plan(const Plan& p, int64_t M, int64_t N, int64_t K) {
+  PackPlan q;
+  if (p.bn != 256) return q;
+  q.groups = (int)(K / kKG);
+  q.rt_w = (int)((N + 127) / 128);
+  q.rt_x = p.mtiles * (p.bn / 128);
+  (void)M;
+  q.w_bytes = (size_t)q.groups * q.rt_w * 512;
+  q.bytes = q.w_bytes + (size_t)q.groups * q.rt_x * 512;
+  return q;
+}
+}  // namespace
+
 size_t tc_gemm_workspace(int64_t M, int64_t N, int64_t K) {
-  (void)M; (void)N; (void)K;
-  return 0;  // split-K partials are reduced inside a cluster through distributed shared memory
+  // split-K partials are reduced inside a cluster through distributed shared memory (no
+  // scratch); only large GEMMs need scratch, for their pre-packed scales
+  if (!tc_gemm_supported(M, N, K)) return 0;
+  return pack_plan(plan_gemm(M, N, K), M, N, K).bytes;
 }
 
 cudaError_t launch_mx_gemm_tc(const uint8_t* xq, const uint8_t* xs, const uint8_t* wq, const uint8_t* ws, int64_t M,
@@ -507,7 +567,20 @@ cudaError_t launch_mx_gemm_tc(const uint8_t* xq, const uint8_t* xs, const uint8_
   a.err = err;
   if (kv) a.kv = *kv;
   dim3 grid((unsigned)p.ntiles, (unsigned)p.mtiles, (unsigned)p.splits);
-  (void)workspace;
+  const PackPlan q = pack_plan(p, M, N, K);
+  if (q.bytes) {
+    uint32_t* pw = static_cast<uint32_t*>(workspace);
+    uint32_t* px = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + q.w_bytes);
+    const int64_t KB = K / 32;
+    cudaError_t e = launch_k(pack_scales_kernel, dim3(1024), dim3(256), 0, st, 1, ws, N, KB, q.rt_w, q.groups, pw);
+    if (e != cudaSuccess) return e;
+    e = launch_k(pack_scales_kernel, dim3(1024), dim3(256), 0, st, 1, xs, M, KB, q.rt_x, q.groups, px);
+    if (e != cudaSuccess) return e;
+    a.wsp = pw;
+    a.xsp = px;
+    a.rt_w = q.rt_w;
+    a.rt_x = q.rt_x;
+  }
   if (p.splits > 1) return launch_tc_bn<kEpiSplit>(p.bn, tw, tx, a, grid, st);
   return launch_tc_bn<kEpiStore>(p.bn, tw, tx, a, grid, st);
 }
