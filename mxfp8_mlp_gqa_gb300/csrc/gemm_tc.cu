@@ -34,7 +34,10 @@ namespace mxg {
 namespace {
 
 constexpr int kKG = 128;  // K elements per stage: one 4-block group of scales
-enum { kEpiStore = 0, kEpiSplit = 1, kEpiSwiGLU = 2 };
+// kEpiPair: bf16 store epilogue; CTA pairs along x (a 2-CTA cluster sharing one token tile)
+// each TMA-load half of the token tile and multicast it to both, and release a stage only when
+// both CTAs' MMAs are done with it.
+enum { kEpiStore = 0, kEpiSplit = 1, kEpiSwiGLU = 2, kEpiPair = 3 };
 
 template <int BN>
 struct TcShape {
@@ -175,7 +178,7 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
     for (int s = 0; s < S::kStages; ++s) {
       // TMA expect-tx arrive (+ one cp.async arrive per producer lane when scales are gathered)
       mbar_init(&full[s], a.wsp ? 1 : 1 + 32);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], EPI == kEpiPair ? 2 : 1);
     }
     mbar_init(tmem_full, 1);
     fence_mbar_init();
@@ -186,6 +189,7 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
   }
   tc::fence_before_sync();
   __syncthreads();
+  if (EPI == kEpiPair) cluster_sync_all();  // the peer's barriers exist before any multicast lands
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_sh;
   const uint32_t t_d = tmem, t_sfa = tmem + BN, t_sfb = tmem + BN + 4;
@@ -222,7 +226,16 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
           tma_load_2d(st, &tmW, &full[s], g * kKG, a_lo);
           tma_load_2d(st + 64 * kKG, &tmW, &full[s], g * kKG, a_hi);
         }
-        tma_load_2d(st + S::kABytes, &tmX, &full[s], g * kKG, m0);
+        if (EPI == kEpiPair) {
+          const uint32_t rank = blockIdx.x & 1;  // CTA rank in the x-pair cluster
+          tma_load_2d_mc(st + S::kABytes + rank * (BN / 2) * kKG, &tmX, &full[s], g * kKG, m0 + (int)rank * (BN / 2),
+                         (uint16_t)0x3);
+        } else if (BN > 128) {  // the token map's box is 128 rows for 256-token tiles
+          tma_load_2d(st + S::kABytes, &tmX, &full[s], g * kKG, m0);
+          tma_load_2d(st + S::kABytes + 128 * kKG, &tmX, &full[s], g * kKG, m0 + 128);
+        } else {
+          tma_load_2d(st + S::kABytes, &tmX, &full[s], g * kKG, m0);
+        }
       }
       uint32_t* sfa = reinterpret_cast<uint32_t*>(st + S::kABytes + S::kBBytes);
       if (a.wsp) {
@@ -267,7 +280,10 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
         for (int kk = 0; kk < 4; ++kk)
           tc::mma_mxf8(t_d, tc::desc_k128_sw128(sa + kk * 32), tc::desc_k128_sw128(sb + kk * 32),
                        tc::idesc_mxf8(BN, kk, kk), t_sfa, t_sfb, (i > 0 || kk > 0) ? 1u : 0u);
-        tc::commit(&empty[s]);
+        if (EPI == kEpiPair)
+          tc::commit_mc(&empty[s], (uint16_t)0x3);  // the peer also writes this slot (multicast)
+        else
+          tc::commit(&empty[s]);
       }
       tc::commit(tmem_full);
     }
@@ -280,7 +296,7 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
     const bool ok = mbar_wait(tmem_full, 0, a.err);
     tc::fence_after_sync();
     const uint32_t trow = t_d + ((uint32_t)(32 * q) << 16);
-    if (EPI == kEpiStore) {
+    if (EPI == kEpiStore || EPI == kEpiPair) {
       const int n = n0 + r;
       const bool nv = n < a.N;
       for (int c = 0; c < BN; c += 16) {
@@ -408,6 +424,7 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
     }
     cluster_sync_all();  // keep this CTA's shared memory alive until every reader is done
   }
+  if (EPI == kEpiPair) cluster_sync_all();  // no CTA leaves while its peer may still signal it
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, S::kTmemCols);
@@ -463,6 +480,7 @@ Plan plan_gemm(int64_t M, int64_t N, int64_t K) {
   Plan p;
   p.bn = M > 1024 ? 256 : pick_bn(M);
   p.ntiles = (int)((N + 127) / 128);
+  if (p.bn == 256) p.ntiles = (p.ntiles + 1) & ~1;  // CTA pairs along x share a token tile
   p.mtiles = (int)((M + p.bn - 1) / p.bn);
   const int groups = (int)(K / kKG);
   const int64_t ctas = (int64_t)p.ntiles * p.mtiles;
@@ -487,8 +505,8 @@ cudaError_t launch_tc(const CUtensorMap& tw, const CUtensorMap& tx, const TcArgs
   cudaError_t e = cudaFuncSetAttribute(mx_gemm_tc_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        S::kSmemBytes);
   if (e != cudaSuccess) return e;
-  return launch_k(mx_gemm_tc_kernel<BN, EPI>, grid, dim3(192), S::kSmemBytes, st, EPI == kEpiSplit ? grid.z : 1u, tw,
-                  tx, a);
+  const dim3 cluster = EPI == kEpiSplit ? dim3(1, 1, grid.z) : (EPI == kEpiPair ? dim3(2, 1, 1) : dim3(1, 1, 1));
+  return launch_kc(mx_gemm_tc_kernel<BN, EPI>, grid, dim3(192), S::kSmemBytes, st, cluster, tw, tx, a);
 }
 
 template <int EPI>
@@ -499,12 +517,13 @@ cudaError_t launch_tc_bn(int bn, const CUtensorMap& tw, const CUtensorMap& tx, c
     case 32: return launch_tc<32, EPI>(tw, tx, a, grid, st);
     case 64: return launch_tc<64, EPI>(tw, tx, a, grid, st);
     case 128: return launch_tc<128, EPI>(tw, tx, a, grid, st);
-    default: return launch_tc<256, EPI == kEpiSwiGLU ? kEpiStore : EPI>(tw, tx, a, grid, st);
+    default: return launch_tc<256, EPI == kEpiSwiGLU ? kEpiStore : (EPI == kEpiStore ? kEpiPair : EPI)>(tw, tx, a, grid, st);
   }
 }
 
 bool maps(CUtensorMap* tw, CUtensorMap* tx, const uint8_t* wq, int64_t wrows, const uint8_t* xq, int64_t M, int64_t K,
           int bn) {
+  if (bn > 128) bn /= 2;  // 256-token tiles are loaded as two multicast halves
   return make_tensor_map_2d(tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)K, (uint64_t)wrows, (uint64_t)K, kKG, 64,
                             CU_TENSOR_MAP_SWIZZLE_128B) &&
          make_tensor_map_2d(tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, (uint64_t)K, (uint64_t)M, (uint64_t)K, kKG,

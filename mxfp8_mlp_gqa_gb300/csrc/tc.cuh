@@ -74,6 +74,15 @@ __device__ __forceinline__ void commit(uint64_t* bar) {
                : "memory");
 }
 
+// As commit(), arriving on the mbarrier at the same offset in every CTA of cta_mask.
+__device__ __forceinline__ void commit_mc(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Each thread of the warp reads its TMEM lane (quadrant of the warp), 16 / 32 consecutive

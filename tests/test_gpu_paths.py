@@ -28,7 +28,7 @@ def path(request):
 
 @pytest.mark.parametrize("M,N,K", [(1, 256, 128), (16, 256, 512), (64, 2560, 4096), (77, 136, 256),
                                    (128, 6144, 2560), (200, 512, 384), (300, 1024, 1024), (1100, 264, 384),
-                                   (2048, 520, 512)])
+                                   (2048, 520, 512), (2048, 256, 1024)])
 def test_gemm_structured_scales(path, M, N, K):
     g = synth.rng(11, M * 7 + N)
     xq, wq = _codes((M, K), g), _codes((N, K), g)
