@@ -58,11 +58,16 @@ struct TcShape {
       128 * (BN + 1) * 4 > BN * kRS * 4 ? 128 * (BN + 1) * 4 : BN * kRS * 4;  // max(SwiGLU, split-K)
   static constexpr int kBodyBytes = kRingBytes > kStagingBytes ? kRingBytes : kStagingBytes;
   static constexpr int kSmemBytes = 1024 + kBodyBytes + 8 * (2 * kStages + 1) + 16;
-  static constexpr uint32_t kTmemCols = BN + 4 * (1 + kSfbAtoms) <= 32    ? 32
-                                        : BN + 4 * (1 + kSfbAtoms) <= 64  ? 64
-                                        : BN + 4 * (1 + kSfbAtoms) <= 128 ? 128
-                                        : BN + 4 * (1 + kSfbAtoms) <= 256 ? 256
-                                                                          : 512;
+  // scale atoms rotate through kSfSlots TMEM slots, so the copy for stage i+1 never
+  // overwrites columns that MMAs of stage i may still be reading
+  static constexpr int kSfSlots = 4;
+  static constexpr int kSfCols = 4 * (1 + kSfbAtoms);
+  static constexpr int kTmemNeed = BN + kSfSlots * kSfCols;
+  static constexpr uint32_t kTmemCols = kTmemNeed <= 32    ? 32
+                                        : kTmemNeed <= 64  ? 64
+                                        : kTmemNeed <= 128 ? 128
+                                        : kTmemNeed <= 256 ? 256
+                                                           : 512;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -192,7 +197,7 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
   if (EPI == kEpiPair) cluster_sync_all();  // the peer's barriers exist before any multicast lands
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_sh;
-  const uint32_t t_d = tmem, t_sfa = tmem + BN, t_sfb = tmem + BN + 4;
+  const uint32_t t_d = tmem;
 
   pdl_trigger();
   if (warp == 0) {
@@ -268,8 +273,9 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
       for (int i = 0; i < ng; ++i) {
         const int s = i % S::kStages;
         if (!mbar_wait(&full[s], (i / S::kStages) & 1, a.err)) break;
-        fence_proxy_async_smem();  // cp.async (generic proxy) scale words -> tcgen05.cp (async proxy)
+        if (!a.wsp) fence_proxy_async_smem();  // cp.async (generic proxy) scale words -> tcgen05.cp (async proxy)
         tc::fence_after_sync();
+        const uint32_t t_sfa = tmem + BN + (uint32_t)((i % S::kSfSlots) * S::kSfCols), t_sfb = t_sfa + 4;
         uint8_t* st = ring + s * S::kStageBytes;
         const uint32_t sa = smem_u32(st), sb = smem_u32(st + S::kABytes);
         const uint32_t ssf = smem_u32(st + S::kABytes + S::kBBytes);
