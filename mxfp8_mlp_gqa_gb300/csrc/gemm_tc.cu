@@ -169,20 +169,7 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
   uint32_t* tmem_sh = reinterpret_cast<uint32_t*>(tmem_full + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int ntile = blockIdx.x, mtile = blockIdx.y;
-  const int split = blockIdx.z;
-  if (EPI == kEpiPair) {
-    // grouped raster order over CTA pairs: consecutive pairs walk 8 token tiles down before
-    // moving to the next pair of feature tiles, so the operands of one wave stay in L2
-    constexpr int GM = 8;
-    const int npairs = gridDim.x >> 1, mt = gridDim.y;
-    const int pid = (blockIdx.x >> 1) + npairs * blockIdx.y;
-    const int group = pid / (GM * npairs), first_m = group * GM;
-    const int gm = mt - first_m < GM ? mt - first_m : GM;
-    const int q = pid - group * GM * npairs;
-    mtile = first_m + q % gm;
-    ntile = 2 * (q / gm) + (blockIdx.x & 1);
-  }
+  const int ntile = blockIdx.x, mtile = blockIdx.y, split = blockIdx.z;
   const int m0 = mtile * BN;
   const int n0 = EPI == kEpiSwiGLU ? ntile * 64 : ntile * 128;
   const int a_lo = n0;                                         // weight rows of tile rows 0..63
