@@ -34,10 +34,7 @@ namespace mxg {
 namespace {
 
 constexpr int kKG = 128;  // K elements per stage: one 4-block group of scales
-// kEpiPair: bf16 store epilogue; CTA pairs along x (a 2-CTA cluster sharing one token tile)
-// each TMA-load half of the token tile and multicast it to both, and release a stage only when
-// both CTAs' MMAs are done with it.
-enum { kEpiStore = 0, kEpiSplit = 1, kEpiSwiGLU = 2, kEpiPair = 3 };
+enum { kEpiStore = 0, kEpiSplit = 1, kEpiSwiGLU = 2 };
 
 template <int BN>
 struct TcShape {
@@ -88,6 +85,7 @@ struct TcArgs {
   const uint32_t* wsp;
   const uint32_t* xsp;
   int rt_w, rt_x;       // 128-row tiles per group in wsp / xsp
+  int tma_out;          // pair kernel: plain bf16 output written by TMA stores
 };
 
 // Scales [rows][K/32] (row-major) -> group-major atoms: word w of atom (g, rt) holds the four
@@ -183,7 +181,7 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
     for (int s = 0; s < S::kStages; ++s) {
       // TMA expect-tx arrive (+ one cp.async arrive per producer lane when scales are gathered)
       mbar_init(&full[s], a.wsp ? 1 : 1 + 32);
-      mbar_init(&empty[s], EPI == kEpiPair ? 2 : 1);
+      mbar_init(&empty[s], 1);
     }
     mbar_init(tmem_full, 1);
     fence_mbar_init();
@@ -194,7 +192,6 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (EPI == kEpiPair) cluster_sync_all();  // the peer's barriers exist before any multicast lands
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_sh;
   const uint32_t t_d = tmem;
@@ -231,11 +228,7 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
           tma_load_2d(st, &tmW, &full[s], g * kKG, a_lo);
           tma_load_2d(st + 64 * kKG, &tmW, &full[s], g * kKG, a_hi);
         }
-        if (EPI == kEpiPair) {
-          const uint32_t rank = blockIdx.x & 1;  // CTA rank in the x-pair cluster
-          tma_load_2d_mc(st + S::kABytes + rank * (BN / 2) * kKG, &tmX, &full[s], g * kKG, m0 + (int)rank * (BN / 2),
-                         (uint16_t)0x3);
-        } else if (BN > 128) {  // the token map's box is 128 rows for 256-token tiles
+        if (BN > 128) {  // the token map's box is 128 rows for 256-token tiles
           tma_load_2d(st + S::kABytes, &tmX, &full[s], g * kKG, m0);
           tma_load_2d(st + S::kABytes + 128 * kKG, &tmX, &full[s], g * kKG, m0 + 128);
         } else {
@@ -286,10 +279,7 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
         for (int kk = 0; kk < 4; ++kk)
           tc::mma_mxf8(t_d, tc::desc_k128_sw128(sa + kk * 32), tc::desc_k128_sw128(sb + kk * 32),
                        tc::idesc_mxf8(BN, kk, kk), t_sfa, t_sfb, (i > 0 || kk > 0) ? 1u : 0u);
-        if (EPI == kEpiPair)
-          tc::commit_mc(&empty[s], (uint16_t)0x3);  // the peer also writes this slot (multicast)
-        else
-          tc::commit(&empty[s]);
+        tc::commit(&empty[s]);
       }
       tc::commit(tmem_full);
     }
@@ -302,7 +292,7 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
     const bool ok = mbar_wait(tmem_full, 0, a.err);
     tc::fence_after_sync();
     const uint32_t trow = t_d + ((uint32_t)(32 * q) << 16);
-    if (EPI == kEpiStore || EPI == kEpiPair) {
+    if (EPI == kEpiStore) {
       const int n = n0 + r;
       const bool nv = n < a.N;
       for (int c = 0; c < BN; c += 16) {
@@ -430,10 +420,210 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
     }
     cluster_sync_all();  // keep this CTA's shared memory alive until every reader is done
   }
-  if (EPI == kEpiPair) cluster_sync_all();  // no CTA leaves while its peer may still signal it
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, S::kTmemCols);
+}
+
+// Large GEMMs (M > 1024): one M=256 block-scaled MMA per CTA pair (cta_group::2). The pair
+// (a 2-CTA cluster along x) owns 256 weight rows x 256 tokens; each CTA stages its own 128
+// weight rows and one 128-token half of the token tile, so a stage is 32 KB per CTA and six
+// stages are in flight. Scales arrive pre-packed: each CTA holds the atom of its own weight
+// rows and both atoms of the 256 tokens. Every load of both CTAs completes on the even CTA's
+// `full` barrier (TMA with cta_group::2), so the even CTA's MMA thread learns of the odd CTA's
+// data from the copy engine itself; its commits arrive on the `empty` / `tmem_full` barriers
+// of both CTAs. (A thread-level remote arrive with release semantics in this loop costs
+// microseconds per stage and throttles the pipeline below a third of the copy rate.) Each
+// CTA's epilogue writes its own 128 feature rows (bf16, + residual).
+struct Tc2Shape {
+  static constexpr int kABytes = 128 * kKG;  // this CTA's weight rows
+  static constexpr int kBBytes = 128 * kKG;  // this CTA's token half
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = 6;
+  static constexpr int kSfBytes = 3 * 512;  // weight atom + two token atoms
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kSfRingBytes = kStages * kSfBytes;
+  static constexpr int kSmemBytes = 1024 + kRingBytes + kSfRingBytes + 8 * (2 * kStages + 1) + 16;
+  static constexpr int kSfSlots = 4;
+  static constexpr int kSfCols = 12;  // 4 (weight scales) + 8 (token scales)
+  static constexpr uint32_t kTmemCols = 512;  // 256 accumulator columns + kSfSlots * kSfCols
+  static_assert(256 + kSfSlots * kSfCols <= 512, "tensor memory budget");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t mapa_shared(const void* local, uint32_t rank) {
+  uint32_t raddr;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(smem_u32(local)), "r"(rank));
+  return raddr;
+}
+
+__global__ void __launch_bounds__(192) mx_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                             const __grid_constant__ CUtensorMap tmX,
+                                                             const __grid_constant__ CUtensorMap tmSW,
+                                                             const __grid_constant__ CUtensorMap tmSX,
+                                                             const __grid_constant__ CUtensorMap tmO, const TcArgs a) {
+  using S = Tc2Shape;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  uint8_t* sfring = smem + S::kRingBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sfring + S::kSfRingBytes);  // used in the even CTA
+  uint64_t* empty = full + S::kStages;
+  uint64_t* tmem_full = empty + S::kStages;
+  uint32_t* tmem_sh = reinterpret_cast<uint32_t*>(tmem_full + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const int ntile = blockIdx.x, m0 = blockIdx.y * 256;
+  const int n0 = ntile * 128;
+  const int ng = a.groups;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tmem_full, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc2(tmem_sh, S::kTmemCols);
+    tc::tmem_relinquish2();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers and TMEM exist before any cross-CTA signal
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_sh;
+
+  pdl_trigger();
+  if (warp == 0) {
+    // ----------------------------------------------------------------- producer (both CTAs)
+    if (lane == 0) {
+      prefetch_tensormap(&tmW);
+      prefetch_tensormap(&tmX);
+      prefetch_tensormap(&tmSW);
+      prefetch_tensormap(&tmSX);
+      // the even CTA expects the bytes of both CTAs; the odd CTA's copies complete there too
+      constexpr uint32_t tx = 2 * (S::kStageBytes + S::kSfBytes);
+      const int pre = ng < S::kStages ? ng : S::kStages;
+      for (int i = 0; i < pre; ++i) {  // weights read nothing produced upstream
+        uint8_t* st = ring + i * S::kStageBytes;
+        const uint32_t fb = mapa_shared(&full[i], 0);
+        if (rank == 0) mbar_arrive_expect_tx(&full[i], tx);
+        tma_load_2d_pair(st, &tmW, fb, i * kKG, n0);
+        tma_load_2d_pair(st + 64 * kKG, &tmW, fb, i * kKG, n0 + 64);
+      }
+      pdl_wait();
+      int i = 0;
+      for (; i < ng; ++i) {
+        const int s = i % S::kStages;
+        if (i >= S::kStages && !mbar_wait(&empty[s], ((i / S::kStages) - 1) & 1, a.err)) break;
+        uint8_t* st = ring + s * S::kStageBytes;
+        const uint32_t fb = mapa_shared(&full[s], 0);
+        if (i >= pre) {
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], tx);
+          tma_load_2d_pair(st, &tmW, fb, i * kKG, n0);
+          tma_load_2d_pair(st + 64 * kKG, &tmW, fb, i * kKG, n0 + 64);
+        }
+        tma_load_2d_pair(st + S::kABytes, &tmX, fb, i * kKG, m0 + 128 * (int)rank);
+        uint8_t* sf = sfring + s * S::kSfBytes;
+        tma_load_2d_pair(sf, &tmSW, fb, ntile * 128, i);
+        tma_load_2d_pair(sf + 512, &tmSX, fb, (m0 >> 7) * 128, i);
+      }
+      // Before this CTA may exit, every MMA that reads its stages has signalled (the last phase
+      // of each stage's `empty`); those MMAs were issued only after all copies had landed.
+      for (int j = i - S::kStages < 0 ? 0 : i - S::kStages; j < i; ++j)
+        if (!mbar_wait(&empty[j % S::kStages], (j / S::kStages) & 1, a.err)) break;
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA issuer (even CTA)
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc0 = tc::idesc_mxf8(256, 0, 0, 256);
+      for (int i = 0; i < ng; ++i) {
+        const int s = i % S::kStages;
+        if (!mbar_wait(&full[s], (i / S::kStages) & 1, a.err)) break;
+        tc::fence_after_sync();
+        const uint32_t t_sfa = tmem + 256 + (uint32_t)((i % S::kSfSlots) * S::kSfCols), t_sfb = t_sfa + 4;
+        const uint32_t sa = smem_u32(ring + s * S::kStageBytes), sb = sa + S::kABytes;
+        const uint32_t ssf = smem_u32(sfring + s * S::kSfBytes);
+        tc::cp_sf_atom2(t_sfa, tc::desc_sf_atom(ssf));
+        tc::cp_sf_atom2(t_sfb, tc::desc_sf_atom(ssf + 512));
+        tc::cp_sf_atom2(t_sfb + 4, tc::desc_sf_atom(ssf + 1024));
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma_mxf8_2(tmem, tc::desc_k128_sw128(sa + kk * 32), tc::desc_k128_sw128(sb + kk * 32),
+                         idesc0 | ((uint32_t)kk << 4) | ((uint32_t)kk << 29), t_sfa, t_sfb, (i > 0 || kk > 0) ? 1u : 0u);
+        tc::commit2_mc(&empty[s], (uint16_t)0x3);
+      }
+      tc::commit2_mc(tmem_full, (uint16_t)0x3);
+    }
+    __syncwarp();
+  } else {
+    // ----------------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int r = 32 * q + lane;
+    pdl_wait();
+    // one thread polls the accumulator barrier for the four epilogue warps
+    __shared__ int ok_sh;
+    if (threadIdx.x == 64) ok_sh = mbar_wait(tmem_full, 0, a.err) ? 1 : 0;
+    epi_bar();
+    const bool ok = ok_sh != 0;
+    tc::fence_after_sync();
+    const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
+    const int n = n0 + r;
+    if (a.tma_out) {
+      // plain store: the warp stages each 16-token chunk of its 32 features ([16][32] bf16, 1 KB,
+      // conflict-free row writes) in the now idle operand ring and hands it to a TMA store
+      uint16_t* stg = reinterpret_cast<uint16_t*>(ring) + (size_t)q * (256 * 32);
+      for (int c = 0; c < 256 && ok; c += 16) {
+        float v[16];
+        tc::ld16(trow + c, v);
+        tc::wait_ld();
+        uint16_t* ch = stg + c * 32;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) ch[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
+        fence_proxy_async_smem();  // generic-proxy writes -> the TMA engine's reads
+        __syncwarp();
+        if (lane == 0 && n0 + 32 * q < a.N && m0 + c < a.M) {  // boxes are clipped at the edges
+          tma_store_2d(&tmO, ch, n0 + 32 * q, m0 + c);
+          bulk_commit_group();
+        }
+      }
+      if (lane == 0) bulk_wait_group0();
+      __syncwarp();
+    } else {
+      const bool nv = n < a.N;
+      for (int c = 0; c < 256; c += 16) {
+        float v[16];
+        tc::ld16(trow + c, v);
+        tc::wait_ld();
+        if (!ok) continue;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int m = m0 + c + j;
+          if (m < a.M && nv) {
+            float y = v[j];
+            if (a.residual) y += __bfloat162float(__ushort_as_bfloat16(a.residual[(int64_t)m * a.N + n]));
+            uint16_t* dst = out_ptr(a, m, n);
+            if (dst) *dst = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+          }
+        }
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  cluster_sync_all();  // neither CTA frees its TMEM or leaves while the pair may still use it
+  tc::fence_after_sync();
+  if (warp == 1) tc::tmem_dealloc2(tmem, S::kTmemCols);
 }
 
 // ---------------------------------------------------------------------------------- host
@@ -486,7 +676,7 @@ Plan plan_gemm(int64_t M, int64_t N, int64_t K) {
   Plan p;
   p.bn = M > 1024 ? 256 : pick_bn(M);
   p.ntiles = (int)((N + 127) / 128);
-  if (p.bn == 256) p.ntiles = (p.ntiles + 1) & ~1;  // CTA pairs along x share a token tile
+  if (p.bn == 256) p.ntiles = (p.ntiles + 1) & ~1;  // CTA pairs along x (one M=256 MMA per pair)
   p.mtiles = (int)((M + p.bn - 1) / p.bn);
   const int groups = (int)(K / kKG);
   const int64_t ctas = (int64_t)p.ntiles * p.mtiles;
@@ -511,8 +701,32 @@ cudaError_t launch_tc(const CUtensorMap& tw, const CUtensorMap& tx, const TcArgs
   cudaError_t e = cudaFuncSetAttribute(mx_gemm_tc_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        S::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const dim3 cluster = EPI == kEpiSplit ? dim3(1, 1, grid.z) : (EPI == kEpiPair ? dim3(2, 1, 1) : dim3(1, 1, 1));
+  const dim3 cluster = EPI == kEpiSplit ? dim3(1, 1, grid.z) : dim3(1, 1, 1);
   return launch_kc(mx_gemm_tc_kernel<BN, EPI>, grid, dim3(192), S::kSmemBytes, st, cluster, tw, tx, a);
+}
+
+cudaError_t launch_tc2(const CUtensorMap& tw, const CUtensorMap& tx, const TcArgs& a, dim3 grid, cudaStream_t st) {
+  using S = Tc2Shape;
+  if (!a.wsp || (grid.x & 1) || grid.z != 1) return cudaErrorInvalidValue;
+  // packed scale atoms as 2-D u32 tensors [K/128][row tiles * 128]: one 512-byte atom (weights)
+  // or two adjacent atoms (the 256 tokens) per load
+  CUtensorMap tsw, tsx;
+  if (!make_tensor_map_2d(&tsw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.wsp, (uint64_t)a.rt_w * 128, (uint64_t)a.groups,
+                          (uint64_t)a.rt_w * 512, 128, 1, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_tensor_map_2d(&tsx, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.xsp, (uint64_t)a.rt_x * 128, (uint64_t)a.groups,
+                          (uint64_t)a.rt_x * 512, 256, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  // bf16 output [M][N] for the staged epilogue (boxes of 32 features x 16 tokens); a residual,
+  // a KV scatter or an output the copy engine cannot address keeps the per-element stores
+  CUtensorMap tso{};
+  TcArgs b = a;
+  b.tma_out = a.residual == nullptr && a.kv.kc == nullptr &&
+              make_tensor_map_2d(&tso, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.out, (uint64_t)a.N, (uint64_t)a.M,
+                                 (uint64_t)a.N * 2, 32, 16, CU_TENSOR_MAP_SWIZZLE_NONE);
+  cudaError_t e =
+      cudaFuncSetAttribute(mx_gemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return launch_kc(mx_gemm_tc2_kernel, grid, dim3(192), S::kSmemBytes, st, dim3(2, 1, 1), tw, tx, tsw, tsx, tso, b);
 }
 
 template <int EPI>
@@ -523,13 +737,16 @@ cudaError_t launch_tc_bn(int bn, const CUtensorMap& tw, const CUtensorMap& tx, c
     case 32: return launch_tc<32, EPI>(tw, tx, a, grid, st);
     case 64: return launch_tc<64, EPI>(tw, tx, a, grid, st);
     case 128: return launch_tc<128, EPI>(tw, tx, a, grid, st);
-    default: return launch_tc<256, EPI == kEpiSwiGLU ? kEpiStore : (EPI == kEpiStore ? kEpiPair : EPI)>(tw, tx, a, grid, st);
+    default:
+      if constexpr (EPI == kEpiStore) return launch_tc2(tw, tx, a, grid, st);
+      else if constexpr (EPI == kEpiSplit) return launch_tc<256, kEpiSplit>(tw, tx, a, grid, st);
+      else return cudaErrorInvalidValue;  // the SwiGLU epilogue tiles at most 128 tokens
   }
 }
 
 bool maps(CUtensorMap* tw, CUtensorMap* tx, const uint8_t* wq, int64_t wrows, const uint8_t* xq, int64_t M, int64_t K,
           int bn) {
-  if (bn > 128) bn /= 2;  // 256-token tiles are loaded as two multicast halves
+  if (bn > 128) bn /= 2;  // 256-token tiles are loaded as two 128-row halves
   return make_tensor_map_2d(tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)K, (uint64_t)wrows, (uint64_t)K, kKG, 64,
                             CU_TENSOR_MAP_SWIZZLE_128B) &&
          make_tensor_map_2d(tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, (uint64_t)K, (uint64_t)M, (uint64_t)K, kKG,
@@ -553,7 +770,8 @@ PackPlan pack_plan(const Plan& p, int64_t M, int64_t N, int64_t K) {
   PackPlan q;
   if (p.bn != 256) return q;
   q.groups = (int)(K / kKG);
-  q.rt_w = (int)((N + 127) / 128);
+  q.rt_w = p.ntiles;  // even: the CTA pairs of the M=256 MMA read whole pairs of weight tiles
+  (void)N;
   q.rt_x = p.mtiles * (p.bn / 128);
   (void)M;
   q.w_bytes = (size_t)q.groups * q.rt_w * 512;

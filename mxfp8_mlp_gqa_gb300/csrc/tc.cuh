@@ -47,8 +47,8 @@ __device__ __forceinline__ uint64_t desc_sf_atom(uint32_t saddr) { return smem_d
 // both K-major, fp32 accumulation, UE8M0 scales (bit 23), M = 128 (M>>4 at bits 24-28),
 // N>>3 at bits 17-22, and the byte of the 32-bit scale word used by this MMA for A
 // (bits 29-30) and B (bits 4-5).
-__host__ __device__ constexpr uint32_t idesc_mxf8(int n, int sfa_id, int sfb_id) {
-  return ((uint32_t)sfb_id << 4) | ((uint32_t)(n >> 3) << 17) | (1u << 23) | ((uint32_t)(128 >> 4) << 24) |
+__host__ __device__ constexpr uint32_t idesc_mxf8(int n, int sfa_id, int sfb_id, int m = 128) {
+  return ((uint32_t)sfb_id << 4) | ((uint32_t)(n >> 3) << 17) | (1u << 23) | ((uint32_t)(m >> 4) << 24) |
          ((uint32_t)sfa_id << 29);
 }
 
@@ -78,6 +78,43 @@ __device__ __forceinline__ void commit(uint64_t* bar) {
 __device__ __forceinline__ void commit_mc(uint64_t* bar, uint16_t cta_mask) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// ------------------------------------------------------------------ CTA-pair (cta_group::2) forms
+// One warp of each CTA of the pair allocates / frees together; the columns are the same in
+// both CTAs. MMAs, scale copies and commits are issued by one thread of the even CTA only:
+// an M=256 MMA reads rows 0..127 of A and the first N/2 rows of B from the even CTA's shared
+// memory and the rest from the odd CTA's, at the same offsets, and writes D rows 0..127 /
+// 128..255 into the tensor memory of the even / odd CTA.
+__device__ __forceinline__ void tmem_alloc2(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish2() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void mma_mxf8_2(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+// Scale atom copy of the pair: each CTA's atom (same shared-memory offset) into its own TMEM.
+__device__ __forceinline__ void cp_sf_atom2(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void commit2_mc(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
           smem_u32(bar)),
       "h"(cta_mask)
       : "memory");

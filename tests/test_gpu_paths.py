@@ -74,3 +74,21 @@ def test_split_k_cluster_reduction_is_deterministic():
     outs = [api.mxfp8_gemm(d(xq), d(xs), d(wq), d(ws)).clone() for _ in range(3)]
     assert all(torch.equal(outs[0].view(torch.int16), o.view(torch.int16)) for o in outs[1:])
     assert_float_close(host_f64(outs[0]), ops.mx_gemm(xq, xs, wq, ws))
+
+
+@pytest.mark.parametrize("M,N,K", [(1100, 264, 384), (2048, 520, 512), (1500, 1032, 256), (1025, 8, 128)])
+def test_large_gemm_plain_store(M, N, K):
+    # more than 1024 tokens and no residual: the CTA-pair kernel writes its tile through staged
+    # copy-engine stores, clipped at ragged M / N edges; every output element must be written
+    g = synth.rng(12, M + N)
+    xq, wq = _codes((M, K), g), _codes((N, K), g)
+    xs = (115 + (np.arange(M)[:, None] * 5 + np.arange(K // 32)[None, :]) % 23).astype(np.uint8)
+    ws = (110 + (np.arange(N)[:, None] * 7 + np.arange(K // 32)[None, :] * 3) % 29).astype(np.uint8)
+    d = lambda a: torch.from_numpy(a).cuda()  # noqa: E731
+    c = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    api.mxfp8_gemm(d(xq), d(xs), d(wq), d(ws), c=c)
+    got = host_f64(c)
+    assert not np.isnan(got).any()
+    ref = ops.mx_gemm(xq, xs, wq, ws)
+    assert np.linalg.norm(got - ref) <= 1e-2 * np.linalg.norm(ref)
+    assert np.abs(got - ref).max() <= 1e-2 * np.abs(ref).max()
