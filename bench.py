@@ -379,7 +379,7 @@ def run_ours(args, rank, local_rank, world):
     }
 
 
-def _time_op(fn, flush, reps=10, warm=3):
+def _time_op(fn, flush, reps=30, warm=3):
     import torch
 
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -388,12 +388,17 @@ def _time_op(fn, flush, reps=10, warm=3):
     out = []
     for _ in range(reps):
         flush.zero_()
+        # keep the GPU busy (~20 us) while the host enqueues fn, so that host-side work (argument
+        # checks, tensor-map encoding, the launch) stays outside the device-timed interval
+        torch.cuda._sleep(40000)
         e0.record()
         fn()
         e1.record()
         e1.synchronize()
         out.append(e0.elapsed_time(e1))
-    return statistics.median(out)
+    # the event clock ticks in ~2 us steps on this part: the mean over many launches resolves
+    # finer than any single interval (the median would stay on the grid)
+    return statistics.fmean(out)
 
 
 def run_sweeps(dev, flush):
@@ -410,7 +415,7 @@ def run_sweeps(dev, flush):
     for M in (1, 2, 4, 8, 16, 32, 64, 128):
         xq, xs = api.mxfp8_quantize(rn((M, D_MODEL)))
         y = torch.empty((M, D_MODEL), dtype=torch.bfloat16, device=dev)
-        ws = torch.empty(api.mlp_swiglu_mxfp8_workspace(M, D_MODEL, D_FF), dtype=torch.uint8, device=dev)
+        ws = torch.zeros(api.mlp_swiglu_mxfp8_workspace(M, D_MODEL, D_FF), dtype=torch.uint8, device=dev)
         ms = _time_op(lambda: api.mlp_swiglu_mxfp8(xq, xs, *w13, *w2, y=y, workspace=ws), flush)
         mlp[str(M)] = {"us": round(ms * 1e3, 2), "GB_s": round(mlp_bytes(M) / (ms * 1e-3) / 1e9, 1)}
     del w13, w2
@@ -526,6 +531,17 @@ def run_profile(args):
         c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         wsb = torch.zeros(max(1, api.mxfp8_gemm_workspace(M, N, K_)), dtype=torch.uint8, device=dev)
         fn = lambda: api.mxfp8_gemm(aq, as_, bq, bs_, c=c, workspace=wsb)  # noqa: E731
+    elif kind == "cublas":
+        # context only: cuBLAS's MXFP8 GEMM (torch._scaled_mm, UE8M0 block scales of 2^0) on
+        # the same shape, for a side-by-side capture of a library kernel
+        M, N, K_ = (int(v) for v in arg.split("x"))
+        fa = api.mxfp8_quantize(rn((M, K_)))[0].view(torch.float8_e4m3fn)
+        fb = api.mxfp8_quantize(rn((N, K_)))[0].view(torch.float8_e4m3fn)
+        sa = torch.full((((M + 127) // 128) * 128 * ((K_ // 32 + 3) // 4) * 4,), 127, dtype=torch.uint8,
+                        device=dev).view(torch.float8_e8m0fnu)
+        sb = torch.full((((N + 127) // 128) * 128 * ((K_ // 32 + 3) // 4) * 4,), 127, dtype=torch.uint8,
+                        device=dev).view(torch.float8_e8m0fnu)
+        fn = lambda: torch._scaled_mm(fa, fb.t(), sa, sb, out_dtype=torch.bfloat16)  # noqa: E731
     else:
         raise SystemExit(f"unknown --profile {args.profile}")
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -645,7 +661,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", default=None,
                     help="run one kernel family only (for ncu captures): mlp:<M> | attn:<bs>[:<cap>] | "
-                         "gemm:<M>x<N>x<K>")
+                         "gemm:<M>x<N>x<K> | cublas:<M>x<N>x<K> (library kernel, context)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -57,6 +57,11 @@ __device__ __forceinline__ void mx_quant_warp_store(float v, uint8_t* q_dst, uin
   if ((threadIdx.x & 31) == 0) *s_dst = (uint8_t)(s + 127);
 }
 
+// SwiGLU activation in fp32, silu(g) * u = g / (1 + e^-g) * u, with the hardware exp and
+// divide intrinsics (a few fp32 ulp); every SwiGLU epilogue of the library uses this one
+// definition, so all kernel paths produce the same bits.
+__device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g, 1.f + __expf(-g)) * u; }
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(256) mx_gemm_simt_kernel(const uint8_t* __rest
       const int m = m0 + r;
       if (m >= M) break;
       const float g = Cs[r * 65 + lane], u = Cs[r * 65 + 32 + lane];
-      const float h = g / (1.f + expf(-g)) * u;
+      const float h = silu_mul(g, u);
       float a = fabsf(h);
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) a = fmaxf(a, __shfl_xor_sync(MXG_FULL_MASK, a, off));

@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
           if (m >= a.M) break;
           const float g = stg[(32 * blk + lane) * (BN + 1) + t];
           const float u = stg[(64 + 32 * blk + lane) * (BN + 1) + t];
-          const float h = g / (1.f + expf(-g)) * u;
+          const float h = silu_mul(g, u);
           mx_quant_warp_store(h, a.hq + (int64_t)m * a.d_ff + j0 + lane, a.hs + (int64_t)m * (a.d_ff >> 5) + (j0 >> 5));
         }
       } else if (ok) {
@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
 #pragma unroll
           for (int r = 0; r < 32; ++r) {
             const float g = gs[r * (BN + 1) + t], u = us[r * (BN + 1) + t];
-            h[r] = g / (1.f + expf(-g)) * u;
+            h[r] = silu_mul(g, u);
             am = fmaxf(am, fabsf(h[r]));
           }
           const int se = mx_shared_exp(am);
@@ -517,8 +517,7 @@ __global__ void __launch_bounds__(192) mx_gemm_tc2_kernel(const __grid_constant_
         uint8_t* st = ring + i * S::kStageBytes;
         const uint32_t fb = mapa_shared(&full[i], 0);
         if (rank == 0) mbar_arrive_expect_tx(&full[i], tx);
-        tma_load_2d_pair(st, &tmW, fb, i * kKG, n0);
-        tma_load_2d_pair(st + 64 * kKG, &tmW, fb, i * kKG, n0 + 64);
+        tma_load_2d_pair(st, &tmW, fb, i * kKG, n0);  // the weight map's box is 128 rows here
       }
       pdl_wait();
       int i = 0;
@@ -530,7 +529,6 @@ __global__ void __launch_bounds__(192) mx_gemm_tc2_kernel(const __grid_constant_
         if (i >= pre) {
           if (rank == 0) mbar_arrive_expect_tx(&full[s], tx);
           tma_load_2d_pair(st, &tmW, fb, i * kKG, n0);
-          tma_load_2d_pair(st + 64 * kKG, &tmW, fb, i * kKG, n0 + 64);
         }
         tma_load_2d_pair(st + S::kABytes, &tmX, fb, i * kKG, m0 + 128 * (int)rank);
         uint8_t* sf = sfring + s * S::kSfBytes;
@@ -745,9 +743,9 @@ cudaError_t launch_tc_bn(int bn, const CUtensorMap& tw, const CUtensorMap& tx, c
 }
 
 bool maps(CUtensorMap* tw, CUtensorMap* tx, const uint8_t* wq, int64_t wrows, const uint8_t* xq, int64_t M, int64_t K,
-          int bn) {
+          int bn, uint32_t wbox = 64) {
   if (bn > 128) bn /= 2;  // 256-token tiles are loaded as two 128-row halves
-  return make_tensor_map_2d(tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)K, (uint64_t)wrows, (uint64_t)K, kKG, 64,
+  return make_tensor_map_2d(tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)K, (uint64_t)wrows, (uint64_t)K, kKG, wbox,
                             CU_TENSOR_MAP_SWIZZLE_128B) &&
          make_tensor_map_2d(tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, (uint64_t)K, (uint64_t)M, (uint64_t)K, kKG,
                             (uint32_t)bn, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -793,7 +791,8 @@ cudaError_t launch_mx_gemm_tc(const uint8_t* xq, const uint8_t* xs, const uint8_
   const Plan p = plan_gemm(M, N, K);
   CUtensorMap tw, tx;
   *unsupported = false;
-  if (!maps(&tw, &tx, wq, N, xq, M, K, p.bn)) {
+  // the CTA-pair kernel (256-token tiles, no split) loads its 128 weight rows as one box
+  if (!maps(&tw, &tx, wq, N, xq, M, K, p.bn, p.bn == 256 && p.splits == 1 ? 128 : 64)) {
     *unsupported = true;
     return cudaSuccess;
   }
