@@ -437,7 +437,41 @@ def run_sweeps(dev, flush):
                       flush)
         attn[str(bs)] = {"us": round(ms * 1e3, 2), "GB_s": round(attn_bytes(lens) / (ms * 1e-3) / 1e9, 1)}
     del K, V
-    return {"mlp_M": mlp, "attn_bs": attn, "gemm_square": gemm_square_sweep(dev)}
+    return {"mlp_M": mlp, "attn_bs": attn, "attn_paged_bs64": paged_attn_sweep(dev, rn, flush),
+            "gemm_square": gemm_square_sweep(dev)}
+
+
+def paged_attn_sweep(dev, rn, flush, bs=BS, page_sizes=(64, 128, 256)):
+    """Paged decode attention at bs=64 over the bench's ragged lengths, pages placed at a seeded
+    random permutation of the pool (with 10 % spare pages); GB/s over the same algorithmic bytes
+    as the contiguous kernel."""
+    import torch
+
+    from mxfp8_mlp_gqa_gb300 import api, synth
+
+    lens = synth.kv_lens(bs, KV_LO, KV_HI, seed=0)
+    q = rn((bs, HQ, HD))
+    kl = torch.from_numpy(lens).to(dev)
+    out = torch.empty((bs, HQ, HD), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(1, api.gqa_decode_attn_workspace(bs, HQ, HKV, HD, KV_HI)), dtype=torch.uint8, device=dev)
+    res = {}
+    for ps in page_sizes:
+        need = (lens.astype(np.int64) + ps - 1) // ps
+        num_pages = int(need.sum() * 11 // 10)
+        perm = np.random.default_rng(ps).permutation(num_pages).astype(np.int32)
+        table = np.full((bs, (KV_HI + ps - 1) // ps), -1, np.int32)
+        k = 0
+        for b in range(bs):
+            table[b, :need[b]] = perm[k:k + need[b]]
+            k += int(need[b])
+        Kp = rn((num_pages, HKV, ps, HD))
+        Vp = rn((num_pages, HKV, ps, HD))
+        tb = torch.from_numpy(table).to(dev)
+        ms = _time_op(lambda: api.gqa_decode_attn_paged(q, Kp, Vp, tb, kl, KV_HI, 1 / math.sqrt(HD), out=out,
+                                                        workspace=ws), flush)
+        res[str(ps)] = {"us": round(ms * 1e3, 2), "GB_s": round(attn_bytes(lens) / (ms * 1e-3) / 1e9, 1)}
+        del Kp, Vp
+    return res
 
 
 def gemm_square_sweep(dev, sizes=(1024, 2048, 4096, 8192, 16384)):

@@ -206,6 +206,38 @@ mxg_status kv_append(void* k_cache, void* v_cache, const void* k_new, const void
                      void* stream);
 
 /*
+ * gqa_decode_attn_paged -- gqa_decode_attn over paged K/V caches ([S2.1] "What's Open
+ * Source": paged decode with native GQA by stride-0 K/V broadcast; [FSKV] §5: only the active
+ * prefix is read).
+ *   k_pool, v_pool bf16 [num_pages, Hkv, page_size, D] (contiguous): a page holds page_size
+ *            consecutive positions of one sequence for all Hkv heads.
+ *   block_table int32 [bs, max_pages] on the device: positions [j*page_size, (j+1)*page_size)
+ *            of sequence b live in pool page block_table[b*max_pages + j]; only the first
+ *            ceil(kv_len[b] / page_size) entries of a row are read.
+ *   page_size a multiple of 64; max_kv_len <= max_pages * page_size; the pools hold fewer
+ *            than 2^31 rows (num_pages * Hkv * page_size).
+ *   err_flag as gqa_decode_attn with capacity max_pages * page_size; also MXG_EDEVICE for a
+ *            page id outside [0, num_pages) (that 64-token tile is read as zeros).
+ *   q, ld_q, kv_len, out, scale, workspace: as gqa_decode_attn (same workspace size).
+ */
+mxg_status gqa_decode_attn_paged(const void* q, int64_t ld_q, const void* k_pool, const void* v_pool,
+                                 const int32_t* block_table, int64_t max_pages, int64_t page_size, int64_t num_pages,
+                                 const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D,
+                                 int64_t max_kv_len, float scale, void* out, int32_t* err_flag, void* workspace,
+                                 size_t ws_bytes, void* stream);
+
+/*
+ * kv_append_paged -- kv_append into paged pools: the row of position kv_len[b]-1 of sequence
+ * b lives in page block_table[b*max_pages + (kv_len[b]-1) / page_size] at offset
+ * (kv_len[b]-1) % page_size. Bit-exact copy. err_flag: MXG_EDEVICE for kv_len outside
+ * [1, max_pages*page_size] or a page id outside [0, num_pages) (that row is skipped).
+ */
+mxg_status kv_append_paged(void* k_pool, void* v_pool, const int32_t* block_table, int64_t max_pages,
+                           int64_t page_size, int64_t num_pages, const void* k_new, const void* v_new, int64_t ld_new,
+                           const int32_t* kv_len, int64_t bs, int64_t Hkv, int64_t D, int32_t* err_flag,
+                           void* stream);
+
+/*
  * prev_tokens_shift -- in-place slide of the Dual-AR previous-tokens window ([S2.1]
  * "DualAR: S2-Specific Batching Constraints": prev int32 [bs, W, cw], next_tokens int32
  * [bs, cw], strict shape/dtype contract). prev[b, w] <- prev[b, w+1] for w < W-1 and

@@ -48,6 +48,10 @@ _SIGS = {
                                                c_i64, c_f32, c_vp, c_vp, c_vp]),
     "kv_append": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_i64, c_vp, c_i64, c_i64, c_i64, c_i64, c_vp, c_vp]),
     "prev_tokens_shift": (ctypes.c_int, [c_vp, c_vp, c_i64, c_i64, c_i64, c_vp]),
+    "gqa_decode_attn_paged": (ctypes.c_int, [c_vp, c_i64, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_i64, c_i64,
+                                             c_i64, c_i64, c_i64, c_f32, c_vp, c_vp, c_vp, c_sz, c_vp]),
+    "kv_append_paged": (ctypes.c_int, [c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_i64, c_vp, c_i64, c_i64,
+                                       c_i64, c_vp, c_vp]),
 }
 
 
@@ -279,6 +283,48 @@ def gqa_decode_attn(q, k_cache, v_cache, kv_len, max_kv_len, scale, out=None, er
           int(max_kv_len), float(scale), _ptr(out), _ptr(oq), _ptr(os), _ptr(err), _ptr(workspace), ws_bytes,
           _stream())
     return out, oq, os
+
+
+def gqa_decode_attn_paged(q, k_pool, v_pool, block_table, kv_len, max_kv_len, scale, out=None, err=None,
+                          workspace=None):
+    """Paged decode attention: q bf16 [bs, Hq, D]; pools bf16 [num_pages, Hkv, page_size, D];
+    block_table int32 [bs, max_pages] (page ids) and kv_len int32 [bs] on the device."""
+    _check(k_pool, "k_pool", torch.bfloat16, ndim=4)
+    num_pages, Hkv, page_size, D = k_pool.shape
+    _check(v_pool, "v_pool", torch.bfloat16, (num_pages, Hkv, page_size, D))
+    _check(block_table, "block_table", torch.int32, ndim=2)
+    bs, max_pages = block_table.shape
+    _check(kv_len, "kv_len", torch.int32, (bs,))
+    _check(q, "q", torch.bfloat16, ndim=3)
+    Hq = q.shape[1]
+    _check(q, "q", torch.bfloat16, (bs, Hq, D))
+    out = _out(out, "out", torch.bfloat16, (bs, Hq, D), k_pool.device)
+    if err is not None:
+        _check(err, "err", torch.int32, (1,))
+    need = gqa_decode_attn_workspace(bs, Hq, Hkv, D, max_kv_len)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=k_pool.device)
+    ws_bytes = 0 if workspace is None else workspace.numel()
+    _call("gqa_decode_attn_paged", _ptr(q), Hq * D, _ptr(k_pool), _ptr(v_pool), _ptr(block_table), max_pages,
+          page_size, num_pages, _ptr(kv_len), bs, Hq, Hkv, D, int(max_kv_len), float(scale), _ptr(out), _ptr(err),
+          _ptr(workspace), ws_bytes, _stream())
+    return out
+
+
+def kv_append_paged(k_pool, v_pool, block_table, k_new, v_new, kv_len, err=None):
+    """kv_append into paged pools [num_pages, Hkv, page_size, D]; k_new/v_new bf16 [bs, Hkv, D]."""
+    _check(k_pool, "k_pool", torch.bfloat16, ndim=4)
+    num_pages, Hkv, page_size, D = k_pool.shape
+    _check(v_pool, "v_pool", torch.bfloat16, (num_pages, Hkv, page_size, D))
+    _check(block_table, "block_table", torch.int32, ndim=2)
+    bs, max_pages = block_table.shape
+    _check(kv_len, "kv_len", torch.int32, (bs,))
+    _check(k_new, "k_new", torch.bfloat16, (bs, Hkv, D))
+    _check(v_new, "v_new", torch.bfloat16, (bs, Hkv, D))
+    if err is not None:
+        _check(err, "err", torch.int32, (1,))
+    _call("kv_append_paged", _ptr(k_pool), _ptr(v_pool), _ptr(block_table), max_pages, page_size, num_pages,
+          _ptr(k_new), _ptr(v_new), Hkv * D, _ptr(kv_len), bs, Hkv, D, _ptr(err), _stream())
 
 
 def gqa_decode_attn_noalloc(q, k_cache, v_cache, kv_len, max_kv_len, scale, out):

@@ -172,20 +172,22 @@ namespace {
 mxg_status attn_call(const void* q, int64_t ld_q, const void* k_cache, const void* v_cache, const int32_t* kv_len,
                      int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t cap, int64_t max_kv_len, float scale,
                      void* out, uint8_t* oq, uint8_t* os, int32_t* err_flag, void* workspace, size_t ws_bytes,
-                     void* stream) {
+                     void* stream, const KvPages* pages = nullptr) {
   if (!q || !k_cache || !v_cache || !kv_len || !out) return MXG_EINVAL;
   if (!(scale > 0.f) || !(scale < 1e30f)) return MXG_EINVAL;
   if (bs < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || Hq / Hkv > 8 || (D != 64 && D != 128) || cap <= 0 ||
       max_kv_len <= 0 || ld_q < Hq * D)
     return MXG_ESHAPE;
-  if (bs * Hkv * cap >= ((int64_t)1 << 31) || bs * Hkv > 65535 || max_kv_len > ((int64_t)1 << 30)) return MXG_ESHAPE;
+  // TMA row coordinates are 32-bit: the cache (or page pool) has < 2^31 rows
+  const int64_t rows_total = pages ? pages->num_pages * Hkv * pages->page_size : bs * Hkv * cap;
+  if (rows_total >= ((int64_t)1 << 31) || bs * Hkv > 65535 || max_kv_len > ((int64_t)1 << 30)) return MXG_ESHAPE;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || ld_q % 8) return MXG_EALIGN;
   if (bs == 0) return MXG_OK;
   const size_t need = attn_workspace_bytes(bs, Hq, Hkv, D, max_kv_len);
   if (need && (!workspace || ws_bytes < need)) return MXG_EWORKSPACE;
   if (need && !aligned16(workspace)) return MXG_EALIGN;
   CUtensorMap tk, tv;
-  const uint64_t rows = (uint64_t)(bs * Hkv * cap);
+  const uint64_t rows = (uint64_t)rows_total;
   if (!make_tensor_map_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_cache, (uint64_t)D, rows, (uint64_t)D * 2, 64, 64,
                           CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tensor_map_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v_cache, (uint64_t)D, rows, (uint64_t)D * 2, 64, 64,
@@ -193,7 +195,15 @@ mxg_status attn_call(const void* q, int64_t ld_q, const void* k_cache, const voi
     return MXG_ENOTSUP;
   return launched(launch_gqa_decode_attn(tk, tv, static_cast<const uint16_t*>(q), ld_q, kv_len, bs, Hq, Hkv, D, cap,
                                          max_kv_len, scale, static_cast<uint16_t*>(out), err_flag, workspace,
-                                         (cudaStream_t)stream, oq, os));
+                                         (cudaStream_t)stream, oq, os, pages));
+}
+
+// The page-table arguments shared by the paged entry points; 0 if valid.
+mxg_status check_pages(const int32_t* table, int64_t max_pages, int64_t page_size, int64_t num_pages) {
+  if (!table) return MXG_EINVAL;
+  if (max_pages <= 0 || num_pages <= 0 || page_size <= 0 || page_size % 64 || max_pages * page_size >= ((int64_t)1 << 31))
+    return MXG_ESHAPE;
+  return MXG_OK;
 }
 
 }  // namespace
@@ -213,6 +223,23 @@ mxg_status gqa_decode_attn_mxfp8(const void* q, int64_t ld_q, const void* k_cach
   if (bs > 0 && (!oq || !os)) return MXG_EINVAL;
   return attn_call(q, ld_q, k_cache, v_cache, kv_len, bs, Hq, Hkv, D, cap, max_kv_len, scale, out, oq, os, err_flag,
                    workspace, ws_bytes, stream);
+}
+
+mxg_status gqa_decode_attn_paged(const void* q, int64_t ld_q, const void* k_pool, const void* v_pool,
+                                 const int32_t* block_table, int64_t max_pages, int64_t page_size, int64_t num_pages,
+                                 const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D,
+                                 int64_t max_kv_len, float scale, void* out, int32_t* err_flag, void* workspace,
+                                 size_t ws_bytes, void* stream) {
+  const mxg_status c = check_pages(block_table, max_pages, page_size, num_pages);
+  if (c != MXG_OK) return c;
+  if (max_kv_len > max_pages * page_size) return MXG_ESHAPE;
+  KvPages pg;
+  pg.table = block_table;
+  pg.max_pages = (int)max_pages;
+  pg.page_size = (int)page_size;
+  pg.num_pages = num_pages;
+  return attn_call(q, ld_q, k_pool, v_pool, kv_len, bs, Hq, Hkv, D, max_pages * page_size, max_kv_len, scale, out,
+                   nullptr, nullptr, err_flag, workspace, ws_bytes, stream, &pg);
 }
 
 mxg_status mxfp8_gemm_qkv_kv_append(const uint8_t* xq, const uint8_t* xs, const uint8_t* wq, const uint8_t* ws,
@@ -255,6 +282,26 @@ mxg_status kv_append(void* k_cache, void* v_cache, const void* k_new, const void
   return launched(launch_kv_append(static_cast<uint16_t*>(k_cache), static_cast<uint16_t*>(v_cache),
                                    static_cast<const uint16_t*>(k_new), static_cast<const uint16_t*>(v_new), ld_new,
                                    kv_len, bs, Hkv, D, cap, err_flag, (cudaStream_t)stream));
+}
+
+mxg_status kv_append_paged(void* k_pool, void* v_pool, const int32_t* block_table, int64_t max_pages,
+                           int64_t page_size, int64_t num_pages, const void* k_new, const void* v_new, int64_t ld_new,
+                           const int32_t* kv_len, int64_t bs, int64_t Hkv, int64_t D, int32_t* err_flag, void* stream) {
+  const mxg_status c = check_pages(block_table, max_pages, page_size, num_pages);
+  if (c != MXG_OK) return c;
+  if (!k_pool || !v_pool || !k_new || !v_new || !kv_len) return MXG_EINVAL;
+  if (bs < 0 || Hkv <= 0 || D <= 0 || D % 8 || D > 256 || ld_new < Hkv * D || bs * Hkv > (1 << 26)) return MXG_ESHAPE;
+  if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k_new) || !aligned16(v_new) || ld_new % 8)
+    return MXG_EALIGN;
+  if (bs == 0) return MXG_OK;
+  KvPages pg;
+  pg.table = block_table;
+  pg.max_pages = (int)max_pages;
+  pg.page_size = (int)page_size;
+  pg.num_pages = num_pages;
+  return launched(launch_kv_append(static_cast<uint16_t*>(k_pool), static_cast<uint16_t*>(v_pool),
+                                   static_cast<const uint16_t*>(k_new), static_cast<const uint16_t*>(v_new), ld_new,
+                                   kv_len, bs, Hkv, D, max_pages * page_size, err_flag, (cudaStream_t)stream, &pg));
 }
 
 mxg_status prev_tokens_shift(int32_t* prev, const int32_t* next_tokens, int64_t bs, int64_t W, int64_t cw,

@@ -28,6 +28,7 @@ namespace mxg {
 namespace {
 
 constexpr int kTileTok = 64;     // tokens per pipeline stage
+constexpr int kMaxSplitTiles = 16;  // a split covers at most 1024 tokens (attn_chunk)
 constexpr int kConsumers = 4;    // consumer warps (16 tokens each per tile)
 constexpr int kThreads = (kConsumers + 1) * 32;
 
@@ -66,6 +67,12 @@ struct SplitParams {
   uint8_t* oq;       // optional MXFP8 copy of out ([bs, Hq*D] E4M3 + [bs, Hq*D/32] UE8M0)
   uint8_t* os;
   int32_t* err;
+  // Paged caches (table != nullptr): K/V rows of position t of sequence b, head g live at row
+  // (page * Hkv + g) * page_size + t % page_size of a [num_pages, Hkv, page_size, D] pool, with
+  // page = table[b * max_pages + t / page_size]. Otherwise [bs, Hkv, cap, D] (row bg * cap + t).
+  const int32_t* table;
+  int max_pages, page_size;
+  int64_t num_pages;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -113,7 +120,7 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
   if (t0 >= n) return;
   const int t1 = min(n, t0 + p.chunk);
   const int ntiles = (t1 - t0 + kTileTok - 1) / kTileTok;
-  const int row0 = (int)((int64_t)bg * p.cap + t0);  // host guarantees bs*Hkv*cap < 2^31
+  const int row0 = (int)((int64_t)bg * p.cap + t0);  // host guarantees bs*Hkv*cap < 2^31 (contiguous)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S::kStages; ++s) {
@@ -126,6 +133,25 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
 
   if (warp == kConsumers) {
     // ------------------------------------------------------------- producer
+    // Paged caches: the warp looks up the page of every tile of the split at once (one round
+    // trip for the table instead of one per tile on the copy issue path). A 64-token tile never
+    // straddles a page (page_size % 64 == 0 and tile starts are multiples of 64).
+    __shared__ int tile_row[kMaxSplitTiles];
+    if (p.table) {
+      for (int i = lane; i < ntiles; i += 32) {
+        const int t = t0 + i * kTileTok;
+        const int page = p.table[(int64_t)b * p.max_pages + t / p.page_size];
+        int row;
+        if (page < 0 || page >= p.num_pages) {
+          set_error(p.err, MXG_EDEVICE);
+          row = (int)(p.num_pages * p.Hkv * p.page_size);  // past the pool: the copy engine reads zeros
+        } else {
+          row = (int)(((int64_t)page * p.Hkv + g) * p.page_size + t % p.page_size);
+        }
+        tile_row[i] = row;
+      }
+      __syncwarp();
+    }
     if (lane == 0) {
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
@@ -133,13 +159,14 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
       for (int i = 0; i < ntiles; ++i) {
         const int s = i % S::kStages;
         if (i >= S::kStages && !mbar_wait(&empty[s], ((i / S::kStages) - 1) & 1, p.err)) break;
+        const int row = p.table ? tile_row[i] : row0 + i * kTileTok;
         mbar_arrive_expect_tx(&full[s], S::kStageBytes);
         uint8_t* kt = ring + s * S::kStageBytes;
         uint8_t* vt = kt + S::kTileBytes;
 #pragma unroll
         for (int h = 0; h < S::kHalves; ++h) {
-          tma_load_2d_hint(kt + h * kTileTok * 128, &tmK, &full[s], h * 64, row0 + i * kTileTok, pol);
-          tma_load_2d_hint(vt + h * kTileTok * 128, &tmV, &full[s], h * 64, row0 + i * kTileTok, pol);
+          tma_load_2d_hint(kt + h * kTileTok * 128, &tmK, &full[s], h * 64, row, pol);
+          tma_load_2d_hint(vt + h * kTileTok * 128, &tmV, &full[s], h * 64, row, pol);
         }
       }
     }
@@ -355,7 +382,7 @@ int attn_chunk(int64_t bs, int64_t Hkv, int64_t max_kv_len) {
   int64_t c = (bs * Hkv * max_kv_len + 2999) / 3000;
   c = (c + kTileTok - 1) / kTileTok * kTileTok;
   if (c < kTileTok) c = kTileTok;
-  if (c > 1024) c = 1024;
+  if (c > kMaxSplitTiles * kTileTok) c = kMaxSplitTiles * kTileTok;
   return (int)c;
 }
 
@@ -369,7 +396,7 @@ size_t attn_workspace_bytes(int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int6
 cudaError_t launch_gqa_decode_attn(const CUtensorMap& tmK, const CUtensorMap& tmV, const uint16_t* q, int64_t ld_q,
                                    const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t cap,
                                    int64_t max_kv_len, float scale, uint16_t* out, int32_t* err, void* ws,
-                                   cudaStream_t st, uint8_t* oq, uint8_t* os) {
+                                   cudaStream_t st, uint8_t* oq, uint8_t* os, const KvPages* pages) {
   const int chunk = attn_chunk(bs, Hkv, max_kv_len);
   const int ms = (int)((max_kv_len + chunk - 1) / chunk);
   SplitParams p;
@@ -390,6 +417,10 @@ cudaError_t launch_gqa_decode_attn(const CUtensorMap& tmK, const CUtensorMap& tm
   p.oq = oq;
   p.os = os;
   p.err = err;
+  p.table = pages ? pages->table : nullptr;
+  p.max_pages = pages ? pages->max_pages : 0;
+  p.page_size = pages ? pages->page_size : 0;
+  p.num_pages = pages ? pages->num_pages : 0;
   dim3 grid((unsigned)ms, (unsigned)(bs * Hkv));
   cudaError_t e;
   if (D == 128) {

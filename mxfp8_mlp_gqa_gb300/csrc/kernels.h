@@ -14,16 +14,24 @@ cudaError_t launch_rmsnorm_mxfp8_quantize(const uint16_t* x, const uint16_t* gam
 
 cudaError_t launch_prev_tokens_shift(int32_t* prev, const int32_t* next, int64_t bs, int64_t W, int64_t cw,
                                      cudaStream_t st);
+struct KvPages;
 cudaError_t launch_kv_append(uint16_t* kc, uint16_t* vc, const uint16_t* kn, const uint16_t* vn, int64_t ld_new,
                              const int32_t* kv_len, int64_t bs, int64_t Hkv, int64_t D, int64_t cap, int32_t* err,
-                             cudaStream_t st);
+                             cudaStream_t st, const KvPages* pages = nullptr);
 
 int attn_chunk(int64_t bs, int64_t Hkv, int64_t max_kv_len);
 size_t attn_workspace_bytes(int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t max_kv_len);
+// Paged KV caches: pools [num_pages, Hkv, page_size, D]; table [bs, max_pages] of page ids.
+struct KvPages {
+  const int32_t* table = nullptr;
+  int max_pages = 0, page_size = 0;
+  int64_t num_pages = 0;
+};
 cudaError_t launch_gqa_decode_attn(const CUtensorMap& tmK, const CUtensorMap& tmV, const uint16_t* q, int64_t ld_q,
                                    const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t cap,
                                    int64_t max_kv_len, float scale, uint16_t* out, int32_t* err, void* ws,
-                                   cudaStream_t st, uint8_t* oq = nullptr, uint8_t* os = nullptr);
+                                   cudaStream_t st, uint8_t* oq = nullptr, uint8_t* os = nullptr,
+                                   const KvPages* pages = nullptr);
 
 cudaError_t launch_mx_gemm_simt(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs,
                                 int64_t M, int64_t N, int64_t K, const uint16_t* res, uint16_t* c, cudaStream_t st);

@@ -25,12 +25,13 @@ __global__ void __launch_bounds__(256) prev_tokens_shift_kernel(int32_t* __restr
 }
 
 // [FSKV] §5 (kv_cache.update, in place): K/V rows of this step land at position kv_len-1.
-// One warp per (sequence, kv head); each lane moves 16 bytes of K and of V.
+// One warp per (sequence, kv head); each lane moves 16 bytes of K and of V. With a page table
+// the row is looked up as in the paged attention (a bad page id sets the error flag, no write).
 __global__ void __launch_bounds__(256) kv_append_kernel(uint16_t* __restrict__ kc, uint16_t* __restrict__ vc,
                                                         const uint16_t* __restrict__ kn,
                                                         const uint16_t* __restrict__ vn, int64_t ld_new,
                                                         const int32_t* __restrict__ kv_len, int bs, int Hkv, int D,
-                                                        int64_t cap, int32_t* err) {
+                                                        int64_t cap, int32_t* err, KvPages pg) {
   pdl_trigger();
   pdl_wait();
   const int gw = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
@@ -42,7 +43,15 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint16_t* __restrict__ k
     if (lane == 0 && g == 0) set_error(err, MXG_EDEVICE);
     return;
   }
-  const int64_t dst = (((int64_t)b * Hkv + g) * cap + (n - 1)) * D;
+  int64_t dst = (((int64_t)b * Hkv + g) * cap + (n - 1)) * D;
+  if (pg.table) {
+    const int page = pg.table[(int64_t)b * pg.max_pages + (n - 1) / pg.page_size];
+    if (page < 0 || page >= pg.num_pages) {
+      if (lane == 0 && g == 0) set_error(err, MXG_EDEVICE);
+      return;
+    }
+    dst = (((int64_t)page * Hkv + g) * pg.page_size + (n - 1) % pg.page_size) * D;
+  }
   const int64_t src = (int64_t)b * ld_new + (int64_t)g * D;
   for (int i = lane * 8; i < D; i += 256) {
     *reinterpret_cast<uint4*>(kc + dst + i) = *reinterpret_cast<const uint4*>(kn + src + i);
@@ -58,11 +67,12 @@ cudaError_t launch_prev_tokens_shift(int32_t* prev, const int32_t* next, int64_t
 
 cudaError_t launch_kv_append(uint16_t* kc, uint16_t* vc, const uint16_t* kn, const uint16_t* vn, int64_t ld_new,
                              const int32_t* kv_len, int64_t bs, int64_t Hkv, int64_t D, int64_t cap, int32_t* err,
-                             cudaStream_t st) {
+                             cudaStream_t st, const KvPages* pages) {
   const int64_t warps = bs * Hkv;
   const int64_t blocks = (warps * 32 + 255) / 256;
+  const KvPages pg = pages ? *pages : KvPages{};
   return launch_k(kv_append_kernel, dim3((unsigned)blocks), dim3(256), 0, st, 1, kc, vc, kn, vn, ld_new, kv_len,
-                  (int)bs, (int)Hkv, (int)D, cap, err);
+                  (int)bs, (int)Hkv, (int)D, cap, err, pg);
 }
 
 }  // namespace mxg

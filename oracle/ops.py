@@ -139,6 +139,39 @@ def kv_append(k_cache, v_cache, k_new, v_new, kv_len):
     return k_cache, v_cache
 
 
+def paged_prefix(pool, block_table, kv_len, page_size) -> list:
+    """Each sequence's active prefix [Hkv, kv_len_b, D] gathered from a paged pool
+    [num_pages, Hkv, page_size, D]: position t of sequence b is row t % page_size of pool
+    page block_table[b, t // page_size] ([S2.1] "What's Open Source": paged decode)."""
+    out = []
+    for b, n in enumerate(np.asarray(kv_len)):
+        n = int(n)
+        pref = np.zeros((pool.shape[1], n, pool.shape[3]), dtype=pool.dtype)
+        for t in range(n):
+            pref[:, t, :] = pool[int(block_table[b, t // page_size]), :, t % page_size, :]
+        out.append(pref)
+    return out
+
+
+def gqa_decode_attention_paged(q, k_pool, v_pool, block_table, kv_len, page_size, scale) -> np.ndarray:
+    """Decode attention over paged caches: the plain decode attention of each sequence's
+    prefix gathered through its page table."""
+    return gqa_decode_attention(q, paged_prefix(k_pool, block_table, kv_len, page_size),
+                                paged_prefix(v_pool, block_table, kv_len, page_size), scale)
+
+
+def kv_append_paged(k_pool, v_pool, block_table, k_new, v_new, kv_len, page_size):
+    """kv_append into paged pools: position kv_len-1 of sequence b is row
+    (kv_len-1) % page_size of page block_table[b, (kv_len-1) // page_size]."""
+    k_pool = k_pool.copy()
+    v_pool = v_pool.copy()
+    for b, n in enumerate(np.asarray(kv_len)):
+        pg = int(block_table[b, (int(n) - 1) // page_size])
+        k_pool[pg, :, (int(n) - 1) % page_size, :] = k_new[b]
+        v_pool[pg, :, (int(n) - 1) % page_size, :] = v_new[b]
+    return k_pool, v_pool
+
+
 # --------------------------------------------------------------------------- prev window
 def prev_tokens_shift(prev, next_tokens) -> np.ndarray:
     """Slide the Dual-AR previous-tokens window by one frame ([S2.1] "DualAR:

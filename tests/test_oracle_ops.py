@@ -236,6 +236,69 @@ def test_kv_append_brute_force():
     assert np.array_equal(v2[1, :, 5], vn[1]) and np.count_nonzero(k2) == np.count_nonzero(kn)
 
 
+def _scatter_to_pages(prefix, page_size, num_pages, rng):
+    """Independent construction of a paged pool: each sequence's prefix cut into pages placed
+    at random distinct pool pages, every other pool entry +-1e4."""
+    Hkv, D = prefix[0].shape[0], prefix[0].shape[2]
+    pool = np.where(np.arange(num_pages * Hkv * page_size * D) % 2 == 0, 1e4, -1e4).reshape(
+        num_pages, Hkv, page_size, D)
+    need = [(p.shape[1] + page_size - 1) // page_size for p in prefix]
+    perm = rng.permutation(num_pages)[:sum(need)]
+    table = np.full((len(prefix), max(need) + 1), -1, np.int32)
+    k = 0
+    for b, p in enumerate(prefix):
+        for j in range(need[b]):
+            seg = p[:, j * page_size:(j + 1) * page_size, :]
+            pool[perm[k], :, :seg.shape[1], :] = seg
+            table[b, j] = perm[k]
+            k += 1
+    return pool, table
+
+
+def test_paged_attention_equals_contiguous_under_page_permutation():
+    # the paged reading is the contiguous one on the same prefix: a random page placement
+    # (and +-1e4 in every unused pool entry) changes nothing, bit for bit
+    rng = np.random.default_rng(3)
+    bs, Hq, Hkv, D, ps = 3, 8, 2, 16, 4
+    lens = np.array([1, 9, 12])
+    q = rng.standard_normal((bs, Hq, D))
+    kp = [rng.standard_normal((Hkv, n, D)) for n in lens]
+    vp = [rng.standard_normal((Hkv, n, D)) for n in lens]
+    kpool, table = _scatter_to_pages(kp, ps, 16, np.random.default_rng(7))
+    vpool, table_v = _scatter_to_pages(vp, ps, 16, np.random.default_rng(7))
+    assert np.array_equal(table, table_v)
+    got = ops.gqa_decode_attention_paged(q, kpool, vpool, table, lens, ps, 0.25)
+    assert np.array_equal(got, ops.gqa_decode_attention(q, kp, vp, 0.25))
+    # one page per sequence of the whole capacity, identity table: the contiguous cache
+    cap = 16
+    kc = np.stack([np.concatenate([k, np.full((Hkv, cap - k.shape[1], D), 7.0)], axis=1) for k in kp])
+    vc = np.stack([np.concatenate([v, np.full((Hkv, cap - v.shape[1], D), 7.0)], axis=1) for v in vp])
+    ident = np.arange(bs, dtype=np.int32)[:, None]
+    assert np.array_equal(ops.gqa_decode_attention_paged(q, kc, vc, ident, lens, cap, 0.25), got)
+
+
+def test_kv_append_paged_lands_where_the_gather_reads():
+    rng = np.random.default_rng(5)
+    Hkv, D, ps = 2, 8, 4
+    prefix = [rng.standard_normal((Hkv, n, D)) for n in (3, 4, 8)]
+    pool, table = _scatter_to_pages(prefix, ps, 12, np.random.default_rng(2))
+    # give every sequence a page for its next position (the sequence of length 4 and 8 start one)
+    free = [p for p in range(12) if p not in set(table[table >= 0].tolist())]
+    for b, n in enumerate((3, 4, 8)):
+        if table[b, n // ps] < 0:
+            table[b, n // ps] = free.pop()
+    kn = rng.standard_normal((3, Hkv, D))
+    vn = rng.standard_normal((3, Hkv, D))
+    lens = np.array([4, 5, 9])  # after the append
+    k2, v2 = ops.kv_append_paged(pool, pool.copy(), table, kn, vn, lens, ps)
+    gk = ops.paged_prefix(k2, table, lens, ps)
+    gv = ops.paged_prefix(v2, table, lens, ps)
+    for b in range(3):
+        assert np.array_equal(gk[b][:, :-1], prefix[b]) and np.array_equal(gk[b][:, -1], kn[b])
+        assert np.array_equal(gv[b][:, -1], vn[b])
+    assert np.count_nonzero(k2 != pool) == np.count_nonzero(kn)
+
+
 def _tiny_step(zero_paths=False, seed=0):
     bs, d, dff, Hq, Hkv, D = 2, 64, 96, 4, 2, 16
     x = synth.activations(bs, d, seed)
