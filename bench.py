@@ -8,8 +8,9 @@ MXFP8 SwiGLU MLP (Qwen3-4B shape 2560/9728) + residual -> prev_tokens_shift [64,
 
 metric/unit: HBM GB/s = algorithmic bytes of the step / step time (the step's KV reads,
 weights and activations; see the design doc for the per-kernel byte counts). The line also
-carries the MLP-only sweep (M = 1..128: us and GB/s) and the attention-only sweep
-(bs = 1..64: GB/s), each timed the same way.
+carries the MLP-only sweep (M = 1..128: us and GB/s), the attention-only sweep (bs = 1..64:
+GB/s), the paged-attention sweep (bs = 64, pages of 64/128/256), the MXFP8-KV attention sweep
+(bs = 1..64 and paged) and the square MXFP8 GEMM sweep, each timed the same way.
 
 Timing: W untimed warm-up steps, then K steps each bracketed by CUDA events on the
 launching stream, with a 256 MiB L2 flush between steps (outside the events);
@@ -57,6 +58,13 @@ def mlp_bytes(M, d=D_MODEL, dff=D_FF, residual=False):
 def attn_bytes(kv_lens, Hq=HQ, Hkv=HKV, D=HD):
     """K and V rows of every active prefix once, plus q read and o written."""
     kv = int(np.sum(kv_lens)) * Hkv * D * 2 * 2
+    return kv + len(kv_lens) * Hq * D * 2 * 2
+
+
+def attn_kv_mxfp8_bytes(kv_lens, Hq=HQ, Hkv=HKV, D=HD):
+    """MXFP8 K and V rows (E4M3 codes + one UE8M0 byte per 32) of every active prefix once,
+    plus q read and o written (bf16)."""
+    kv = int(np.sum(kv_lens)) * Hkv * (D + D // 32) * 2
     return kv + len(kv_lens) * Hq * D * 2 * 2
 
 
@@ -164,11 +172,11 @@ class ClockSampler:
 
 
 # DRAM traffic of the attention split kernel per algorithmic byte, from one ncu capture of the
-# same kernel on a smaller cache (profiles/gqa_split_kernel_bs64_cap4096.md: 634.67 MB of
+# same kernel on a smaller cache (profiles/gqa_split_kernel_bs64_cap4096.md: 634.95 MB of
 # dram__bytes_read.sum + dram__bytes_write.sum for 622.54 MB of algorithmic bytes). Traffic
 # grows in proportion to the prefix tokens read, so it is scaled to the step's launch. Set to
 # None whenever the kernel changes until it is captured again.
-ATTN_TRAFFIC_PER_ALG_BYTE = 634.671104e6 / 622538752
+ATTN_TRAFFIC_PER_ALG_BYTE = 634.950912e6 / 622538752
 
 
 # --------------------------------------------------------------------------- measured peaks
@@ -438,7 +446,53 @@ def run_sweeps(dev, flush):
         attn[str(bs)] = {"us": round(ms * 1e3, 2), "GB_s": round(attn_bytes(lens) / (ms * 1e-3) / 1e9, 1)}
     del K, V
     return {"mlp_M": mlp, "attn_bs": attn, "attn_paged_bs64": paged_attn_sweep(dev, rn, flush),
-            "gemm_square": gemm_square_sweep(dev)}
+            "attn_kv_mxfp8_bs": kv_mxfp8_attn_sweep(dev, rn, flush), "gemm_square": gemm_square_sweep(dev)}
+
+
+def kv_mxfp8_attn_sweep(dev, rn, flush):
+    """Decode attention over an MXFP8 K/V cache (contiguous, cap = 4096; and paged, 64-token
+    pages) at bs = 1…64 over the bench's ragged lengths; GB/s over the MXFP8 algorithmic bytes."""
+    import torch
+
+    from mxfp8_mlp_gqa_gb300 import api, synth
+
+    cap, bs_max = KV_HI, BS
+    kc = torch.empty((bs_max, HKV, cap, HD), dtype=torch.uint8, device=dev)
+    ks = torch.empty((bs_max, HKV, cap, HD // 32), dtype=torch.uint8, device=dev)
+    vc, vs = torch.empty_like(kc), torch.empty_like(ks)
+    for b in range(bs_max):
+        for c, s in ((kc, ks), (vc, vs)):
+            q8, s8 = api.mxfp8_quantize(rn((HKV * cap, HD)))
+            c[b].copy_(q8.view(HKV, cap, HD))
+            s[b].copy_(s8.view(HKV, cap, HD // 32))
+    res = {}
+    for bs in (1, 8, 16, 32, 64):
+        lens = synth.kv_lens(bs, KV_LO, KV_HI, seed=0)
+        q = rn((bs, HQ, HD))
+        kl = torch.from_numpy(lens).to(dev)
+        out = torch.empty((bs, HQ, HD), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(max(1, api.gqa_decode_attn_workspace(bs, HQ, HKV, HD, KV_HI)), dtype=torch.uint8, device=dev)
+        a = (kc[:bs], ks[:bs], vc[:bs], vs[:bs])
+        ms = _time_op(lambda: api.gqa_decode_attn_kv_mxfp8(q, *a, kl, KV_HI, 1 / math.sqrt(HD), out=out,
+                                                           workspace=ws), flush)
+        res[str(bs)] = {"us": round(ms * 1e3, 2), "GB_s": round(attn_kv_mxfp8_bytes(lens) / (ms * 1e-3) / 1e9, 1)}
+    # paged, bs = 64: the contiguous arrays viewed as 64-token pages, visited in a seeded
+    # random order
+    ps = 64
+    lens = synth.kv_lens(bs_max, KV_LO, KV_HI, seed=0)
+    npg = cap // ps
+    pools = [t.view(bs_max, HKV, npg, ps, -1).permute(0, 2, 1, 3, 4).contiguous().view(bs_max * npg, HKV, ps, -1)
+             for t in (kc, ks, vc, vs)]
+    table = np.random.default_rng(ps).permutation(bs_max * npg).astype(np.int32).reshape(bs_max, npg)
+    tb = torch.from_numpy(table).to(dev)
+    q = rn((bs_max, HQ, HD))
+    kl = torch.from_numpy(lens).to(dev)
+    out = torch.empty((bs_max, HQ, HD), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(1, api.gqa_decode_attn_workspace(bs_max, HQ, HKV, HD, KV_HI)), dtype=torch.uint8, device=dev)
+    ms = _time_op(lambda: api.gqa_decode_attn_kv_mxfp8_paged(q, *pools, tb, kl, KV_HI, 1 / math.sqrt(HD), out=out,
+                                                             workspace=ws), flush)
+    res["paged64_bs64"] = {"us": round(ms * 1e3, 2), "GB_s": round(attn_kv_mxfp8_bytes(lens) / (ms * 1e-3) / 1e9, 1)}
+    return res
 
 
 def paged_attn_sweep(dev, rn, flush, bs=BS, page_sizes=(64, 128, 256)):
@@ -558,6 +612,26 @@ def run_profile(args):
         ws = torch.empty(max(1, api.gqa_decode_attn_workspace(bs, HQ, HKV, HD, KV_HI)), dtype=torch.uint8, device=dev)
         out = torch.empty((bs, HQ, HD), dtype=torch.bfloat16, device=dev)
         fn = lambda: api.gqa_decode_attn(q, K, V, kl, KV_HI, 1 / math.sqrt(HD), out=out, workspace=ws)  # noqa: E731
+    elif kind == "attn_mx":
+        # decode attention over an MXFP8 K/V cache [bs, Hkv, cap, D] (+ scales)
+        bs, _, capa = arg.partition(":")
+        bs, cap = int(bs), int(capa or KV_HI)
+        arrs = []
+        for _ in range(2):
+            c = torch.empty((bs, HKV, cap, HD), dtype=torch.uint8, device=dev)
+            sc = torch.empty((bs, HKV, cap, HD // 32), dtype=torch.uint8, device=dev)
+            for b in range(bs):
+                q8, s8 = api.mxfp8_quantize(rn((HKV * cap, HD)))
+                c[b].copy_(q8.view(HKV, cap, HD))
+                sc[b].copy_(s8.view(HKV, cap, HD // 32))
+            arrs += [c, sc]
+        lens = synth.kv_lens(bs, KV_LO, min(KV_HI, cap), seed=0)
+        kl = torch.from_numpy(lens).to(dev)
+        q = rn((bs, HQ, HD))
+        ws = torch.empty(max(1, api.gqa_decode_attn_workspace(bs, HQ, HKV, HD, KV_HI)), dtype=torch.uint8, device=dev)
+        out = torch.empty((bs, HQ, HD), dtype=torch.bfloat16, device=dev)
+        fn = lambda: api.gqa_decode_attn_kv_mxfp8(q, *arrs, kl, KV_HI, 1 / math.sqrt(HD), out=out,  # noqa: E731
+                                                  workspace=ws)
     elif kind == "gemm":
         M, N, K_ = (int(v) for v in arg.split("x"))
         aq, as_ = api.mxfp8_quantize(rn((M, K_)))
@@ -583,6 +657,9 @@ def run_profile(args):
     out = {"profile": args.profile, "median_us": round(ms * 1e3, 2)}
     if kind == "attn":
         out["attn_bytes"] = attn_bytes(lens)
+        out["sum_kv_len"] = int(lens.sum())
+    if kind == "attn_mx":
+        out["attn_bytes"] = attn_kv_mxfp8_bytes(lens)
         out["sum_kv_len"] = int(lens.sum())
     return out
 

@@ -238,6 +238,57 @@ mxg_status kv_append_paged(void* k_pool, void* v_pool, const int32_t* block_tabl
                            void* stream);
 
 /*
+ * gqa_decode_attn_kv_mxfp8 -- gqa_decode_attn over an MXFP8 K/V cache ([S2.1] "What's Open
+ * Source": MXFP8 FlashAttention, paged decode with native GQA; the MX format of [S2.1] "FP8
+ * Quantization Strategy": 1x32 blocks, E4M3 elements, OCP UE8M0 shared exponents).
+ *   k_codes, v_codes  E4M3 [bs, Hkv, cap, D] (one byte per element, D contiguous);
+ *   k_scales, v_scales UE8M0 [bs, Hkv, cap, D/32]: element d of row t has the value
+ *            E4M3(codes[.., t, d]) * 2^(scales[.., t, d/32] - 127), as written by
+ *            kv_append_mxfp8 (or mxfp8_quantize of rows of D).
+ *   cap a multiple of 16; other arguments, workspace size, errors and the result as
+ *   gqa_decode_attn: o = softmax(scale q K^T) V over the dequantised prefix, bf16 out.
+ *   Values are finite with block exponents up to 2^71 (scale bytes <= 198); scale bytes of 0
+ *   (blocks whose values lie below 2^-118) contribute zero.
+ */
+mxg_status gqa_decode_attn_kv_mxfp8(const void* q, int64_t ld_q, const uint8_t* k_codes, const uint8_t* k_scales,
+                                   const uint8_t* v_codes, const uint8_t* v_scales, const int32_t* kv_len, int64_t bs,
+                                   int64_t Hq, int64_t Hkv, int64_t D, int64_t cap, int64_t max_kv_len, float scale,
+                                   void* out, int32_t* err_flag, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * gqa_decode_attn_kv_mxfp8_paged -- gqa_decode_attn_kv_mxfp8 over paged MXFP8 pools:
+ * k_codes, v_codes E4M3 [num_pages, Hkv, page_size, D], k_scales, v_scales UE8M0
+ * [num_pages, Hkv, page_size, D/32]; block_table, page_size, max_kv_len and err_flag as
+ * gqa_decode_attn_paged.
+ */
+mxg_status gqa_decode_attn_kv_mxfp8_paged(const void* q, int64_t ld_q, const uint8_t* k_codes,
+                                         const uint8_t* k_scales, const uint8_t* v_codes, const uint8_t* v_scales,
+                                         const int32_t* block_table, int64_t max_pages, int64_t page_size,
+                                         int64_t num_pages, const int32_t* kv_len, int64_t bs, int64_t Hq,
+                                         int64_t Hkv, int64_t D, int64_t max_kv_len, float scale, void* out,
+                                         int32_t* err_flag, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * kv_append_mxfp8 -- kv_append into an MXFP8 cache: the bf16 rows k_new, v_new [bs, Hkv, D]
+ * (row stride ld_new elements between sequences) are MX-quantised along D with the rule of
+ * mxfp8_quantize (bit-identical to it) and written at position kv_len[b]-1 of the code and
+ * scale arrays laid out as in gqa_decode_attn_kv_mxfp8. D a multiple of 32. err_flag:
+ * MXG_EDEVICE for kv_len outside [1, cap] (that row is skipped).
+ */
+mxg_status kv_append_mxfp8(uint8_t* k_codes, uint8_t* k_scales, uint8_t* v_codes, uint8_t* v_scales,
+                           const void* k_new, const void* v_new, int64_t ld_new, const int32_t* kv_len, int64_t bs,
+                           int64_t Hkv, int64_t D, int64_t cap, int32_t* err_flag, void* stream);
+
+/*
+ * kv_append_mxfp8_paged -- kv_append_mxfp8 into paged MXFP8 pools (layout of
+ * gqa_decode_attn_kv_mxfp8_paged, row lookup and errors of kv_append_paged).
+ */
+mxg_status kv_append_mxfp8_paged(uint8_t* k_codes, uint8_t* k_scales, uint8_t* v_codes, uint8_t* v_scales,
+                                 const int32_t* block_table, int64_t max_pages, int64_t page_size, int64_t num_pages,
+                                 const void* k_new, const void* v_new, int64_t ld_new, const int32_t* kv_len,
+                                 int64_t bs, int64_t Hkv, int64_t D, int32_t* err_flag, void* stream);
+
+/*
  * prev_tokens_shift -- in-place slide of the Dual-AR previous-tokens window ([S2.1]
  * "DualAR: S2-Specific Batching Constraints": prev int32 [bs, W, cw], next_tokens int32
  * [bs, cw], strict shape/dtype contract). prev[b, w] <- prev[b, w+1] for w < W-1 and

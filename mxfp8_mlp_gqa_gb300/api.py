@@ -52,6 +52,15 @@ _SIGS = {
                                              c_i64, c_i64, c_i64, c_f32, c_vp, c_vp, c_vp, c_sz, c_vp]),
     "kv_append_paged": (ctypes.c_int, [c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_i64, c_vp, c_i64, c_i64,
                                        c_i64, c_vp, c_vp]),
+    "gqa_decode_attn_kv_mxfp8": (ctypes.c_int, [c_vp, c_i64, c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_i64,
+                                                c_i64, c_i64, c_f32, c_vp, c_vp, c_vp, c_sz, c_vp]),
+    "gqa_decode_attn_kv_mxfp8_paged": (ctypes.c_int, [c_vp, c_i64, c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64,
+                                                      c_vp, c_i64, c_i64, c_i64, c_i64, c_i64, c_f32, c_vp, c_vp, c_vp,
+                                                      c_sz, c_vp]),
+    "kv_append_mxfp8": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_vp, c_i64, c_i64, c_i64, c_i64,
+                                       c_vp, c_vp]),
+    "kv_append_mxfp8_paged": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_i64,
+                                             c_vp, c_i64, c_i64, c_i64, c_vp, c_vp]),
 }
 
 
@@ -325,6 +334,98 @@ def kv_append_paged(k_pool, v_pool, block_table, k_new, v_new, kv_len, err=None)
         _check(err, "err", torch.int32, (1,))
     _call("kv_append_paged", _ptr(k_pool), _ptr(v_pool), _ptr(block_table), max_pages, page_size, num_pages,
           _ptr(k_new), _ptr(v_new), Hkv * D, _ptr(kv_len), bs, Hkv, D, _ptr(err), _stream())
+
+
+def _mx_cache(codes, scales, cname, sname):
+    """MXFP8 cache arrays: codes uint8 [A, Hkv, T, D], scales uint8 [A, Hkv, T, D/32]."""
+    _check(codes, cname, torch.uint8, ndim=4)
+    A, Hkv, T, D = codes.shape
+    if D % 32:
+        raise ValueError(f"{cname}: D must be a multiple of 32")
+    _check(scales, sname, torch.uint8, (A, Hkv, T, D // 32))
+    return A, Hkv, T, D
+
+
+def gqa_decode_attn_kv_mxfp8(q, k_codes, k_scales, v_codes, v_scales, kv_len, max_kv_len, scale, out=None, err=None,
+                             workspace=None):
+    """Decode attention over an MXFP8 cache: q bf16 [bs, Hq, D]; codes uint8 [bs, Hkv, cap, D],
+    scales uint8 [bs, Hkv, cap, D/32]; kv_len int32 [bs] -> out bf16 [bs, Hq, D]."""
+    bs, Hkv, cap, D = _mx_cache(k_codes, k_scales, "k_codes", "k_scales")
+    _mx_cache(v_codes, v_scales, "v_codes", "v_scales")
+    _check(v_codes, "v_codes", torch.uint8, (bs, Hkv, cap, D))
+    _check(kv_len, "kv_len", torch.int32, (bs,))
+    _check(q, "q", torch.bfloat16, ndim=3)
+    Hq = q.shape[1]
+    _check(q, "q", torch.bfloat16, (bs, Hq, D))
+    out = _out(out, "out", torch.bfloat16, (bs, Hq, D), k_codes.device)
+    if err is not None:
+        _check(err, "err", torch.int32, (1,))
+    need = gqa_decode_attn_workspace(bs, Hq, Hkv, D, max_kv_len)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=k_codes.device)
+    ws_bytes = 0 if workspace is None else workspace.numel()
+    _call("gqa_decode_attn_kv_mxfp8", _ptr(q), Hq * D, _ptr(k_codes), _ptr(k_scales), _ptr(v_codes), _ptr(v_scales),
+          _ptr(kv_len), bs, Hq, Hkv, D, cap, int(max_kv_len), float(scale), _ptr(out), _ptr(err), _ptr(workspace),
+          ws_bytes, _stream())
+    return out
+
+
+def gqa_decode_attn_kv_mxfp8_paged(q, k_codes, k_scales, v_codes, v_scales, block_table, kv_len, max_kv_len, scale,
+                                   out=None, err=None, workspace=None):
+    """Paged decode attention over MXFP8 pools: codes uint8 [num_pages, Hkv, page_size, D],
+    scales uint8 [num_pages, Hkv, page_size, D/32]; block_table int32 [bs, max_pages]."""
+    num_pages, Hkv, page_size, D = _mx_cache(k_codes, k_scales, "k_codes", "k_scales")
+    _mx_cache(v_codes, v_scales, "v_codes", "v_scales")
+    _check(v_codes, "v_codes", torch.uint8, (num_pages, Hkv, page_size, D))
+    _check(block_table, "block_table", torch.int32, ndim=2)
+    bs, max_pages = block_table.shape
+    _check(kv_len, "kv_len", torch.int32, (bs,))
+    _check(q, "q", torch.bfloat16, ndim=3)
+    Hq = q.shape[1]
+    _check(q, "q", torch.bfloat16, (bs, Hq, D))
+    out = _out(out, "out", torch.bfloat16, (bs, Hq, D), k_codes.device)
+    if err is not None:
+        _check(err, "err", torch.int32, (1,))
+    need = gqa_decode_attn_workspace(bs, Hq, Hkv, D, max_kv_len)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=k_codes.device)
+    ws_bytes = 0 if workspace is None else workspace.numel()
+    _call("gqa_decode_attn_kv_mxfp8_paged", _ptr(q), Hq * D, _ptr(k_codes), _ptr(k_scales), _ptr(v_codes),
+          _ptr(v_scales), _ptr(block_table), max_pages, page_size, num_pages, _ptr(kv_len), bs, Hq, Hkv, D,
+          int(max_kv_len), float(scale), _ptr(out), _ptr(err), _ptr(workspace), ws_bytes, _stream())
+    return out
+
+
+def kv_append_mxfp8(k_codes, k_scales, v_codes, v_scales, k_new, v_new, kv_len, err=None):
+    """kv_append into an MXFP8 cache (codes [bs, Hkv, cap, D], scales [bs, Hkv, cap, D/32]);
+    k_new/v_new bf16 [bs, Hkv, D] are MX-quantised on the way in."""
+    bs, Hkv, cap, D = _mx_cache(k_codes, k_scales, "k_codes", "k_scales")
+    _mx_cache(v_codes, v_scales, "v_codes", "v_scales")
+    _check(v_codes, "v_codes", torch.uint8, (bs, Hkv, cap, D))
+    _check(kv_len, "kv_len", torch.int32, (bs,))
+    _check(k_new, "k_new", torch.bfloat16, (bs, Hkv, D))
+    _check(v_new, "v_new", torch.bfloat16, (bs, Hkv, D))
+    if err is not None:
+        _check(err, "err", torch.int32, (1,))
+    _call("kv_append_mxfp8", _ptr(k_codes), _ptr(k_scales), _ptr(v_codes), _ptr(v_scales), _ptr(k_new), _ptr(v_new),
+          Hkv * D, _ptr(kv_len), bs, Hkv, D, cap, _ptr(err), _stream())
+
+
+def kv_append_mxfp8_paged(k_codes, k_scales, v_codes, v_scales, block_table, k_new, v_new, kv_len, err=None):
+    """kv_append_mxfp8 into paged MXFP8 pools [num_pages, Hkv, page_size, D (/32)]."""
+    num_pages, Hkv, page_size, D = _mx_cache(k_codes, k_scales, "k_codes", "k_scales")
+    _mx_cache(v_codes, v_scales, "v_codes", "v_scales")
+    _check(v_codes, "v_codes", torch.uint8, (num_pages, Hkv, page_size, D))
+    _check(block_table, "block_table", torch.int32, ndim=2)
+    bs, max_pages = block_table.shape
+    _check(kv_len, "kv_len", torch.int32, (bs,))
+    _check(k_new, "k_new", torch.bfloat16, (bs, Hkv, D))
+    _check(v_new, "v_new", torch.bfloat16, (bs, Hkv, D))
+    if err is not None:
+        _check(err, "err", torch.int32, (1,))
+    _call("kv_append_mxfp8_paged", _ptr(k_codes), _ptr(k_scales), _ptr(v_codes), _ptr(v_scales), _ptr(block_table),
+          max_pages, page_size, num_pages, _ptr(k_new), _ptr(v_new), Hkv * D, _ptr(kv_len), bs, Hkv, D, _ptr(err),
+          _stream())
 
 
 def gqa_decode_attn_noalloc(q, k_cache, v_cache, kv_len, max_kv_len, scale, out):

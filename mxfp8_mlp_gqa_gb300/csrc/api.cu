@@ -198,6 +198,59 @@ mxg_status attn_call(const void* q, int64_t ld_q, const void* k_cache, const voi
                                          (cudaStream_t)stream, oq, os, pages));
 }
 
+// Decode attention over an MXFP8 K/V cache (codes [rows, D] E4M3, scales [rows, D/32] UE8M0).
+mxg_status attn_kv_mx_call(const void* q, int64_t ld_q, const uint8_t* kc, const uint8_t* ks, const uint8_t* vc,
+                           const uint8_t* vs, const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D,
+                           int64_t cap, int64_t max_kv_len, float scale, void* out, int32_t* err_flag,
+                           void* workspace, size_t ws_bytes, void* stream, const KvPages* pages = nullptr) {
+  if (!q || !kc || !ks || !vc || !vs || !kv_len || !out) return MXG_EINVAL;
+  if (!(scale > 0.f) || !(scale < 1e30f)) return MXG_EINVAL;
+  if (bs < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || Hq / Hkv > 8 || (D != 64 && D != 128) || cap <= 0 ||
+      max_kv_len <= 0 || ld_q < Hq * D)
+    return MXG_ESHAPE;
+  // scales are copied as 16-byte lines: a (b, g) row block must start on one (cap % 16 == 0)
+  if (!pages && cap % 16) return MXG_ESHAPE;
+  const int64_t rows_total = pages ? pages->num_pages * Hkv * pages->page_size : bs * Hkv * cap;
+  if (rows_total >= ((int64_t)1 << 31) || bs * Hkv > 65535 || max_kv_len > ((int64_t)1 << 30)) return MXG_ESHAPE;
+  if (!aligned16(q) || !aligned16(kc) || !aligned16(ks) || !aligned16(vc) || !aligned16(vs) || !aligned16(out) ||
+      ld_q % 8)
+    return MXG_EALIGN;
+  if (bs == 0) return MXG_OK;
+  const size_t need = attn_workspace_bytes(bs, Hq, Hkv, D, max_kv_len);
+  if (need && (!workspace || ws_bytes < need)) return MXG_EWORKSPACE;
+  if (need && !aligned16(workspace)) return MXG_EALIGN;
+  const uint64_t rows = (uint64_t)rows_total;
+  const uint64_t lines = rows * (uint64_t)(D / 32) / 16;
+  const CUtensorMapSwizzle swz = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const uint32_t sbox = (uint32_t)(64 * (D / 32) / 16);
+  CUtensorMap tk, tv, tks, tvs;
+  if (!make_tensor_map_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, kc, (uint64_t)D, rows, (uint64_t)D, (uint32_t)D, 64,
+                          swz) ||
+      !make_tensor_map_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, vc, (uint64_t)D, rows, (uint64_t)D, (uint32_t)D, 64,
+                          swz) ||
+      !make_tensor_map_2d(&tks, CU_TENSOR_MAP_DATA_TYPE_UINT8, ks, 16, lines, 16, 16, sbox,
+                          CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_tensor_map_2d(&tvs, CU_TENSOR_MAP_DATA_TYPE_UINT8, vs, 16, lines, 16, 16, sbox,
+                          CU_TENSOR_MAP_SWIZZLE_NONE))
+    return MXG_ENOTSUP;
+  return launched(launch_gqa_decode_attn_kv_mx(tk, tv, tks, tvs, static_cast<const uint16_t*>(q), ld_q, kv_len, bs,
+                                               Hq, Hkv, D, cap, max_kv_len, scale, static_cast<uint16_t*>(out),
+                                               err_flag, workspace, (cudaStream_t)stream, pages));
+}
+
+mxg_status kv_append_mx_call(uint8_t* kc, uint8_t* ks, uint8_t* vc, uint8_t* vs, const void* k_new,
+                             const void* v_new, int64_t ld_new, const int32_t* kv_len, int64_t bs, int64_t Hkv,
+                             int64_t D, int64_t cap, int32_t* err_flag, void* stream, const KvPages* pages) {
+  if (!kc || !ks || !vc || !vs || !k_new || !v_new || !kv_len) return MXG_EINVAL;
+  if (bs < 0 || Hkv <= 0 || D <= 0 || D % 32 || D > 1024 || cap <= 0 || ld_new < Hkv * D || bs * Hkv > (1 << 26))
+    return MXG_ESHAPE;
+  if (!aligned16(k_new) || !aligned16(v_new) || ld_new % 8) return MXG_EALIGN;
+  if (bs == 0) return MXG_OK;
+  return launched(launch_kv_append_mx(kc, ks, vc, vs, static_cast<const uint16_t*>(k_new),
+                                      static_cast<const uint16_t*>(v_new), ld_new, kv_len, bs, Hkv, D, cap, err_flag,
+                                      (cudaStream_t)stream, pages));
+}
+
 // The page-table arguments shared by the paged entry points; 0 if valid.
 mxg_status check_pages(const int32_t* table, int64_t max_pages, int64_t page_size, int64_t num_pages) {
   if (!table) return MXG_EINVAL;
@@ -302,6 +355,54 @@ mxg_status kv_append_paged(void* k_pool, void* v_pool, const int32_t* block_tabl
   return launched(launch_kv_append(static_cast<uint16_t*>(k_pool), static_cast<uint16_t*>(v_pool),
                                    static_cast<const uint16_t*>(k_new), static_cast<const uint16_t*>(v_new), ld_new,
                                    kv_len, bs, Hkv, D, max_pages * page_size, err_flag, (cudaStream_t)stream, &pg));
+}
+
+mxg_status gqa_decode_attn_kv_mxfp8(const void* q, int64_t ld_q, const uint8_t* k_codes, const uint8_t* k_scales,
+                                   const uint8_t* v_codes, const uint8_t* v_scales, const int32_t* kv_len, int64_t bs,
+                                   int64_t Hq, int64_t Hkv, int64_t D, int64_t cap, int64_t max_kv_len, float scale,
+                                   void* out, int32_t* err_flag, void* workspace, size_t ws_bytes, void* stream) {
+  return attn_kv_mx_call(q, ld_q, k_codes, k_scales, v_codes, v_scales, kv_len, bs, Hq, Hkv, D, cap, max_kv_len,
+                         scale, out, err_flag, workspace, ws_bytes, stream);
+}
+
+mxg_status gqa_decode_attn_kv_mxfp8_paged(const void* q, int64_t ld_q, const uint8_t* k_codes,
+                                         const uint8_t* k_scales, const uint8_t* v_codes, const uint8_t* v_scales,
+                                         const int32_t* block_table, int64_t max_pages, int64_t page_size,
+                                         int64_t num_pages, const int32_t* kv_len, int64_t bs, int64_t Hq,
+                                         int64_t Hkv, int64_t D, int64_t max_kv_len, float scale, void* out,
+                                         int32_t* err_flag, void* workspace, size_t ws_bytes, void* stream) {
+  const mxg_status c = check_pages(block_table, max_pages, page_size, num_pages);
+  if (c != MXG_OK) return c;
+  if (max_kv_len > max_pages * page_size) return MXG_ESHAPE;
+  KvPages pg;
+  pg.table = block_table;
+  pg.max_pages = (int)max_pages;
+  pg.page_size = (int)page_size;
+  pg.num_pages = num_pages;
+  return attn_kv_mx_call(q, ld_q, k_codes, k_scales, v_codes, v_scales, kv_len, bs, Hq, Hkv, D, max_pages * page_size,
+                         max_kv_len, scale, out, err_flag, workspace, ws_bytes, stream, &pg);
+}
+
+mxg_status kv_append_mxfp8(uint8_t* k_codes, uint8_t* k_scales, uint8_t* v_codes, uint8_t* v_scales,
+                           const void* k_new, const void* v_new, int64_t ld_new, const int32_t* kv_len, int64_t bs,
+                           int64_t Hkv, int64_t D, int64_t cap, int32_t* err_flag, void* stream) {
+  return kv_append_mx_call(k_codes, k_scales, v_codes, v_scales, k_new, v_new, ld_new, kv_len, bs, Hkv, D, cap,
+                           err_flag, stream, nullptr);
+}
+
+mxg_status kv_append_mxfp8_paged(uint8_t* k_codes, uint8_t* k_scales, uint8_t* v_codes, uint8_t* v_scales,
+                                 const int32_t* block_table, int64_t max_pages, int64_t page_size, int64_t num_pages,
+                                 const void* k_new, const void* v_new, int64_t ld_new, const int32_t* kv_len,
+                                 int64_t bs, int64_t Hkv, int64_t D, int32_t* err_flag, void* stream) {
+  const mxg_status c = check_pages(block_table, max_pages, page_size, num_pages);
+  if (c != MXG_OK) return c;
+  KvPages pg;
+  pg.table = block_table;
+  pg.max_pages = (int)max_pages;
+  pg.page_size = (int)page_size;
+  pg.num_pages = num_pages;
+  return kv_append_mx_call(k_codes, k_scales, v_codes, v_scales, k_new, v_new, ld_new, kv_len, bs, Hkv, D,
+                           max_pages * page_size, err_flag, stream, &pg);
 }
 
 mxg_status prev_tokens_shift(int32_t* prev, const int32_t* next_tokens, int64_t bs, int64_t W, int64_t cw,

@@ -27,17 +27,24 @@ namespace mxg {
 
 namespace {
 
-constexpr int kTileTok = 64;     // tokens per pipeline stage
+constexpr int kTileTok = 64;        // tokens per pipeline stage
 constexpr int kMaxSplitTiles = 16;  // a split covers at most 1024 tokens (attn_chunk)
-constexpr int kConsumers = 4;    // consumer warps (16 tokens each per tile)
+constexpr int kConsumers = 4;       // consumer warps (16 tokens each per tile)
 constexpr int kThreads = (kConsumers + 1) * 32;
 
-template <int D>
+// Shared-memory plan of the split kernel. kMx: K and V are MXFP8 (E4M3 codes [64, D] per tile,
+// plus their UE8M0 scales [64, D/32]); otherwise bf16 [64, D] per tile.
+template <int D, bool kMx>
 struct AttnShape {
-  static constexpr int kHalves = D / 64;                // 128-byte TMA boxes per row
-  static constexpr int kTileBytes = kTileTok * D * 2;   // one K (or V) tile
-  static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kStages = D == 128 ? 3 : 4;
+  static constexpr int kHalves = D / 64;                               // 128-byte TMA boxes per bf16 row
+  static constexpr int kTileBytes = kTileTok * D * (kMx ? 1 : 2);      // one K (or V) tile
+  static constexpr int kScaleTileBytes = kMx ? kTileTok * D / 32 : 0;  // its scale bytes
+  static constexpr int kCodeStageBytes = 2 * kTileBytes;
+  static constexpr int kStageBytes = kCodeStageBytes + 2 * kScaleTileBytes;  // bytes landing per stage
+  // MXFP8: 3 stages of 16.5 KB keep 4 CTAs (16 consumer warps) on an SM; the consumer's
+  // conversion work, not the bytes in flight, limits that variant
+  static constexpr int kStages = kMx ? (D == 128 ? 3 : 6) : (D == 128 ? 3 : 4);
+  static constexpr int kScaleRingOff = kStages * kCodeStageBytes;  // scales after all code stages
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kMergeBytes = kConsumers * 8 * D * 4 + kConsumers * 8 * 2 * 4;
   static constexpr int kBodyBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
@@ -51,6 +58,74 @@ __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int row, int col) {
   const int half = col >> 6;
   const int chunk = (col & 63) >> 3;
   return base + half * (kTileTok * 128) + row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+// Byte address of code byte `col` of row `row` in a [64, D] E4M3 tile loaded by TMA with a
+// D-byte swizzle: 128-byte rows, 16-byte chunk ^= row % 8 (D = 128); 64-byte rows, chunk ^=
+// (row / 2) % 4 (D = 64).
+template <int D>
+__device__ __forceinline__ uint32_t code_addr(uint32_t base, int row, int col) {
+  if constexpr (D == 128)
+    return base + row * 128 + (((col >> 4) ^ (row & 7)) << 4) + (col & 15);
+  else
+    return base + row * 64 + (((col >> 4) ^ ((row >> 1) & 3)) << 4) + (col & 15);
+}
+
+// Shared-memory loads that the compiler may schedule freely between memory barriers (not
+// volatile; the "memory" clobber keeps them after the mbarrier wait that publishes the stage).
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint2 lds_u32x2(uint32_t addr) {
+  uint2 v;
+  asm("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+  uint16_t v;
+  asm("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// Four E4M3 codes (the bytes of w) -> two f16 pairs, exactly: lo = codes 0, 1; hi = codes 2, 3.
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// Byte X of a and byte X of b, each an E4M3 code, as a bf16 pair (value * 2^-120 each). The
+// code's sign goes to bf16's sign bit and its 4 exponent + 3 mantissa bits to bf16 bits 10..4;
+// read with bf16's exponent bias (127 instead of 7) every code -- zero and subnormals included
+// -- is its E4M3 value times 2^-120 exactly, and none is Inf or NaN. (prmt with the selector's
+// high bit set replicates the selected byte's sign into the byte above it.)
+template <int X>
+__device__ __forceinline__ uint32_t e4m3_pair_bf16(uint32_t a, uint32_t b) {
+  constexpr uint32_t sel = ((8u | (4u + X)) << 12) | ((4u + X) << 8) | ((8u | X) << 4) | X;
+  uint32_t t;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(t) : "r"(a), "r"(b), "n"(sel));
+  return (t << 4) & 0x87F087F0u;
+}
+
+// UE8M0 byte e -> 2^(e - 127) in fp32. e = 0 (2^-127, blocks whose values are all below
+// 2^-118) is read as 0.
+__device__ __forceinline__ float ue8m0_f32(uint32_t e) { return __uint_as_float(e << 23); }
+
+// Scale bytes e0 (bits 0..7) and e1 (bits 16..23) of v -> the bf16 pair (2^(e0-71), 2^(e1-71)),
+// i.e. 2^(s + 56) for s = e - 127: bf16 exponent field e + 56 (exact for e <= 198).
+__device__ __forceinline__ uint32_t pscale_pair(uint32_t v) { return (v & 0x00FF00FFu) * 128u + 0x1C001C00u; }
+
+__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
 }
 
 struct SplitParams {
@@ -75,19 +150,28 @@ struct SplitParams {
   int64_t num_pages;
 };
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
 }  // namespace
 
-template <int D>
+// One CTA = one (split, b, g). tmK/tmV map the K/V rows (bf16 [rows, D], or E4M3 codes
+// [rows, D] when kMx); tmKS/tmVS map the UE8M0 scales of an MXFP8 cache as 16-byte lines
+// ([rows * D/32 / 16, 16]) and are unused for bf16.
+//
+// MXFP8 K/V: a cached value is c * 2^s (c an E4M3 value, s the shared exponent of its 32-wide
+// block along D). S = K q^T is taken per block: the codes enter an f16 MMA exactly (hardware
+// E4M3 -> f16 conversion) against q prescaled by a power of two into f16's range, and each
+// block's partial dot product is multiplied by 2^s in fp32. In O^T += V^T P^T the exponent
+// varies along the contraction (tokens), so it moves to P: a code enters as the bf16 c * 2^-120
+// (bit placement, exact) and P as P * 2^(s + 56) (exact bf16 multiply); O then carries 2^-64,
+// removed in the merge.
+template <int D, bool kMx>
 __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_constant__ CUtensorMap tmK,
                                                              const __grid_constant__ CUtensorMap tmV,
+                                                             const __grid_constant__ CUtensorMap tmKS,
+                                                             const __grid_constant__ CUtensorMap tmVS,
                                                              const SplitParams p) {
-  using S = AttnShape<D>;
+  using S = AttnShape<D, kMx>;
   constexpr int KS = D / 16;  // k-steps of the QK^T product / m-tiles of O^T
+  constexpr int NB = D / 32;  // MX blocks per row
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
@@ -155,18 +239,32 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
     if (lane == 0) {
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
+      if constexpr (kMx) {
+        prefetch_tensormap(&tmKS);
+        prefetch_tensormap(&tmVS);
+      }
       const uint64_t pol = l2_policy_evict_first();
       for (int i = 0; i < ntiles; ++i) {
         const int s = i % S::kStages;
         if (i >= S::kStages && !mbar_wait(&empty[s], ((i / S::kStages) - 1) & 1, p.err)) break;
         const int row = p.table ? tile_row[i] : row0 + i * kTileTok;
         mbar_arrive_expect_tx(&full[s], S::kStageBytes);
-        uint8_t* kt = ring + s * S::kStageBytes;
+        uint8_t* kt = ring + s * S::kCodeStageBytes;
         uint8_t* vt = kt + S::kTileBytes;
+        if constexpr (kMx) {
+          uint8_t* kst = ring + S::kScaleRingOff + s * 2 * S::kScaleTileBytes;
+          tma_load_2d_hint(kt, &tmK, &full[s], 0, row, pol);
+          tma_load_2d_hint(vt, &tmV, &full[s], 0, row, pol);
+          // row is a multiple of 64, so its scales start on a 16-byte line
+          const int line = row / (16 / NB);
+          tma_load_2d_hint(kst, &tmKS, &full[s], 0, line, pol);
+          tma_load_2d_hint(kst + S::kScaleTileBytes, &tmVS, &full[s], 0, line, pol);
+        } else {
 #pragma unroll
-        for (int h = 0; h < S::kHalves; ++h) {
-          tma_load_2d_hint(kt + h * kTileTok * 128, &tmK, &full[s], h * 64, row, pol);
-          tma_load_2d_hint(vt + h * kTileTok * 128, &tmV, &full[s], h * 64, row, pol);
+          for (int h = 0; h < S::kHalves; ++h) {
+            tma_load_2d_hint(kt + h * kTileTok * 128, &tmK, &full[s], h * 64, row, pol);
+            tma_load_2d_hint(vt + h * kTileTok * 128, &tmV, &full[s], h * 64, row, pol);
+          }
         }
       }
     }
@@ -176,15 +274,49 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
   // --------------------------------------------------------------- consumers
   const int c4 = lane & 3, r4 = lane >> 2;
   const int h0 = g * p.group;
-  // B fragments of Q^T (k = dim, n = head): lane holds head r4, dims 2*c4 (+1) and +8 (+9)
+  // B fragments of Q^T (k = dim, n = head); lane holds head r4.
+  //  bf16 cache: k-step ks, dims ks*16 + 2*c4 (+1) and +8 (+9).
+  //  MXFP8 cache: k-steps 2j, 2j+1 cover MX block j; the thread's k slots of step 2j+e hold
+  //  dims 32j + 8*c4 + 4e + {0, 1} and + {2, 3} (the K fragments below use the same order, so
+  //  the dot product is unchanged), as f16 after scaling q by 2^qa.
   uint32_t qb[KS][2];
+  float sl2 = p.scale_log2;
   {
     const bool hv = r4 < p.group;
     const uint16_t* qh = p.q + (int64_t)b * p.ld_q + (int64_t)(h0 + (hv ? r4 : 0)) * D;
+    if constexpr (!kMx) {
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      qb[ks][0] = hv ? *reinterpret_cast<const uint32_t*>(qh + ks * 16 + 2 * c4) : 0u;
-      qb[ks][1] = hv ? *reinterpret_cast<const uint32_t*>(qh + ks * 16 + 8 + 2 * c4) : 0u;
+      for (int ks = 0; ks < KS; ++ks) {
+        qb[ks][0] = hv ? *reinterpret_cast<const uint32_t*>(qh + ks * 16 + 2 * c4) : 0u;
+        qb[ks][1] = hv ? *reinterpret_cast<const uint32_t*>(qh + ks * 16 + 8 + 2 * c4) : 0u;
+      }
+    } else {
+      uint4 qw[NB];
+      float am = 0.f;
+#pragma unroll
+      for (int j = 0; j < NB; ++j) {
+        qw[j] = hv ? *reinterpret_cast<const uint4*>(qh + 32 * j + 8 * c4) : make_uint4(0, 0, 0, 0);
+        const uint32_t w[4] = {qw[j].x, qw[j].y, qw[j].z, qw[j].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) am = fmaxf(am, fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
+      }
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) am = fmaxf(am, __shfl_xor_sync(MXG_FULL_MASK, am, off));
+      // 2^qa brings the group's largest |q| into [2^14, 2^15): every bf16 q is then an f16 exactly
+      // unless it sits 2^38 below that maximum
+      int qa = 0;
+      if (am > 0.f) qa = min(100, max(-100, 14 - ((int)((__float_as_uint(am) >> 23) & 0xFF) - 127)));
+      const float f = __uint_as_float((uint32_t)(qa + 127) << 23);
+#pragma unroll
+      for (int j = 0; j < NB; ++j) {
+        const uint32_t w[4] = {qw[j].x, qw[j].y, qw[j].z, qw[j].w};
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          qb[2 * j + e][0] = pack_f16x2(bf16_lo(w[2 * e]) * f, bf16_hi(w[2 * e]) * f);
+          qb[2 * j + e][1] = pack_f16x2(bf16_lo(w[2 * e + 1]) * f, bf16_hi(w[2 * e + 1]) * f);
+        }
+      }
+      sl2 = p.scale_log2 * __uint_as_float((uint32_t)(127 - qa) << 23);
     }
   }
   float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
@@ -199,24 +331,60 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
   for (int i = 0; i < ntiles; ++i) {
     const int s = i % S::kStages;
     if (!mbar_wait(&full[s], (i / S::kStages) & 1, p.err)) { ok = false; break; }
-    const uint32_t kbase = smem_u32(ring + s * S::kStageBytes);
+    const uint32_t kbase = smem_u32(ring + s * S::kCodeStageBytes);
     const uint32_t vbase = kbase + S::kTileBytes;
+    const uint32_t ksbase = smem_u32(ring + S::kScaleRingOff + s * 2 * S::kScaleTileBytes);
+    const uint32_t vsbase = ksbase + S::kScaleTileBytes;
     const int tb = t0 + i * kTileTok + r0;  // first token of this warp's 16 rows
 
     // S^T[16 tok x 8 heads] = K[16 x D] Q^T[D x 8]
     float sc[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (!kMx) {
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      uint32_t a0, a1, a2, a3;
-      ldmatrix_x4(tile_addr(kbase, r0 + (lane & 7) + 8 * ((lane >> 3) & 1), ks * 16 + 8 * (lane >> 4)), a0, a1, a2,
-                  a3);
-      mma_bf16_16816(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4(tile_addr(kbase, r0 + (lane & 7) + 8 * ((lane >> 3) & 1), ks * 16 + 8 * (lane >> 4)), a0, a1,
+                    a2, a3);
+        mma_bf16_16816(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+      }
+    } else {
+      float acc[NB][4];
+#pragma unroll
+      for (int j = 0; j < NB; ++j) {
+        acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+        const uint2 ka = lds_u32x2(code_addr<D>(kbase, r0 + r4, 32 * j + 8 * c4));
+        const uint2 kb = lds_u32x2(code_addr<D>(kbase, r0 + r4 + 8, 32 * j + 8 * c4));
+        uint32_t a0, a1, a2, a3;
+        e4m3x4_to_f16(ka.x, a0, a2);
+        e4m3x4_to_f16(kb.x, a1, a3);
+        mma_f16_16816(acc[j], a0, a1, a2, a3, qb[2 * j][0], qb[2 * j][1]);
+        e4m3x4_to_f16(ka.y, a0, a2);
+        e4m3x4_to_f16(kb.y, a1, a3);
+        mma_f16_16816(acc[j], a0, a1, a2, a3, qb[2 * j + 1][0], qb[2 * j + 1][1]);
+      }
+      // per-block exponents of tokens r4 and r4+8
+      uint32_t ska, skb;
+      if constexpr (D == 128) {
+        ska = lds_u32(ksbase + (r0 + r4) * NB);
+        skb = lds_u32(ksbase + (r0 + r4 + 8) * NB);
+      } else {
+        ska = lds_u16(ksbase + (r0 + r4) * NB);
+        skb = lds_u16(ksbase + (r0 + r4 + 8) * NB);
+      }
+#pragma unroll
+      for (int j = 0; j < NB; ++j) {
+        const float fa = ue8m0_f32((ska >> (8 * j)) & 0xFF), fb = ue8m0_f32((skb >> (8 * j)) & 0xFF);
+        sc[0] = fmaf(acc[j][0], fa, sc[0]);
+        sc[1] = fmaf(acc[j][1], fa, sc[1]);
+        sc[2] = fmaf(acc[j][2], fb, sc[2]);
+        sc[3] = fmaf(acc[j][3], fb, sc[3]);
+      }
     }
     const bool va = tb + r4 < t1, vb = tb + r4 + 8 < t1;
-    const float x0 = va ? sc[0] * p.scale_log2 : -INFINITY;  // token r4,   head 2c4
-    const float x1 = va ? sc[1] * p.scale_log2 : -INFINITY;  // token r4,   head 2c4+1
-    const float x2 = vb ? sc[2] * p.scale_log2 : -INFINITY;  // token r4+8, head 2c4
-    const float x3 = vb ? sc[3] * p.scale_log2 : -INFINITY;  // token r4+8, head 2c4+1
+    const float x0 = va ? sc[0] * sl2 : -INFINITY;  // token r4,   head 2c4
+    const float x1 = va ? sc[1] * sl2 : -INFINITY;  // token r4,   head 2c4+1
+    const float x2 = vb ? sc[2] * sl2 : -INFINITY;  // token r4+8, head 2c4
+    const float x3 = vb ? sc[3] * sl2 : -INFINITY;  // token r4+8, head 2c4+1
     float ma = fmaxf(x0, x2), mb = fmaxf(x1, x3);
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
@@ -252,18 +420,31 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
     pl[(2 * c4 + 1) * 16 + r4] = __bfloat16_as_ushort(q1);
     pl[(2 * c4) * 16 + r4 + 8] = __bfloat16_as_ushort(q2);
     pl[(2 * c4 + 1) * 16 + r4 + 8] = __bfloat16_as_ushort(q3);
-    // rows past the split end may hold anything; P is 0 there, and V is zeroed so that a
-    // non-finite value cannot turn 0 * V into NaN
+    // rows past the split end may hold anything; P is 0 there, and V (codes and scales) is
+    // zeroed so that a non-finite value cannot turn 0 * V into NaN
     if (tb + 16 > t1) {
-      for (int rr = lane >> 4; rr < 16; rr += 2) {
-        if (tb + rr >= t1) {
-          const int row = r0 + rr;
-          const int cb = (lane & 15) * 16;  // 16 lanes x 16 bytes cover 256 bytes (two 128-byte halves)
-          if (cb < D * 2) {
-            const int half = cb >> 7;
-            uint8_t* dst = ring + s * S::kStageBytes + S::kTileBytes + half * (kTileTok * 128) + row * 128 + (cb & 127);
-            *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+      uint8_t* vt = ring + s * S::kCodeStageBytes + S::kTileBytes;
+      if constexpr (!kMx) {
+        for (int rr = lane >> 4; rr < 16; rr += 2) {
+          if (tb + rr >= t1) {
+            const int row = r0 + rr;
+            const int cb = (lane & 15) * 16;  // 16 lanes x 16 bytes cover 256 bytes (two 128-byte halves)
+            if (cb < D * 2) {
+              const int half = cb >> 7;
+              *reinterpret_cast<uint4*>(vt + half * (kTileTok * 128) + row * 128 + (cb & 127)) = make_uint4(0, 0, 0, 0);
+            }
           }
+        }
+      } else {
+        // a row's D code bytes stay inside its own D-byte span under the swizzle
+        for (int idx = lane; idx < 16 * (D / 16); idx += 32) {
+          const int rr = idx / (D / 16);
+          if (tb + rr >= t1) *reinterpret_cast<uint4*>(vt + (r0 + rr) * D + (idx % (D / 16)) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        uint8_t* vst = ring + S::kScaleRingOff + s * 2 * S::kScaleTileBytes + S::kScaleTileBytes;
+        if (lane < 16 && tb + lane >= t1) {
+#pragma unroll
+          for (int j = 0; j < NB; ++j) vst[(r0 + lane) * NB + j] = 0;
         }
       }
       fence_proxy_async_smem();
@@ -274,13 +455,57 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
     const uint32_t l0 = *reinterpret_cast<const uint32_t*>(pl + r4 * 16 + 2 * c4);
     const uint32_t l1 = *reinterpret_cast<const uint32_t*>(pl + r4 * 16 + 8 + 2 * c4);
     // O^T[D x 8] += V^T[D x 16 tok] P^T[16 tok x 8]
+    if constexpr (!kMx) {
 #pragma unroll
-    for (int mt = 0; mt < KS; ++mt) {
-      uint32_t a0, a1, a2, a3;
-      ldmatrix_x4_trans(tile_addr(vbase, r0 + (lane & 7) + 8 * (lane >> 4), mt * 16 + 8 * ((lane >> 3) & 1)), a0, a1,
-                        a2, a3);
-      mma_bf16_16816(o[mt], a0, a1, a2, a3, b0, b1);
-      mma_bf16_16816(o[mt], a0, a1, a2, a3, l0, l1);
+      for (int mt = 0; mt < KS; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4_trans(tile_addr(vbase, r0 + (lane & 7) + 8 * (lane >> 4), mt * 16 + 8 * ((lane >> 3) & 1)), a0,
+                          a1, a2, a3);
+        mma_bf16_16816(o[mt], a0, a1, a2, a3, b0, b1);
+        mma_bf16_16816(o[mt], a0, a1, a2, a3, l0, l1);
+      }
+    } else {
+      // m-tile 2j+f of block j: A row r4 is dim 32j + 4*r4 + 2f, row r4+8 is that dim + 1; the
+      // k slots are tokens 2*c4 (+1) and 2*c4 + 8 (+9), as in P^T.
+      uint32_t s01[NB], s89[NB];  // (token 2c4, 2c4+1) / (2c4+8, 2c4+9) exponent bytes of block j at bits 0 / 16
+      if constexpr (D == 128) {
+        const uint2 x01 = lds_u32x2(vsbase + (r0 + 2 * c4) * NB);
+        const uint2 x89 = lds_u32x2(vsbase + (r0 + 2 * c4 + 8) * NB);
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+          s01[j] = __byte_perm(x01.x, x01.y, 0x0400 + j * 0x0101);
+          s89[j] = __byte_perm(x89.x, x89.y, 0x0400 + j * 0x0101);
+        }
+      } else {
+        const uint32_t x01 = lds_u32(vsbase + (r0 + 2 * c4) * NB);
+        const uint32_t x89 = lds_u32(vsbase + (r0 + 2 * c4 + 8) * NB);
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+          s01[j] = __byte_perm(x01, 0, 0x0200 + j * 0x0101);
+          s89[j] = __byte_perm(x89, 0, 0x0200 + j * 0x0101);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < NB; ++j) {
+        const uint32_t f01 = pscale_pair(s01[j]), f89 = pscale_pair(s89[j]);
+        const uint32_t bh0 = bmul2(b0, f01), bh1 = bmul2(b1, f89), bl0 = bmul2(l0, f01), bl1 = bmul2(l1, f89);
+        const uint32_t w0 = lds_u32(code_addr<D>(vbase, r0 + 2 * c4, 32 * j + 4 * r4));
+        const uint32_t w1 = lds_u32(code_addr<D>(vbase, r0 + 2 * c4 + 1, 32 * j + 4 * r4));
+        const uint32_t w8 = lds_u32(code_addr<D>(vbase, r0 + 2 * c4 + 8, 32 * j + 4 * r4));
+        const uint32_t w9 = lds_u32(code_addr<D>(vbase, r0 + 2 * c4 + 9, 32 * j + 4 * r4));
+        {
+          const uint32_t a0 = e4m3_pair_bf16<0>(w0, w1), a1 = e4m3_pair_bf16<1>(w0, w1);
+          const uint32_t a2 = e4m3_pair_bf16<0>(w8, w9), a3 = e4m3_pair_bf16<1>(w8, w9);
+          mma_bf16_16816(o[2 * j], a0, a1, a2, a3, bh0, bh1);
+          mma_bf16_16816(o[2 * j], a0, a1, a2, a3, bl0, bl1);
+        }
+        {
+          const uint32_t a0 = e4m3_pair_bf16<2>(w0, w1), a1 = e4m3_pair_bf16<3>(w0, w1);
+          const uint32_t a2 = e4m3_pair_bf16<2>(w8, w9), a3 = e4m3_pair_bf16<3>(w8, w9);
+          mma_bf16_16816(o[2 * j + 1], a0, a1, a2, a3, bh0, bh1);
+          mma_bf16_16816(o[2 * j + 1], a0, a1, a2, a3, bl0, bl1);
+        }
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
@@ -298,13 +523,15 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
   float* os = reinterpret_cast<float*>(ring);                 // [warp][8 heads][D]
   float* ml = os + kConsumers * 8 * D;                         // [warp][8 heads][m, l]
+  const float oscale = kMx ? 0x1p64f : 1.f;                    // MXFP8 V: O carried 2^-64
 #pragma unroll
   for (int mt = 0; mt < KS; ++mt) {
-    const int d = mt * 16 + r4;
-    os[(warp * 8 + 2 * c4) * D + d] = o[mt][0];
-    os[(warp * 8 + 2 * c4 + 1) * D + d] = o[mt][1];
-    os[(warp * 8 + 2 * c4) * D + d + 8] = o[mt][2];
-    os[(warp * 8 + 2 * c4 + 1) * D + d + 8] = o[mt][3];
+    const int d = kMx ? 32 * (mt >> 1) + 4 * r4 + 2 * (mt & 1) : mt * 16 + r4;
+    const int d2 = kMx ? d + 1 : d + 8;
+    os[(warp * 8 + 2 * c4) * D + d] = o[mt][0] * oscale;
+    os[(warp * 8 + 2 * c4 + 1) * D + d] = o[mt][1] * oscale;
+    os[(warp * 8 + 2 * c4) * D + d2] = o[mt][2] * oscale;
+    os[(warp * 8 + 2 * c4 + 1) * D + d2] = o[mt][3] * oscale;
   }
   if (r4 == 0) {
     ml[(warp * 8 + 2 * c4) * 2] = m_a;
@@ -393,10 +620,14 @@ size_t attn_workspace_bytes(int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int6
   return (size_t)(bs * Hq * ms * (D + 1)) * sizeof(float);
 }
 
-cudaError_t launch_gqa_decode_attn(const CUtensorMap& tmK, const CUtensorMap& tmV, const uint16_t* q, int64_t ld_q,
-                                   const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t cap,
-                                   int64_t max_kv_len, float scale, uint16_t* out, int32_t* err, void* ws,
-                                   cudaStream_t st, uint8_t* oq, uint8_t* os, const KvPages* pages) {
+namespace {
+
+template <bool kMx>
+cudaError_t launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmKS,
+                         const CUtensorMap& tmVS, const uint16_t* q, int64_t ld_q, const int32_t* kv_len, int64_t bs,
+                         int64_t Hq, int64_t Hkv, int64_t D, int64_t cap, int64_t max_kv_len, float scale,
+                         uint16_t* out, int32_t* err, void* ws, cudaStream_t st, uint8_t* oq, uint8_t* os,
+                         const KvPages* pages) {
   const int chunk = attn_chunk(bs, Hkv, max_kv_len);
   const int ms = (int)((max_kv_len + chunk - 1) / chunk);
   SplitParams p;
@@ -424,15 +655,15 @@ cudaError_t launch_gqa_decode_attn(const CUtensorMap& tmK, const CUtensorMap& tm
   dim3 grid((unsigned)ms, (unsigned)(bs * Hkv));
   cudaError_t e;
   if (D == 128) {
-    const int smem = AttnShape<128>::kSmemBytes;
-    e = cudaFuncSetAttribute(gqa_split_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const int smem = AttnShape<128, kMx>::kSmemBytes;
+    e = cudaFuncSetAttribute(gqa_split_kernel<128, kMx>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    e = launch_k(gqa_split_kernel<128>, grid, dim3(kThreads), smem, st, 1, tmK, tmV, p);
+    e = launch_k(gqa_split_kernel<128, kMx>, grid, dim3(kThreads), smem, st, 1, tmK, tmV, tmKS, tmVS, p);
   } else {
-    const int smem = AttnShape<64>::kSmemBytes;
-    e = cudaFuncSetAttribute(gqa_split_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const int smem = AttnShape<64, kMx>::kSmemBytes;
+    e = cudaFuncSetAttribute(gqa_split_kernel<64, kMx>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    e = launch_k(gqa_split_kernel<64>, grid, dim3(kThreads), smem, st, 1, tmK, tmV, p);
+    e = launch_k(gqa_split_kernel<64, kMx>, grid, dim3(kThreads), smem, st, 1, tmK, tmV, tmKS, tmVS, p);
   }
   if (e != cudaSuccess || ms == 1) return e;
   if (D == 128)
@@ -442,6 +673,25 @@ cudaError_t launch_gqa_decode_attn(const CUtensorMap& tmK, const CUtensorMap& tm
   return launch_k(gqa_combine_kernel<64>, dim3((unsigned)(bs * Hq)), dim3(64), 0, st, 1,
                   static_cast<const float*>(p.o_part), static_cast<const float*>(p.lse), kv_len, (int)Hq, cap, chunk, ms,
                   (int)max_kv_len, out, oq, os);
+}
+
+}  // namespace
+
+cudaError_t launch_gqa_decode_attn(const CUtensorMap& tmK, const CUtensorMap& tmV, const uint16_t* q, int64_t ld_q,
+                                   const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t cap,
+                                   int64_t max_kv_len, float scale, uint16_t* out, int32_t* err, void* ws,
+                                   cudaStream_t st, uint8_t* oq, uint8_t* os, const KvPages* pages) {
+  return launch_split<false>(tmK, tmV, tmK, tmV, q, ld_q, kv_len, bs, Hq, Hkv, D, cap, max_kv_len, scale, out, err, ws,
+                             st, oq, os, pages);
+}
+
+cudaError_t launch_gqa_decode_attn_kv_mx(const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmKS,
+                                         const CUtensorMap& tmVS, const uint16_t* q, int64_t ld_q,
+                                         const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D,
+                                         int64_t cap, int64_t max_kv_len, float scale, uint16_t* out, int32_t* err,
+                                         void* ws, cudaStream_t st, const KvPages* pages) {
+  return launch_split<true>(tmK, tmV, tmKS, tmVS, q, ld_q, kv_len, bs, Hq, Hkv, D, cap, max_kv_len, scale, out, err,
+                            ws, st, nullptr, nullptr, pages);
 }
 
 }  // namespace mxg

@@ -32,6 +32,17 @@ cudaError_t launch_gqa_decode_attn(const CUtensorMap& tmK, const CUtensorMap& tm
                                    int64_t max_kv_len, float scale, uint16_t* out, int32_t* err, void* ws,
                                    cudaStream_t st, uint8_t* oq = nullptr, uint8_t* os = nullptr,
                                    const KvPages* pages = nullptr);
+// MXFP8 K/V: tmK/tmV map E4M3 codes [rows, D]; tmKS/tmVS the UE8M0 scales [rows, D/32] as
+// 16-byte lines [rows * D/32 / 16, 16].
+cudaError_t launch_gqa_decode_attn_kv_mx(const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmKS,
+                                         const CUtensorMap& tmVS, const uint16_t* q, int64_t ld_q,
+                                         const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D,
+                                         int64_t cap, int64_t max_kv_len, float scale, uint16_t* out, int32_t* err,
+                                         void* ws, cudaStream_t st, const KvPages* pages = nullptr);
+// kv_append into an MXFP8 cache (codes [.., D] + scales [.., D/32]); the rows are MX-quantised.
+cudaError_t launch_kv_append_mx(uint8_t* kc, uint8_t* ks, uint8_t* vc, uint8_t* vs, const uint16_t* kn,
+                                const uint16_t* vn, int64_t ld_new, const int32_t* kv_len, int64_t bs, int64_t Hkv,
+                                int64_t D, int64_t cap, int32_t* err, cudaStream_t st, const KvPages* pages = nullptr);
 
 cudaError_t launch_mx_gemm_simt(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs,
                                 int64_t M, int64_t N, int64_t K, const uint16_t* res, uint16_t* c, cudaStream_t st);

@@ -65,6 +65,45 @@ cudaError_t launch_prev_tokens_shift(int32_t* prev, const int32_t* next, int64_t
   return launch_k(prev_tokens_shift_kernel, dim3((unsigned)bs), dim3(256), smem, st, 1, prev, next, (int)W, (int)cw);
 }
 
+// kv_append into an MXFP8 cache: the K and V rows of this step are MX-quantised along D ([S2.1]
+// "FP8 Quantization Strategy": 1x32 blocks, E4M3 + UE8M0) and land at position kv_len-1.
+// One warp per (sequence, kv head); lane i holds element i of each 32-wide block.
+__global__ void __launch_bounds__(256) kv_append_mx_kernel(uint8_t* __restrict__ kc, uint8_t* __restrict__ ks,
+                                                           uint8_t* __restrict__ vc, uint8_t* __restrict__ vs,
+                                                           const uint16_t* __restrict__ kn,
+                                                           const uint16_t* __restrict__ vn, int64_t ld_new,
+                                                           const int32_t* __restrict__ kv_len, int bs, int Hkv, int D,
+                                                           int64_t cap, int32_t* err, KvPages pg) {
+  pdl_trigger();
+  pdl_wait();
+  const int gw = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (gw >= bs * Hkv) return;
+  const int b = gw / Hkv, g = gw - b * Hkv;
+  const int n = kv_len[b];
+  if (n < 1 || (int64_t)n > cap) {
+    if (lane == 0 && g == 0) set_error(err, MXG_EDEVICE);
+    return;
+  }
+  int64_t row = ((int64_t)b * Hkv + g) * cap + (n - 1);
+  if (pg.table) {
+    const int page = pg.table[(int64_t)b * pg.max_pages + (n - 1) / pg.page_size];
+    if (page < 0 || page >= pg.num_pages) {
+      if (lane == 0 && g == 0) set_error(err, MXG_EDEVICE);
+      return;
+    }
+    row = ((int64_t)page * Hkv + g) * pg.page_size + (n - 1) % pg.page_size;
+  }
+  const int64_t src = (int64_t)b * ld_new + (int64_t)g * D;
+  const int nb = D >> 5;
+  for (int j = 0; j < nb; ++j) {
+    const float kv = __uint_as_float((uint32_t)kn[src + 32 * j + lane] << 16);
+    const float vv = __uint_as_float((uint32_t)vn[src + 32 * j + lane] << 16);
+    mx_quant_warp_store(kv, kc + row * D + 32 * j + lane, ks + row * nb + j);
+    mx_quant_warp_store(vv, vc + row * D + 32 * j + lane, vs + row * nb + j);
+  }
+}
+
 cudaError_t launch_kv_append(uint16_t* kc, uint16_t* vc, const uint16_t* kn, const uint16_t* vn, int64_t ld_new,
                              const int32_t* kv_len, int64_t bs, int64_t Hkv, int64_t D, int64_t cap, int32_t* err,
                              cudaStream_t st, const KvPages* pages) {
@@ -73,6 +112,16 @@ cudaError_t launch_kv_append(uint16_t* kc, uint16_t* vc, const uint16_t* kn, con
   const KvPages pg = pages ? *pages : KvPages{};
   return launch_k(kv_append_kernel, dim3((unsigned)blocks), dim3(256), 0, st, 1, kc, vc, kn, vn, ld_new, kv_len,
                   (int)bs, (int)Hkv, (int)D, cap, err, pg);
+}
+
+cudaError_t launch_kv_append_mx(uint8_t* kc, uint8_t* ks, uint8_t* vc, uint8_t* vs, const uint16_t* kn,
+                                const uint16_t* vn, int64_t ld_new, const int32_t* kv_len, int64_t bs, int64_t Hkv,
+                                int64_t D, int64_t cap, int32_t* err, cudaStream_t st, const KvPages* pages) {
+  const int64_t warps = bs * Hkv;
+  const int64_t blocks = (warps * 32 + 255) / 256;
+  const KvPages pg = pages ? *pages : KvPages{};
+  return launch_k(kv_append_mx_kernel, dim3((unsigned)blocks), dim3(256), 0, st, 1, kc, ks, vc, vs, kn, vn, ld_new,
+                  kv_len, (int)bs, (int)Hkv, (int)D, cap, err, pg);
 }
 
 }  // namespace mxg

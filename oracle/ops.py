@@ -172,6 +172,80 @@ def kv_append_paged(k_pool, v_pool, block_table, k_new, v_new, kv_len, page_size
     return k_pool, v_pool
 
 
+# --------------------------------------------------------------------------- prefill / extend
+def gqa_prefill_attention(q_new, k_prefix, v_prefix, scale) -> list:
+    """Causal prefill / extend attention with native GQA ([S2.1] "What's Open Source":
+    contiguous prefill and paged prefill (extend)). Sequence b holds kv_len_b rows in its cache,
+    the last T_b of which belong to the new tokens; new token i sits at position
+    kv_len_b - T_b + i and attends to positions 0 .. kv_len_b - T_b + i (T_b = kv_len_b is a
+    prefill from scratch). q_new[b]: [T_b, Hq, D]; k_prefix[b], v_prefix[b]: [Hkv, kv_len_b, D].
+    Returns o[b]: [T_b, Hq, D] fp64."""
+    out = []
+    for qb, K, V in zip(q_new, k_prefix, v_prefix):
+        qb = np.asarray(qb, np.float64)
+        K = np.asarray(K, np.float64)
+        V = np.asarray(V, np.float64)
+        T, Hq, D = qb.shape
+        Hkv, n = K.shape[0], K.shape[1]
+        grp = Hq // Hkv
+        pos = n - T + np.arange(T)
+        allowed = np.arange(n)[None, :] <= pos[:, None]
+        o = np.zeros((T, Hq, D))
+        for h in range(Hq):
+            g = h // grp
+            s = scale * (qb[:, h, :] @ K[g].T)
+            s = np.where(allowed, s, -np.inf)
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            o[:, h, :] = (p @ V[g]) / p.sum(axis=1, keepdims=True)
+        out.append(o)
+    return out
+
+
+def kv_append_extend(k_cache, v_cache, k_new, v_new, kv_len):
+    """Write T_b new K/V rows per sequence (k_new[b], v_new[b]: [T_b, Hkv, D]) at positions
+    kv_len_b - T_b .. kv_len_b - 1 of the cache [bs, Hkv, cap, D] ([FSKV] §5, kv_cache.update
+    for a prefill or extend)."""
+    k_cache = k_cache.copy()
+    v_cache = v_cache.copy()
+    for b, n in enumerate(np.asarray(kv_len)):
+        T = k_new[b].shape[0]
+        k_cache[b, :, n - T:n, :] = np.transpose(k_new[b], (1, 0, 2))
+        v_cache[b, :, n - T:n, :] = np.transpose(v_new[b], (1, 0, 2))
+    return k_cache, v_cache
+
+
+# --------------------------------------------------------------------------- MXFP8 KV cache
+def kv_rows_mx(rows):
+    """K or V rows [..., D] (fp64 values of bf16 rows) MX-quantised along D: the 1x32-block
+    format of [S2.1] "FP8 Quantization Strategy" (E4M3 elements, UE8M0 shared exponents),
+    applied to the cache as the pages' MXFP8 FlashAttention reads it ("What's Open Source").
+    Returns (codes uint8 [..., D], scale bytes uint8 [..., D/32])."""
+    return mx_quantize(rows)
+
+
+def kv_append_mxfp8(k_codes, k_scales, v_codes, v_scales, k_new, v_new, kv_len):
+    """kv_append into an MXFP8 cache: the new rows k_new, v_new [bs, Hkv, D] (fp64 values of
+    bf16) are MX-quantised along D and written at position kv_len-1 ([FSKV] §5)."""
+    k_codes, k_scales, v_codes, v_scales = (a.copy() for a in (k_codes, k_scales, v_codes, v_scales))
+    kq, ks = kv_rows_mx(k_new)
+    vq, vs = kv_rows_mx(v_new)
+    for b, n in enumerate(np.asarray(kv_len)):
+        k_codes[b, :, n - 1, :] = kq[b]
+        k_scales[b, :, n - 1, :] = ks[b]
+        v_codes[b, :, n - 1, :] = vq[b]
+        v_scales[b, :, n - 1, :] = vs[b]
+    return k_codes, k_scales, v_codes, v_scales
+
+
+def gqa_decode_attention_kv_mxfp8(q, k_codes, k_scales, v_codes, v_scales, scale) -> np.ndarray:
+    """Decode attention over MXFP8 prefixes: every cached row is dequantised exactly
+    (E4M3 value x 2^s of its 32-wide block) and the plain decode attention runs on those
+    values. k_codes[b] [Hkv, kv_len_b, D] uint8, k_scales[b] [Hkv, kv_len_b, D/32] uint8."""
+    K = [mx_dequantize(c, s) for c, s in zip(k_codes, k_scales)]
+    V = [mx_dequantize(c, s) for c, s in zip(v_codes, v_scales)]
+    return gqa_decode_attention(q, K, V, scale)
+
+
 # --------------------------------------------------------------------------- prev window
 def prev_tokens_shift(prev, next_tokens) -> np.ndarray:
     """Slide the Dual-AR previous-tokens window by one frame ([S2.1] "DualAR:
