@@ -68,6 +68,13 @@ def attn_kv_mxfp8_bytes(kv_lens, Hq=HQ, Hkv=HKV, D=HD):
     return kv + len(kv_lens) * Hq * D * 2 * 2
 
 
+def prefill_flops(prefix, new, Hq=HQ, D=HD):
+    """Causal prefill / extend attention flop: new token i of a sequence with P cached positions
+    sees P + i + 1 keys, 2 D flop each for q.k and for p.v, per query head."""
+    p, t = np.asarray(prefix, np.float64), np.asarray(new, np.float64)
+    return float(np.sum(4.0 * D * Hq * (t * p + t * (t + 1) / 2)))
+
+
 def gemm_bytes(M, N, K, residual=False):
     return int(N * K * (1 + 1 / 32) + M * K * (1 + 1 / 32) + M * N * 2 + (M * N * 2 if residual else 0))
 
@@ -446,7 +453,41 @@ def run_sweeps(dev, flush):
         attn[str(bs)] = {"us": round(ms * 1e3, 2), "GB_s": round(attn_bytes(lens) / (ms * 1e-3) / 1e9, 1)}
     del K, V
     return {"mlp_M": mlp, "attn_bs": attn, "attn_paged_bs64": paged_attn_sweep(dev, rn, flush),
-            "attn_kv_mxfp8_bs": kv_mxfp8_attn_sweep(dev, rn, flush), "gemm_square": gemm_square_sweep(dev)}
+            "attn_kv_mxfp8_bs": kv_mxfp8_attn_sweep(dev, rn, flush), "prefill": prefill_sweep(dev, rn, flush),
+            "gemm_square": gemm_square_sweep(dev)}
+
+
+PREFILL_CASES = {"bs64_T234": ([0] * 64, [234] * 64), "bs1_T4096": ([0], [4096]),
+                 "bs4_P2048_T2048": ([2048] * 4, [2048] * 4)}
+
+
+def prefill_setup(dev, rn, prefix, new):
+    """Device inputs of one causal prefill / extend call (caches already holding the new rows)."""
+    import torch
+
+    lens = np.asarray(prefix) + np.asarray(new)
+    cap = int((lens.max() + 127) // 128 * 128)
+    bs, total = len(new), int(np.sum(new))
+    K = rn((bs, HKV, cap, HD))
+    V = rn((bs, HKV, cap, HD))
+    q = rn((total, HQ, HD))
+    q_start = torch.from_numpy(np.concatenate([[0], np.cumsum(new)]).astype(np.int32)).to(dev)
+    kl = torch.from_numpy(lens.astype(np.int32)).to(dev)
+    out = torch.empty((total, HQ, HD), dtype=torch.bfloat16, device=dev)
+    return q, K, V, q_start, kl, out, int(max(new))
+
+
+def prefill_sweep(dev, rn, flush):
+    """Causal prefill / extend attention (tcgen05): TFLOP/s of the causal flop count."""
+    from mxfp8_mlp_gqa_gb300 import api
+
+    res = {}
+    for name, (prefix, new) in PREFILL_CASES.items():
+        q, K, V, qs, kl, out, mq = prefill_setup(dev, rn, prefix, new)
+        ms = _time_op(lambda: api.gqa_prefill_attn(q, K, V, qs, kl, mq, 1 / math.sqrt(HD), out=out), flush)
+        res[name] = {"us": round(ms * 1e3, 2), "TFLOP_s": round(prefill_flops(prefix, new) / (ms * 1e-3) / 1e12, 1)}
+        del q, K, V, out
+    return res
 
 
 def kv_mxfp8_attn_sweep(dev, rn, flush):
@@ -632,6 +673,11 @@ def run_profile(args):
         out = torch.empty((bs, HQ, HD), dtype=torch.bfloat16, device=dev)
         fn = lambda: api.gqa_decode_attn_kv_mxfp8(q, *arrs, kl, KV_HI, 1 / math.sqrt(HD), out=out,  # noqa: E731
                                                   workspace=ws)
+    elif kind == "prefill":
+        # causal prefill / extend attention, one of PREFILL_CASES
+        prefix, new = PREFILL_CASES[arg]
+        q, K, V, qs, kl, pout, mq = prefill_setup(dev, rn, prefix, new)
+        fn = lambda: api.gqa_prefill_attn(q, K, V, qs, kl, mq, 1 / math.sqrt(HD), out=pout)  # noqa: E731
     elif kind == "gemm":
         M, N, K_ = (int(v) for v in arg.split("x"))
         aq, as_ = api.mxfp8_quantize(rn((M, K_)))
@@ -658,6 +704,8 @@ def run_profile(args):
     if kind == "attn":
         out["attn_bytes"] = attn_bytes(lens)
         out["sum_kv_len"] = int(lens.sum())
+    if kind == "prefill":
+        out["TFLOP_s"] = round(prefill_flops(*PREFILL_CASES[arg]) / (ms * 1e-3) / 1e12, 1)
     if kind == "attn_mx":
         out["attn_bytes"] = attn_kv_mxfp8_bytes(lens)
         out["sum_kv_len"] = int(lens.sum())

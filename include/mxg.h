@@ -289,6 +289,60 @@ mxg_status kv_append_mxfp8_paged(uint8_t* k_codes, uint8_t* k_scales, uint8_t* v
                                  int64_t bs, int64_t Hkv, int64_t D, int32_t* err_flag, void* stream);
 
 /*
+ * gqa_prefill_attn -- causal prefill / extend attention with native GQA ([S2.1] "What's Open
+ * Source": contiguous prefill and paged prefill (extend); [FSKV] §5: the cache keeps its
+ * capacity and only the filled prefix is read). Sequence b's new tokens are rows
+ * q_start[b] .. q_start[b+1]-1 of q; their K/V rows are already in the cache (kv_append_extend),
+ * so kv_len[b] counts them: new token i of b sits at position kv_len[b] - T_b + i
+ * (T_b = q_start[b+1] - q_start[b]) and attends to positions 0 .. that position.
+ *   q        bf16 [total_q, Hq, 128], ld_q elements between token rows (>= Hq*128, % 8 == 0).
+ *   k_cache, v_cache bf16 [bs, Hkv, cap, 128] (contiguous).
+ *   q_start  int32 [bs + 1] on the device, non-decreasing, q_start[bs] <= total_q;
+ *   kv_len   int32 [bs] on the device; T_b <= max_q_len and T_b <= kv_len[b] <= cap.
+ *   out      bf16 [total_q, Hq, 128] (rows of tokens that belong to no sequence are not written).
+ *   D must be 128; Hq/Hkv must divide 128 and be <= 16.
+ *   Computed with bf16 products and fp32 accumulation on the tensor cores; P = softmax weights
+ *   enter the PV product in bf16 (|error| <= 2^-8 * max|V| + one bf16 step of the output).
+ *   err_flag: MXG_EDEVICE for a sequence whose lengths break the rules above (it is skipped);
+ *   MXG_ETIMEOUT if a bounded in-kernel wait ran out.
+ */
+mxg_status gqa_prefill_attn(const void* q, int64_t ld_q, const void* k_cache, const void* v_cache,
+                            const int32_t* q_start, const int32_t* kv_len, int64_t bs, int64_t total_q, int64_t Hq,
+                            int64_t Hkv, int64_t D, int64_t cap, int64_t max_q_len, float scale, void* out,
+                            int32_t* err_flag, void* stream);
+
+/*
+ * gqa_prefill_attn_paged -- gqa_prefill_attn over paged pools bf16 [num_pages, Hkv,
+ * page_size, 128] with block_table int32 [bs, max_pages] (layout, page_size rule and page-id
+ * errors of gqa_decode_attn_paged; capacity max_pages * page_size).
+ */
+mxg_status gqa_prefill_attn_paged(const void* q, int64_t ld_q, const void* k_pool, const void* v_pool,
+                                  const int32_t* block_table, int64_t max_pages, int64_t page_size, int64_t num_pages,
+                                  const int32_t* q_start, const int32_t* kv_len, int64_t bs, int64_t total_q,
+                                  int64_t Hq, int64_t Hkv, int64_t D, int64_t max_q_len, float scale, void* out,
+                                  int32_t* err_flag, void* stream);
+
+/*
+ * kv_append_extend -- kv_append of a prefill / extend: row q_start[b] + i of k_new, v_new
+ * (bf16 [total_q, Hkv, D], ld_new elements between token rows) goes to position
+ * kv_len[b] - T_b + i of sequence b's cache [bs, Hkv, cap, D]. Bit-exact copy; D % 8 == 0.
+ * err_flag: MXG_EDEVICE for a sequence with inconsistent lengths (skipped).
+ */
+mxg_status kv_append_extend(void* k_cache, void* v_cache, const void* k_new, const void* v_new, int64_t ld_new,
+                            const int32_t* q_start, const int32_t* kv_len, int64_t bs, int64_t total_q, int64_t Hkv,
+                            int64_t D, int64_t cap, int64_t max_q_len, int32_t* err_flag, void* stream);
+
+/*
+ * kv_append_extend_paged -- kv_append_extend into paged pools (row lookup and errors of
+ * kv_append_paged).
+ */
+mxg_status kv_append_extend_paged(void* k_pool, void* v_pool, const int32_t* block_table, int64_t max_pages,
+                                  int64_t page_size, int64_t num_pages, const void* k_new, const void* v_new,
+                                  int64_t ld_new, const int32_t* q_start, const int32_t* kv_len, int64_t bs,
+                                  int64_t total_q, int64_t Hkv, int64_t D, int64_t max_q_len, int32_t* err_flag,
+                                  void* stream);
+
+/*
  * prev_tokens_shift -- in-place slide of the Dual-AR previous-tokens window ([S2.1]
  * "DualAR: S2-Specific Batching Constraints": prev int32 [bs, W, cw], next_tokens int32
  * [bs, cw], strict shape/dtype contract). prev[b, w] <- prev[b, w+1] for w < W-1 and

@@ -61,6 +61,14 @@ _SIGS = {
                                        c_vp, c_vp]),
     "kv_append_mxfp8_paged": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_i64,
                                              c_vp, c_i64, c_i64, c_i64, c_vp, c_vp]),
+    "gqa_prefill_attn": (ctypes.c_int, [c_vp, c_i64, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_i64, c_i64, c_i64,
+                                        c_i64, c_f32, c_vp, c_vp, c_vp]),
+    "gqa_prefill_attn_paged": (ctypes.c_int, [c_vp, c_i64, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_i64,
+                                              c_i64, c_i64, c_i64, c_i64, c_i64, c_f32, c_vp, c_vp, c_vp]),
+    "kv_append_extend": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_i64, c_vp, c_vp, c_i64, c_i64, c_i64, c_i64, c_i64,
+                                        c_i64, c_vp, c_vp]),
+    "kv_append_extend_paged": (ctypes.c_int, [c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_i64, c_vp, c_vp,
+                                              c_i64, c_i64, c_i64, c_i64, c_i64, c_vp, c_vp]),
 }
 
 
@@ -426,6 +434,90 @@ def kv_append_mxfp8_paged(k_codes, k_scales, v_codes, v_scales, block_table, k_n
     _call("kv_append_mxfp8_paged", _ptr(k_codes), _ptr(k_scales), _ptr(v_codes), _ptr(v_scales), _ptr(block_table),
           max_pages, page_size, num_pages, _ptr(k_new), _ptr(v_new), Hkv * D, _ptr(kv_len), bs, Hkv, D, _ptr(err),
           _stream())
+
+
+def _prefill_common(q, q_start, kv_len, max_q_len):
+    _check(q, "q", torch.bfloat16, ndim=3)
+    total_q, Hq, D = q.shape
+    _check(q_start, "q_start", torch.int32, ndim=1)
+    bs = q_start.shape[0] - 1
+    _check(kv_len, "kv_len", torch.int32, (bs,))
+    return total_q, Hq, D, bs
+
+
+def gqa_prefill_attn(q, k_cache, v_cache, q_start, kv_len, max_q_len, scale, out=None, err=None):
+    """Causal prefill / extend attention: q bf16 [total_q, Hq, 128] (new tokens of all sequences,
+    sequence b at rows q_start[b] .. q_start[b+1]-1), caches bf16 [bs, Hkv, cap, 128] already
+    holding the new rows, kv_len int32 [bs] counting them -> out bf16 [total_q, Hq, 128]."""
+    total_q, Hq, D, bs = _prefill_common(q, q_start, kv_len, max_q_len)
+    _check(k_cache, "k_cache", torch.bfloat16, ndim=4)
+    _, Hkv, cap, _ = k_cache.shape
+    _check(k_cache, "k_cache", torch.bfloat16, (bs, Hkv, cap, D))
+    _check(v_cache, "v_cache", torch.bfloat16, (bs, Hkv, cap, D))
+    out = _out(out, "out", torch.bfloat16, (total_q, Hq, D), q.device)
+    if err is not None:
+        _check(err, "err", torch.int32, (1,))
+    _call("gqa_prefill_attn", _ptr(q), Hq * D, _ptr(k_cache), _ptr(v_cache), _ptr(q_start), _ptr(kv_len), bs,
+          total_q, Hq, Hkv, D, cap, int(max_q_len), float(scale), _ptr(out), _ptr(err), _stream())
+    return out
+
+
+def gqa_prefill_attn_paged(q, k_pool, v_pool, block_table, q_start, kv_len, max_q_len, scale, out=None, err=None):
+    """gqa_prefill_attn over paged pools bf16 [num_pages, Hkv, page_size, 128]."""
+    total_q, Hq, D, bs = _prefill_common(q, q_start, kv_len, max_q_len)
+    _check(k_pool, "k_pool", torch.bfloat16, ndim=4)
+    num_pages, Hkv, page_size, _ = k_pool.shape
+    _check(k_pool, "k_pool", torch.bfloat16, (num_pages, Hkv, page_size, D))
+    _check(v_pool, "v_pool", torch.bfloat16, (num_pages, Hkv, page_size, D))
+    _check(block_table, "block_table", torch.int32, ndim=2)
+    if block_table.shape[0] != bs:
+        raise ValueError("block_table: expected one row per sequence")
+    max_pages = block_table.shape[1]
+    out = _out(out, "out", torch.bfloat16, (total_q, Hq, D), q.device)
+    if err is not None:
+        _check(err, "err", torch.int32, (1,))
+    _call("gqa_prefill_attn_paged", _ptr(q), Hq * D, _ptr(k_pool), _ptr(v_pool), _ptr(block_table), max_pages,
+          page_size, num_pages, _ptr(q_start), _ptr(kv_len), bs, total_q, Hq, Hkv, D, int(max_q_len), float(scale),
+          _ptr(out), _ptr(err), _stream())
+    return out
+
+
+def kv_append_extend(k_cache, v_cache, k_new, v_new, q_start, kv_len, max_q_len, err=None):
+    """Write the new tokens' K/V rows (bf16 [total_q, Hkv, D]) into caches [bs, Hkv, cap, D] at
+    positions kv_len[b] - T_b .. kv_len[b] - 1."""
+    _check(k_cache, "k_cache", torch.bfloat16, ndim=4)
+    bs, Hkv, cap, D = k_cache.shape
+    _check(v_cache, "v_cache", torch.bfloat16, (bs, Hkv, cap, D))
+    _check(k_new, "k_new", torch.bfloat16, ndim=3)
+    total_q = k_new.shape[0]
+    _check(k_new, "k_new", torch.bfloat16, (total_q, Hkv, D))
+    _check(v_new, "v_new", torch.bfloat16, (total_q, Hkv, D))
+    _check(q_start, "q_start", torch.int32, (bs + 1,))
+    _check(kv_len, "kv_len", torch.int32, (bs,))
+    if err is not None:
+        _check(err, "err", torch.int32, (1,))
+    _call("kv_append_extend", _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), Hkv * D, _ptr(q_start),
+          _ptr(kv_len), bs, total_q, Hkv, D, cap, int(max_q_len), _ptr(err), _stream())
+
+
+def kv_append_extend_paged(k_pool, v_pool, block_table, k_new, v_new, q_start, kv_len, max_q_len, err=None):
+    """kv_append_extend into paged pools bf16 [num_pages, Hkv, page_size, D]."""
+    _check(k_pool, "k_pool", torch.bfloat16, ndim=4)
+    num_pages, Hkv, page_size, D = k_pool.shape
+    _check(v_pool, "v_pool", torch.bfloat16, (num_pages, Hkv, page_size, D))
+    _check(block_table, "block_table", torch.int32, ndim=2)
+    bs, max_pages = block_table.shape
+    _check(k_new, "k_new", torch.bfloat16, ndim=3)
+    total_q = k_new.shape[0]
+    _check(k_new, "k_new", torch.bfloat16, (total_q, Hkv, D))
+    _check(v_new, "v_new", torch.bfloat16, (total_q, Hkv, D))
+    _check(q_start, "q_start", torch.int32, (bs + 1,))
+    _check(kv_len, "kv_len", torch.int32, (bs,))
+    if err is not None:
+        _check(err, "err", torch.int32, (1,))
+    _call("kv_append_extend_paged", _ptr(k_pool), _ptr(v_pool), _ptr(block_table), max_pages, page_size, num_pages,
+          _ptr(k_new), _ptr(v_new), Hkv * D, _ptr(q_start), _ptr(kv_len), bs, total_q, Hkv, D, int(max_q_len),
+          _ptr(err), _stream())
 
 
 def gqa_decode_attn_noalloc(q, k_cache, v_cache, kv_len, max_kv_len, scale, out):

@@ -46,6 +46,19 @@ bool make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* ba
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D tensor map (innermost dimension first; strides of dimensions 1 and 2 in bytes).
+bool make_tensor_map_3d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, const uint64_t (&dims)[3],
+                        const uint64_t (&stride_bytes)[2], const uint32_t (&box)[3], CUtensorMapSwizzle swz) {
+  auto fn = encode_tiled_fn();
+  if (!fn) return false;
+  cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  cuuint64_t st[2] = {stride_bytes[0], stride_bytes[1]};
+  cuuint32_t bx[3] = {box[0], box[1], box[2]};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, dt, 3, const_cast<void*>(base), d, st, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace mxg
 
 using namespace mxg;
@@ -251,6 +264,55 @@ mxg_status kv_append_mx_call(uint8_t* kc, uint8_t* ks, uint8_t* vc, uint8_t* vs,
                                       (cudaStream_t)stream, pages));
 }
 
+// Causal prefill / extend attention (D = 128) over contiguous caches or paged pools.
+mxg_status prefill_call(const void* q, int64_t ld_q, const void* k_cache, const void* v_cache,
+                        const int32_t* q_start, const int32_t* kv_len, int64_t bs, int64_t total_q, int64_t Hq,
+                        int64_t Hkv, int64_t D, int64_t cap, int64_t max_q_len, float scale, void* out,
+                        int32_t* err_flag, void* stream, const KvPages* pages = nullptr) {
+  if (!q || !k_cache || !v_cache || !q_start || !kv_len || !out) return MXG_EINVAL;
+  if (!(scale > 0.f) || !(scale < 1e30f)) return MXG_EINVAL;
+  if (bs < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D != 128 || cap <= 0 || total_q < 0 || max_q_len < 0 ||
+      ld_q < Hq * D)
+    return MXG_ESHAPE;
+  const int64_t G = Hq / Hkv;
+  if (128 % G || G > 16) return MXG_ESHAPE;
+  const int64_t rows_total = pages ? pages->num_pages * Hkv * pages->page_size : bs * Hkv * cap;
+  if (rows_total >= ((int64_t)1 << 31) || bs * Hkv > 65535 || total_q >= ((int64_t)1 << 31) ||
+      max_q_len > ((int64_t)1 << 30))
+    return MXG_ESHAPE;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || ld_q % 8) return MXG_EALIGN;
+  if (bs == 0 || total_q == 0 || max_q_len == 0) return MXG_OK;
+  CUtensorMap tq, tk, tv;
+  const uint64_t qdims[3] = {(uint64_t)D, (uint64_t)Hq, (uint64_t)total_q};
+  const uint64_t qstr[2] = {(uint64_t)D * 2, (uint64_t)ld_q * 2};
+  const uint32_t qbox[3] = {64, (uint32_t)G, (uint32_t)(128 / G)};
+  if (!make_tensor_map_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, qdims, qstr, qbox, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tensor_map_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_cache, (uint64_t)D, (uint64_t)rows_total,
+                          (uint64_t)D * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tensor_map_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v_cache, (uint64_t)D, (uint64_t)rows_total,
+                          (uint64_t)D * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+    return MXG_ENOTSUP;
+  return launched(launch_gqa_prefill_attn(tq, tk, tv, q_start, kv_len, bs, Hq, Hkv, cap, total_q, max_q_len, scale,
+                                          static_cast<uint16_t*>(out), err_flag, (cudaStream_t)stream, pages));
+}
+
+mxg_status append_extend_call(void* k_cache, void* v_cache, const void* k_new, const void* v_new, int64_t ld_new,
+                              const int32_t* q_start, const int32_t* kv_len, int64_t bs, int64_t total_q,
+                              int64_t Hkv, int64_t D, int64_t cap, int64_t max_q_len, int32_t* err_flag,
+                              void* stream, const KvPages* pages = nullptr) {
+  if (!k_cache || !v_cache || !k_new || !v_new || !q_start || !kv_len) return MXG_EINVAL;
+  if (bs < 0 || Hkv <= 0 || D <= 0 || D % 8 || D > 1024 || cap <= 0 || total_q < 0 || max_q_len < 0 ||
+      ld_new < Hkv * D || bs > 65535)
+    return MXG_ESHAPE;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new) || ld_new % 8)
+    return MXG_EALIGN;
+  if (bs == 0 || total_q == 0 || max_q_len == 0) return MXG_OK;
+  return launched(launch_kv_append_extend(static_cast<uint16_t*>(k_cache), static_cast<uint16_t*>(v_cache),
+                                          static_cast<const uint16_t*>(k_new), static_cast<const uint16_t*>(v_new),
+                                          ld_new, q_start, kv_len, bs, Hkv, D, cap, total_q, max_q_len, err_flag,
+                                          (cudaStream_t)stream, pages));
+}
+
 // The page-table arguments shared by the paged entry points; 0 if valid.
 mxg_status check_pages(const int32_t* table, int64_t max_pages, int64_t page_size, int64_t num_pages) {
   if (!table) return MXG_EINVAL;
@@ -403,6 +465,53 @@ mxg_status kv_append_mxfp8_paged(uint8_t* k_codes, uint8_t* k_scales, uint8_t* v
   pg.num_pages = num_pages;
   return kv_append_mx_call(k_codes, k_scales, v_codes, v_scales, k_new, v_new, ld_new, kv_len, bs, Hkv, D,
                            max_pages * page_size, err_flag, stream, &pg);
+}
+
+mxg_status gqa_prefill_attn(const void* q, int64_t ld_q, const void* k_cache, const void* v_cache,
+                            const int32_t* q_start, const int32_t* kv_len, int64_t bs, int64_t total_q, int64_t Hq,
+                            int64_t Hkv, int64_t D, int64_t cap, int64_t max_q_len, float scale, void* out,
+                            int32_t* err_flag, void* stream) {
+  return prefill_call(q, ld_q, k_cache, v_cache, q_start, kv_len, bs, total_q, Hq, Hkv, D, cap, max_q_len, scale, out,
+                      err_flag, stream);
+}
+
+mxg_status gqa_prefill_attn_paged(const void* q, int64_t ld_q, const void* k_pool, const void* v_pool,
+                                  const int32_t* block_table, int64_t max_pages, int64_t page_size, int64_t num_pages,
+                                  const int32_t* q_start, const int32_t* kv_len, int64_t bs, int64_t total_q,
+                                  int64_t Hq, int64_t Hkv, int64_t D, int64_t max_q_len, float scale, void* out,
+                                  int32_t* err_flag, void* stream) {
+  const mxg_status c = check_pages(block_table, max_pages, page_size, num_pages);
+  if (c != MXG_OK) return c;
+  KvPages pg;
+  pg.table = block_table;
+  pg.max_pages = (int)max_pages;
+  pg.page_size = (int)page_size;
+  pg.num_pages = num_pages;
+  return prefill_call(q, ld_q, k_pool, v_pool, q_start, kv_len, bs, total_q, Hq, Hkv, D, max_pages * page_size,
+                      max_q_len, scale, out, err_flag, stream, &pg);
+}
+
+mxg_status kv_append_extend(void* k_cache, void* v_cache, const void* k_new, const void* v_new, int64_t ld_new,
+                            const int32_t* q_start, const int32_t* kv_len, int64_t bs, int64_t total_q, int64_t Hkv,
+                            int64_t D, int64_t cap, int64_t max_q_len, int32_t* err_flag, void* stream) {
+  return append_extend_call(k_cache, v_cache, k_new, v_new, ld_new, q_start, kv_len, bs, total_q, Hkv, D, cap,
+                            max_q_len, err_flag, stream);
+}
+
+mxg_status kv_append_extend_paged(void* k_pool, void* v_pool, const int32_t* block_table, int64_t max_pages,
+                                  int64_t page_size, int64_t num_pages, const void* k_new, const void* v_new,
+                                  int64_t ld_new, const int32_t* q_start, const int32_t* kv_len, int64_t bs,
+                                  int64_t total_q, int64_t Hkv, int64_t D, int64_t max_q_len, int32_t* err_flag,
+                                  void* stream) {
+  const mxg_status c = check_pages(block_table, max_pages, page_size, num_pages);
+  if (c != MXG_OK) return c;
+  KvPages pg;
+  pg.table = block_table;
+  pg.max_pages = (int)max_pages;
+  pg.page_size = (int)page_size;
+  pg.num_pages = num_pages;
+  return append_extend_call(k_pool, v_pool, k_new, v_new, ld_new, q_start, kv_len, bs, total_q, Hkv, D,
+                            max_pages * page_size, max_q_len, err_flag, stream, &pg);
 }
 
 mxg_status prev_tokens_shift(int32_t* prev, const int32_t* next_tokens, int64_t bs, int64_t W, int64_t cw,

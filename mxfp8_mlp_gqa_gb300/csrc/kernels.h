@@ -39,6 +39,16 @@ cudaError_t launch_gqa_decode_attn_kv_mx(const CUtensorMap& tmK, const CUtensorM
                                          const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D,
                                          int64_t cap, int64_t max_kv_len, float scale, uint16_t* out, int32_t* err,
                                          void* ws, cudaStream_t st, const KvPages* pages = nullptr);
+// Causal prefill / extend attention (tcgen05, D = 128): tmQ maps q as [total_q, Hq, 128] bf16
+// (box {64, G, 128/G}), tmK/tmV the cache rows [rows, 128] bf16 (box {64, 64}, 128-byte swizzle).
+cudaError_t launch_gqa_prefill_attn(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                    const int32_t* q_start, const int32_t* kv_len, int64_t bs, int64_t Hq,
+                                    int64_t Hkv, int64_t cap, int64_t total_q, int64_t max_q_len, float scale,
+                                    uint16_t* out, int32_t* err, cudaStream_t st, const KvPages* pages = nullptr);
+cudaError_t launch_kv_append_extend(uint16_t* kc, uint16_t* vc, const uint16_t* kn, const uint16_t* vn,
+                                    int64_t ld_new, const int32_t* q_start, const int32_t* kv_len, int64_t bs,
+                                    int64_t Hkv, int64_t D, int64_t cap, int64_t total_q, int64_t max_q_len,
+                                    int32_t* err, cudaStream_t st, const KvPages* pages = nullptr);
 // kv_append into an MXFP8 cache (codes [.., D] + scales [.., D/32]); the rows are MX-quantised.
 cudaError_t launch_kv_append_mx(uint8_t* kc, uint8_t* ks, uint8_t* vc, uint8_t* vs, const uint16_t* kn,
                                 const uint16_t* vn, int64_t ld_new, const int32_t* kv_len, int64_t bs, int64_t Hkv,
