@@ -27,6 +27,12 @@
  *     `err_flag` (first error code wins; the caller zeroes it) -- no kernel ever traps.
  *   - Launch failures return MXG_ELAUNCH.
  *   - Alignment: every pointer 16-byte aligned; ld values multiples of 8 (bf16) / 16 (bytes).
+ *   - Kernels are chained with programmatic dependent launch: a GEMM / MLP call starts copying
+ *     its WEIGHT operand (bq/bs of mxfp8_gemm, the W13/W2/Wqkv codes and scales) before the
+ *     previous kernel on the stream has finished, so a weight must not be written by the
+ *     kernel that immediately precedes the call on that stream (prepare weights at setup).
+ *     Activations and outputs are touched only after the previous kernel completes.
+ *     Environment variable MXG_PDL=0 turns the chaining off.
  */
 #ifndef MXG_H
 #define MXG_H
