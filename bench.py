@@ -10,7 +10,8 @@ metric/unit: HBM GB/s = algorithmic bytes of the step / step time (the step's KV
 weights and activations; see the design doc for the per-kernel byte counts). The line also
 carries the MLP-only sweep (M = 1..128: us and GB/s), the attention-only sweep (bs = 1..64:
 GB/s), the paged-attention sweep (bs = 64, pages of 64/128/256), the MXFP8-KV attention sweep
-(bs = 1..64 and paged) and the square MXFP8 GEMM sweep, each timed the same way.
+(bs = 1..64 and paged), the prefill / extend attention sweep (TFLOP/s), the block-scaled FP8
+(bsgemm) sweep and the square MXFP8 GEMM sweep, each timed the same way.
 
 Timing: W untimed warm-up steps, then K steps each bracketed by CUDA events on the
 launching stream, with a 256 MiB L2 flush between steps (outside the events);
@@ -454,7 +455,43 @@ def run_sweeps(dev, flush):
     del K, V
     return {"mlp_M": mlp, "attn_bs": attn, "attn_paged_bs64": paged_attn_sweep(dev, rn, flush),
             "attn_kv_mxfp8_bs": kv_mxfp8_attn_sweep(dev, rn, flush), "prefill": prefill_sweep(dev, rn, flush),
+            "bsgemm": bsgemm_sweep(dev, rn, flush),
             "gemm_square": gemm_square_sweep(dev)}
+
+
+def bsgemm_bytes(M, N, K):
+    """Block-scaled FP8 GEMM: E4M3 weights + one fp32 scale per 128x128 block, E4M3 activations
+    + one fp32 scale per 1x128 block, bf16 out."""
+    return int(N * K + ((N + 127) // 128) * (K // 128) * 4 + M * K + M * (K // 128) * 4 + M * N * 2)
+
+
+def bsgemm_sweep(dev, rn, flush):
+    """bsgemm recipe at the decode MLP's two weight shapes (gate/up 19456x2560, down
+    2560x9728), next to the MXFP8 GEMM on the same shapes: us and GB/s of each format's bytes."""
+    import torch
+
+    from mxfp8_mlp_gqa_gb300 import api
+
+    res = {}
+    for name, (N, K) in {"gate_up": (2 * D_FF, D_MODEL), "down": (D_MODEL, D_FF)}.items():
+        wb = rn((N, K), 0.02)
+        wq, ws = api.bs_quantize_weight(wb)
+        mq, ms_ = api.mxfp8_quantize(wb)
+        del wb
+        for M in (1, 16, 64, 128):
+            x = rn((M, K))
+            xq, xs = api.bs_quantize_act(x)
+            mxq, mxs = api.mxfp8_quantize(x)
+            out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            wsb = torch.empty(max(1, api.bs_gemm_workspace(M, N, K)), dtype=torch.uint8, device=dev)
+            wsm = torch.zeros(max(1, api.lib().mxfp8_gemm_workspace(M, N, K)), dtype=torch.uint8, device=dev)
+            t_bs = _time_op(lambda: api.bs_gemm(xq, xs, wq, ws, out=out, workspace=wsb), flush)
+            t_mx = _time_op(lambda: api.mxfp8_gemm(mxq, mxs, mq, ms_, c=out, workspace=wsm), flush)
+            res[f"{name}_M{M}"] = {"us": round(t_bs * 1e3, 2),
+                                   "GB_s": round(bsgemm_bytes(M, N, K) / (t_bs * 1e-3) / 1e9, 1),
+                                   "mxfp8_us": round(t_mx * 1e3, 2)}
+        del wq, ws, mq, ms_
+    return res
 
 
 PREFILL_CASES = {"bs64_T234": ([0] * 64, [234] * 64), "bs1_T4096": ([0], [4096]),

@@ -349,6 +349,33 @@ mxg_status kv_append_extend_paged(void* k_pool, void* v_pool, const int32_t* blo
                                   void* stream);
 
 /*
+ * Block-scaled FP8, the pages' "bsgemm" recipe ([S2.1] "FP8 Quantization Strategy": 128x128
+ * block-scaled FP8; "What's Open Source": 1x128 activation x 128x128 weight blocks). Each block
+ * has one fp32 scale s = amax / 448 (fp32 division) and E4M3 elements E4M3(x / s) (fp32
+ * division, round to nearest even, saturating at +-448); a block with amax 0 has s = 0 and
+ * signed-zero elements.
+ *
+ * bs_quantize_act -- x bf16 [M, K] (row stride ld_x) -> q E4M3 [M, K], s fp32 [M, K/128].
+ * bs_quantize_weight -- w bf16 [N, K] (contiguous) -> q E4M3 [N, K], s fp32
+ *   [ceil(N/128), K/128] (the last row block may be shorter than 128 rows).
+ * Both bit-identical to the rule above; K % 128 == 0.
+ */
+mxg_status bs_quantize_act(const void* x, int64_t M, int64_t K, int64_t ld_x, uint8_t* q, float* s, void* stream);
+mxg_status bs_quantize_weight(const void* w, int64_t N, int64_t K, uint8_t* q, float* s, void* stream);
+
+/*
+ * bs_gemm -- out[m][n] = sum over 128-wide K blocks kb of xs[m][kb] * ws[n/128][kb] *
+ * (E4M3 xq[m, kb block] . E4M3 wq[n, kb block]), bf16 out [M, N] (contiguous). Operands as
+ * produced by bs_quantize_act / bs_quantize_weight (xq [M, K], wq [N, K], contiguous).
+ * Products of each block on the tensor cores in fp32, block scales applied in fp32.
+ * workspace: bs_gemm_workspace(M, N, K) bytes (0 when K is not split), 16-byte aligned.
+ * err_flag: MXG_ETIMEOUT if a bounded in-kernel wait ran out.
+ */
+size_t bs_gemm_workspace(int64_t M, int64_t N, int64_t K);
+mxg_status bs_gemm(const uint8_t* xq, const float* xs, const uint8_t* wq, const float* ws, int64_t M, int64_t N,
+                   int64_t K, void* out, void* workspace, size_t ws_bytes, int32_t* err_flag, void* stream);
+
+/*
  * prev_tokens_shift -- in-place slide of the Dual-AR previous-tokens window ([S2.1]
  * "DualAR: S2-Specific Batching Constraints": prev int32 [bs, W, cw], next_tokens int32
  * [bs, cw], strict shape/dtype contract). prev[b, w] <- prev[b, w+1] for w < W-1 and

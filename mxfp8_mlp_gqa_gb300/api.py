@@ -67,6 +67,10 @@ _SIGS = {
                                               c_i64, c_i64, c_i64, c_i64, c_i64, c_f32, c_vp, c_vp, c_vp]),
     "kv_append_extend": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_i64, c_vp, c_vp, c_i64, c_i64, c_i64, c_i64, c_i64,
                                         c_i64, c_vp, c_vp]),
+    "bs_quantize_act": (ctypes.c_int, [c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_vp]),
+    "bs_quantize_weight": (ctypes.c_int, [c_vp, c_i64, c_i64, c_vp, c_vp, c_vp]),
+    "bs_gemm_workspace": (c_sz, [c_i64, c_i64, c_i64]),
+    "bs_gemm": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_sz, c_vp, c_vp]),
     "kv_append_extend_paged": (ctypes.c_int, [c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_i64, c_vp, c_vp,
                                               c_i64, c_i64, c_i64, c_i64, c_i64, c_vp, c_vp]),
 }
@@ -518,6 +522,53 @@ def kv_append_extend_paged(k_pool, v_pool, block_table, k_new, v_new, q_start, k
     _call("kv_append_extend_paged", _ptr(k_pool), _ptr(v_pool), _ptr(block_table), max_pages, page_size, num_pages,
           _ptr(k_new), _ptr(v_new), Hkv * D, _ptr(q_start), _ptr(kv_len), bs, total_q, Hkv, D, int(max_q_len),
           _ptr(err), _stream())
+
+
+# ------------------------------------------------------------------ block-scaled FP8 (bsgemm recipe)
+def bs_quantize_act(x, q=None, s=None):
+    """bf16 [M, K] -> (E4M3 codes [M, K], fp32 scales [M, K/128]): 1x128 blocks."""
+    ld = _rows_view(x, "x", torch.bfloat16)
+    M, K = x.shape
+    q = _out(q, "q", torch.uint8, (M, K), x.device)
+    s = _out(s, "s", torch.float32, (M, K // 128), x.device)
+    _call("bs_quantize_act", _ptr(x), M, K, ld, _ptr(q), _ptr(s), _stream())
+    return q, s
+
+
+def bs_quantize_weight(w, q=None, s=None):
+    """bf16 [N, K] -> (E4M3 codes [N, K], fp32 scales [ceil(N/128), K/128]): 128x128 blocks."""
+    _check(w, "w", torch.bfloat16, ndim=2)
+    N, K = w.shape
+    q = _out(q, "q", torch.uint8, (N, K), w.device)
+    s = _out(s, "s", torch.float32, ((N + 127) // 128, K // 128), w.device)
+    _call("bs_quantize_weight", _ptr(w), N, K, _ptr(q), _ptr(s), _stream())
+    return q, s
+
+
+def bs_gemm_workspace(M, N, K):
+    return int(lib().bs_gemm_workspace(M, N, K))
+
+
+def bs_gemm(xq, xs, wq, ws, out=None, workspace=None, err=None):
+    """out[M, N] (bf16) = block-scaled X' W'^T; xq/xs from bs_quantize_act, wq/ws from
+    bs_quantize_weight."""
+    _check(xq, "xq", torch.uint8, ndim=2)
+    M, K = xq.shape
+    _check(xs, "xs", torch.float32, (M, K // 128))
+    _check(wq, "wq", torch.uint8, ndim=2)
+    N = wq.shape[0]
+    _check(wq, "wq", torch.uint8, (N, K))
+    _check(ws, "ws", torch.float32, ((N + 127) // 128, K // 128))
+    out = _out(out, "out", torch.bfloat16, (M, N), xq.device)
+    if err is not None:
+        _check(err, "err", torch.int32, (1,))
+    need = bs_gemm_workspace(M, N, K)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=xq.device)
+    ws_bytes = 0 if workspace is None else workspace.numel()
+    _call("bs_gemm", _ptr(xq), _ptr(xs), _ptr(wq), _ptr(ws), M, N, K, _ptr(out), _ptr(workspace), ws_bytes, _ptr(err),
+          _stream())
+    return out
 
 
 def gqa_decode_attn_noalloc(q, k_cache, v_cache, kv_len, max_kv_len, scale, out):

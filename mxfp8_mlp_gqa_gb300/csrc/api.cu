@@ -514,6 +514,39 @@ mxg_status kv_append_extend_paged(void* k_pool, void* v_pool, const int32_t* blo
                             max_pages * page_size, max_q_len, err_flag, stream, &pg);
 }
 
+mxg_status bs_quantize_act(const void* x, int64_t M, int64_t K, int64_t ld_x, uint8_t* q, float* s, void* stream) {
+  if (!x || !q || !s) return MXG_EINVAL;
+  if (M < 0 || K <= 0 || K % 128 || ld_x < K || M >= ((int64_t)1 << 31)) return MXG_ESHAPE;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(s) || ld_x % 8) return MXG_EALIGN;
+  if (M == 0) return MXG_OK;
+  return launched(launch_bs_quantize_act(static_cast<const uint16_t*>(x), M, K, ld_x, q, s, (cudaStream_t)stream));
+}
+
+mxg_status bs_quantize_weight(const void* w, int64_t N, int64_t K, uint8_t* q, float* s, void* stream) {
+  if (!w || !q || !s) return MXG_EINVAL;
+  if (N < 0 || K <= 0 || K % 128 || N >= ((int64_t)1 << 31) || (N + 127) / 128 > 65535) return MXG_ESHAPE;
+  if (!aligned16(w) || !aligned16(q) || !aligned16(s)) return MXG_EALIGN;
+  if (N == 0) return MXG_OK;
+  return launched(launch_bs_quantize_weight(static_cast<const uint16_t*>(w), N, K, q, s, (cudaStream_t)stream));
+}
+
+size_t bs_gemm_workspace(int64_t M, int64_t N, int64_t K) { return bs_gemm_workspace_bytes(M, N, K); }
+
+mxg_status bs_gemm(const uint8_t* xq, const float* xs, const uint8_t* wq, const float* ws, int64_t M, int64_t N,
+                   int64_t K, void* out, void* workspace, size_t ws_bytes, int32_t* err_flag, void* stream) {
+  if (!xq || !xs || !wq || !ws || !out) return MXG_EINVAL;
+  if (M < 0 || N <= 0 || K <= 0 || K % 128 || M >= ((int64_t)1 << 31) || N >= ((int64_t)1 << 31) ||
+      (N + 127) / 128 > 65535)
+    return MXG_ESHAPE;
+  if (!aligned16(xq) || !aligned16(xs) || !aligned16(wq) || !aligned16(ws) || !aligned16(out)) return MXG_EALIGN;
+  if (M == 0) return MXG_OK;
+  const size_t need = bs_gemm_workspace_bytes(M, N, K);
+  if (need && (!workspace || ws_bytes < need)) return MXG_EWORKSPACE;
+  if (need && !aligned16(workspace)) return MXG_EALIGN;
+  return launched(launch_bs_gemm(xq, xs, wq, ws, M, N, K, static_cast<uint16_t*>(out), workspace, err_flag,
+                                 (cudaStream_t)stream));
+}
+
 mxg_status prev_tokens_shift(int32_t* prev, const int32_t* next_tokens, int64_t bs, int64_t W, int64_t cw,
                              void* stream) {
   if (!prev || !next_tokens) return MXG_EINVAL;

@@ -49,6 +49,13 @@ cudaError_t launch_kv_append_extend(uint16_t* kc, uint16_t* vc, const uint16_t* 
                                     int64_t ld_new, const int32_t* q_start, const int32_t* kv_len, int64_t bs,
                                     int64_t Hkv, int64_t D, int64_t cap, int64_t total_q, int64_t max_q_len,
                                     int32_t* err, cudaStream_t st, const KvPages* pages = nullptr);
+// Block-scaled FP8 (bsgemm recipe): 1x128 activation and 128x128 weight blocks, fp32 scales.
+cudaError_t launch_bs_quantize_act(const uint16_t* x, int64_t M, int64_t K, int64_t ld_x, uint8_t* q, float* s,
+                                   cudaStream_t st);
+cudaError_t launch_bs_quantize_weight(const uint16_t* w, int64_t N, int64_t K, uint8_t* q, float* s, cudaStream_t st);
+size_t bs_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_bs_gemm(const uint8_t* xq, const float* xs, const uint8_t* wq, const float* ws, int64_t M,
+                           int64_t N, int64_t K, uint16_t* out, void* workspace, int32_t* err, cudaStream_t st);
 // kv_append into an MXFP8 cache (codes [.., D] + scales [.., D/32]); the rows are MX-quantised.
 cudaError_t launch_kv_append_mx(uint8_t* kc, uint8_t* ks, uint8_t* vc, uint8_t* vs, const uint16_t* kn,
                                 const uint16_t* vn, int64_t ld_new, const int32_t* kv_len, int64_t bs, int64_t Hkv,
