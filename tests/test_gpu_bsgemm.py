@@ -71,3 +71,18 @@ def test_gemm_sampled_at_the_gate_up_shape():
     wsel = mx.e4m3_value(wq_o[cols]) * np.repeat(ws_o.astype(np.float64)[cols // 128], 128, axis=1)
     ref = bs.bs_dequantize_act(oq, os_) @ wsel.T
     assert_float_close(out[:, cols], ref)
+
+
+def test_several_token_tiles_and_host_checks():
+    M, N, K = 300, 640, 1024  # three 128-token tiles, a ragged last one
+    x = _bits((M, K), 1.0, 9, synth.TID["x"])
+    w = _bits((N, K), 0.02, 10, synth.TID["w13"])
+    xq, xs = api.bs_quantize_act(dev_bf16(x))
+    wq, ws = api.bs_quantize_weight(dev_bf16(w))
+    out = api.bs_gemm(xq, xs, wq, ws)
+    oq, os_ = bs.bs_quantize_act(mx.bf16_to_f64(x))
+    wq_o, ws_o = bs.bs_quantize_weight(mx.bf16_to_f64(w))
+    assert_float_close(host_f64(out), bs.bs_gemm(oq, os_, wq_o, ws_o))
+    bad = torch.zeros((4, 96), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(api.MxgError):  # K % 128 != 0
+        api.bs_quantize_act(bad)

@@ -206,3 +206,27 @@ def test_kv_append_mxfp8_bit_exact_contiguous_and_paged():
             np.testing.assert_array_equal(arr[pg, :, r], want)
             arr[pg, :, r] = 0x7F if arr.shape[-1] == D else 0xFF
     assert all((a == (0x7F if a.shape[-1] == D else 0xFF)).all() for a in got)  # nothing else written
+
+
+def test_paged_bad_page_id_sets_the_flag_other_sequences_intact():
+    bs, Hq, Hkv, D, ps = 2, 8, 2, 128, 64
+    lens = np.array([150, 90], np.int32)
+    q, kp, vp = _case(bs, Hq, Hkv, D, lens, 13)
+    num_pages = 6
+    pools = [_filled((num_pages, Hkv, ps, D), 0x7F), _filled((num_pages, Hkv, ps, D // 32), 0xFF),
+             _filled((num_pages, Hkv, ps, D), 0x7F), _filled((num_pages, Hkv, ps, D // 32), 0xFF)]
+    table = np.array([[4, 0, 2, -1], [5, 1, -1, -1]], np.int32)
+    for b in range(bs):
+        kq, ksc = _gpu_rows_mx(kp[b])
+        vq, vsc = _gpu_rows_mx(vp[b])
+        for j in range((int(lens[b]) + ps - 1) // ps):
+            sl = slice(j * ps, min(int(lens[b]), (j + 1) * ps))
+            for pool, arr in zip(pools, (kq, ksc, vq, vsc)):
+                pool[int(table[b, j]), :, :sl.stop - sl.start].copy_(arr[:, sl])
+    table[1, 1] = num_pages + 3  # outside the pool
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = api.gqa_decode_attn_kv_mxfp8_paged(dev_bf16(q), *pools, dev(table), dev(lens), 256, 0.1, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 7
+    assert np.isfinite(host_f64(out)).all()
+    assert_attn_close(host_f64(out)[:1], _oracle(q[:1], kp[:1], vp[:1], 0.1))

@@ -153,3 +153,30 @@ def test_inconsistent_lengths_set_the_flag():
     assert int(err.item()) == 7
     assert not host_f64(out)[40:].any()  # the bad sequence was skipped
     _check(out[:40].contiguous(), q[:40], kp[:1], vp[:1], q_start[:2], 0.1)
+
+
+def test_paged_bad_page_id_sets_the_flag():
+    prefix, new, ps = [0, 0], [70, 130], 64
+    q, kp, vp, kn, vn, q_start, lens = _case(prefix, new, 32, 8, seed=8)
+    kpool, vpool = _garbage((8, 8, ps, D)), _garbage((8, 8, ps, D))
+    table = np.array([[3, 6, -1], [0, 5, 1]], np.int32)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.kv_append_extend_paged(kpool, vpool, dev(table), dev_bf16(kn), dev_bf16(vn), dev(q_start), dev(lens), 130,
+                               err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    table[1, 2] = 99  # outside the pool: sequence 1's last 64 keys
+    out = api.gqa_prefill_attn_paged(dev_bf16(q), kpool, vpool, dev(table), dev(q_start), dev(lens), 130, 0.09,
+                                     err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 7
+    assert np.isfinite(host_f64(out)).all()
+    _check(out[:70].contiguous(), q[:70], kp[:1], vp[:1], q_start[:2], 0.09)
+
+
+def test_host_checks():
+    q = torch.zeros((4, 8, 64), dtype=torch.bfloat16, device="cuda")
+    K = torch.zeros((1, 2, 64, 64), dtype=torch.bfloat16, device="cuda")
+    qs, kl = dev(np.array([0, 4], np.int32)), dev(np.array([4], np.int32))
+    with pytest.raises(api.MxgError):  # head dim 64: the tensor-core prefill needs 128
+        api.gqa_prefill_attn(q, K, K, qs, kl, 4, 0.1)
