@@ -6,6 +6,7 @@
 // new token i sits at position kv_len[b] - T_b + i and attends to positions 0 .. that position
 // (T_b = kv_len[b]: a prefill from scratch). Its query row is q[q_start[b] + i].
 //
+// Two kernels share this design; the launcher picks by prompt length (see launch_gqa_prefill_attn).
 // Design (tensor-bound: S = Q K^T and O = P V are dense 128 x 128 x 128 contractions):
 //  * CTA = 128 query rows of one (sequence b, kv head g): 128/G consecutive new tokens x the G
 //    query heads of the group (row r = token r/G, head g*G + r%G), so every K/V tile is read
@@ -446,6 +447,343 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_prefill_kernel(const __grid_c
   }
 }
 
+// ------------------------------------------------------------------------------------------
+// Ping-pong variant: two 128-row query tiles (A, B) per CTA share every K/V tile. P of a tile is
+// written in bf16 into TMEM over that tile's own S (the columns already read) and the PV MMA
+// takes it from tensor memory, so shared memory holds only Q_A, Q_B and the K/V ring. The MMA
+// thread issues S_A(0), S_B(0), then per key tile j: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1): while
+// one softmax warpgroup works on its tile, the tensor cores serve the other.
+constexpr int kPPThreads = 10 * 32;  // producer, MMA, softmax A (warps 2..5), softmax B (6..9)
+constexpr int kPPOffQ = 0;                        // Q_A, Q_B
+constexpr int kPPOffK = kPPOffQ + 2 * kTile;
+constexpr int kPPOffV = kPPOffK + kStages * kTile;
+constexpr int kPPOffBar = kPPOffV + kStages * kTile;
+// q full, k/v full, kv empty, s full[2], p full[2], o done[2], mma drained
+constexpr int kPPNumBars = 1 + 3 * kStages + 2 + 2 + 2 + 1;
+constexpr int kPPSmemBytes = 1024 + kPPOffBar + kPPNumBars * 8 + 16;
+
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+__global__ void __launch_bounds__(kPPThreads) gqa_prefill_pp_kernel(const __grid_constant__ CUtensorMap tmQ,
+                                                                      const __grid_constant__ CUtensorMap tmK,
+                                                                      const __grid_constant__ CUtensorMap tmV,
+                                                                      const PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPPOffBar);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* v_full = k_full + kStages;
+  uint64_t* kv_empty = v_full + kStages;
+  uint64_t* s_full = kv_empty + kStages;  // [tile]
+  uint64_t* p_full = s_full + 2;          // [tile]
+  uint64_t* o_done = p_full + 2;          // [tile]
+  uint64_t* drained = o_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kPPNumBars);
+
+  pdl_trigger();
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bg = blockIdx.y;
+  const int b = bg / p.Hkv, g = bg - b * p.Hkv;
+  const int G = p.group, tpt = kRows / G;  // tokens per 128-row tile
+  const int tile = (int)gridDim.x - 1 - (int)blockIdx.x;  // latest (heaviest) tiles first
+  const int qs = p.q_start[b];
+  const int T = p.q_start[b + 1] - qs;
+  const int n = p.kv_len[b];
+  if (T < 0 || T > p.max_q_len || T > n || (int64_t)n > p.cap || qs < 0 || (int64_t)qs + T > p.total_q) {
+    if (tile == 0 && g == 0 && threadIdx.x == 0) set_error(p.err, MXG_EDEVICE);
+    return;
+  }
+  const int tok0 = tile * 2 * tpt;  // tile A: tok0 .., tile B: tok0 + tpt ..
+  if (tok0 >= T) return;
+  const int P0 = n - T;
+  const int pos_hi = P0 + min(T, tok0 + 2 * tpt) - 1;
+  const int nk = pos_hi / kKeys + 1;
+  const int64_t row0 = ((int64_t)b * p.Hkv + g) * p.cap;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&p_full[x], 128);
+      mbar_init(&o_done[x], 1);
+    }
+    mbar_init(drained, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = *tmem_slot;  // S/P_A at 0, S/P_B at 128, O_A at 256, O_B at 384
+  bool ok = true;
+
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer (TMA)
+    if (lane == 0) {
+      prefetch_tensormap(&tmQ);
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+      mbar_arrive_expect_tx(q_full, 2 * kTile);
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        tma_load_3d(smem + kPPOffQ + x * kTile, &tmQ, q_full, 0, g * G, qs + tok0 + x * tpt);
+        tma_load_3d(smem + kPPOffQ + x * kTile + kBox, &tmQ, q_full, 64, g * G, qs + tok0 + x * tpt);
+      }
+      const int64_t past = p.table ? p.num_pages * p.Hkv * p.page_size : 0;
+      for (int j = 0; j < nk; ++j) {
+        const int s = j & 1;
+        if (j >= kStages && !mbar_wait(&kv_empty[s], ((j >> 1) - 1) & 1, p.err)) break;
+        int rows[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int key = j * kKeys + 64 * h;
+          if (!p.table) {
+            rows[h] = (int)(row0 + key);
+          } else if (key >= n) {
+            rows[h] = (int)past;  // nothing visible there: the copy engine reads zeros
+          } else {
+            const int page = p.table[(int64_t)b * p.max_pages + key / p.page_size];
+            if (page < 0 || page >= p.num_pages) {
+              set_error(p.err, MXG_EDEVICE);
+              rows[h] = (int)past;
+            } else {
+              rows[h] = (int)(((int64_t)page * p.Hkv + g) * p.page_size + key % p.page_size);
+            }
+          }
+        }
+        uint8_t* kt = smem + kPPOffK + s * kTile;
+        uint8_t* vt = smem + kPPOffV + s * kTile;
+        mbar_arrive_expect_tx(&k_full[s], kTile);
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) tma_load_2d(kt + c * kBox + h * (kBox / 2), &tmK, &k_full[s], 64 * c, rows[h]);
+        mbar_arrive_expect_tx(&v_full[s], kTile);
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) tma_load_2d(vt + c * kBox + h * (kBox / 2), &tmV, &v_full[s], 64 * c, rows[h]);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issue (one thread)
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16(kRows, kKeys, false);
+      constexpr uint32_t kIdPV = idesc_bf16(kRows, kHd, true);
+      const uint32_t qa = smem_u32(smem + kPPOffQ);
+      bool issued = false;
+      // S_x(j) = Q_x K_j^T into the S/P buffer of tile x
+      auto issue_s = [&](int x, int j) {
+        const uint32_t ka = smem_u32(smem + kPPOffK + (j & 1) * kTile);
+#pragma unroll
+        for (int ks = 0; ks < kHd / 16; ++ks)
+          mma_bf16_tc(tmem + x * kKeys, desc_kmajor(qa + x * kTile, ks), desc_kmajor(ka, ks), kIdS, ks > 0);
+        commit(&s_full[x]);
+        issued = true;
+      };
+      // O_x += P_x(j) V_j, P from tensor memory (16-key step ks = 8 columns of bf16 pairs)
+      auto issue_pv = [&](int x, int j) {
+        const uint32_t va = smem_u32(smem + kPPOffV + (j & 1) * kTile);
+#pragma unroll
+        for (int ks = 0; ks < kKeys / 16; ++ks)
+          mma_bf16_ts(tmem + kColO + x * kKeys, tmem + x * kKeys + 8 * ks, desc_v_mn(va, ks), kIdPV,
+                      (j > 0 || ks > 0) ? 1u : 0u);
+      };
+      ok = mbar_wait(q_full, 0, p.err) && mbar_wait(&k_full[0], 0, p.err);
+      if (ok) {
+        fence_after_sync();
+        issue_s(0, 0);
+        issue_s(1, 0);
+      }
+      for (int j = 0; j < nk && ok; ++j) {
+        const int s = j & 1;
+        const bool more = j + 1 < nk;
+        if (!mbar_wait(&p_full[0], j & 1, p.err) || !mbar_wait(&v_full[s], (j >> 1) & 1, p.err)) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+        issue_pv(0, j);
+        if (!more) {
+          commit(&o_done[0]);
+        } else {
+          if (!mbar_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, p.err)) {
+            ok = false;
+            break;
+          }
+          fence_after_sync();
+          issue_s(0, j + 1);
+        }
+        if (!mbar_wait(&p_full[1], j & 1, p.err)) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+        issue_pv(1, j);
+        commit(&kv_empty[s]);
+        if (!more) commit(&o_done[1]);
+        else issue_s(1, j + 1);
+      }
+      if (issued) {
+        // every MMA has finished before TMEM is released, also when a wait above ran out
+        commit(drained);
+        mbar_wait(drained, 0, p.err);
+      }
+    }
+  } else {
+    // ------------------------------------------------ softmax of tile x (thread = row = TMEM lane)
+    const int x = (warp - 2) >> 2;
+    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+    const int r = quad * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t sbuf = tmem + lane_off + x * kKeys;          // S, then P (bf16 pairs) of tile x
+    const uint32_t obuf = tmem + lane_off + kColO + x * kKeys;  // O of tile x
+    const int tl = r / G, hh = r - tl * G;
+    const int tok = tok0 + x * tpt + tl;
+    const bool valid = tok < T;
+    const int pos = valid ? P0 + tok : -1;  // rows past the sequence see no key
+    float m_ref = -INFINITY, l = 0.f;
+    for (int j = 0; j < nk; ++j) {
+      const int key0 = j * kKeys;
+      if (!warp_wait(&s_full[x], j & 1, p.err)) {
+        ok = false;
+        break;
+      }
+      fence_after_sync();
+      const int lim = pos - key0;  // columns <= lim are visible to this row
+      const bool masked = !__all_sync(MXG_FULL_MASK, lim >= kKeys - 1);
+      // pass 1: the scaled row maximum, base 2
+      float mp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32(sbuf + 32 * c, v);
+        wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float t = v[i] * p.scale_log2;
+          if (masked && 32 * c + i > lim) t = -INFINITY;
+          mp[i & 3] = fmaxf(mp[i & 3], t);
+        }
+      }
+      const float mx = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3]));
+      const float m_new = mx > m_ref + kRescaleLog2 ? mx : m_ref;
+      const bool moved = m_new != m_ref;
+      const float alpha = moved ? fast_exp2(m_ref - m_new) : 1.f;
+      const float mu = m_new == -INFINITY ? 0.f : m_new;
+      if (j >= 1 && __any_sync(MXG_FULL_MASK, moved)) {
+        // O holds tiles < j (PV_x(j-1) completed before S_x(j) was committed): rescale moved rows
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float o[32];
+          tmem_ld32(obuf + 32 * c, o);
+          wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(obuf + 32 * c, o);
+        }
+      }
+      bool zeroed = false;
+      if (x == 0 && key0 + kKeys > n) {
+        // V rows past kv_len may hold anything (P is 0 there): zero them for both tiles
+        if (!warp_wait(&v_full[j & 1], (j >> 1) & 1, p.err)) {
+          ok = false;
+          break;
+        }
+        if (key0 + r >= n) {
+          uint8_t* vt = smem + kPPOffV + (j & 1) * kTile + r * 128;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            *reinterpret_cast<uint4*>(vt + 16 * q) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(vt + kBox + 16 * q) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        zeroed = true;
+      }
+      // pass 2: P = 2^(s - mu) in bf16 pairs (column c: keys 2c, 2c+1) over S columns already read
+      float sp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32(sbuf + 32 * c, v);
+        wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float t0 = v[2 * i] * p.scale_log2, t1 = v[2 * i + 1] * p.scale_log2;
+          if (masked && 32 * c + 2 * i > lim) t0 = -INFINITY;
+          if (masked && 32 * c + 2 * i + 1 > lim) t1 = -INFINITY;
+          const float e0 = fast_exp2(t0 - mu), e1 = fast_exp2(t1 - mu);
+          sp[i & 3] += e0 + e1;
+          w[i] = pack_bf16x2(e0, e1);
+        }
+        tmem_st16(sbuf + 16 * c, w);
+      }
+      l = l * alpha + ((sp[0] + sp[1]) + (sp[2] + sp[3]));
+      m_ref = m_new;
+      tmem_wait_st();
+      if (zeroed) fence_proxy_async_smem();
+      fence_before_sync();
+      mbar_arrive(&p_full[x]);
+    }
+    if (ok && warp_wait(&o_done[x], 0, p.err)) {
+      fence_after_sync();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint16_t* orow = p.out + ((int64_t)(qs + (valid ? tok : 0)) * p.Hq + g * G + hh) * kHd;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float o[32];
+        tmem_ld32(obuf + 32 * c, o);
+        wait_ld();
+        if (valid) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 wv;
+            wv.x = pack_bf16x2(o[8 * q] * inv, o[8 * q + 1] * inv);
+            wv.y = pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv);
+            wv.z = pack_bf16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv);
+            wv.w = pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv);
+            *reinterpret_cast<uint4*>(orow + 32 * c + 8 * q) = wv;
+          }
+        }
+      }
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 // kv_append for a prefill / extend: token i of sequence b (row q_start[b] + i of k_new / v_new,
 // [total_q, Hkv, D] with ld_new elements between token rows) lands at position
 // kv_len[b] - T_b + i. One warp per (token, sequence); 16-byte moves.
@@ -514,6 +852,16 @@ cudaError_t launch_gqa_prefill_attn(const CUtensorMap& tmQ, const CUtensorMap& t
   p.page_size = pages ? pages->page_size : 0;
   p.num_pages = pages ? pages->num_pages : 0;
   const int tpt = kRows / p.group;
+  if (max_q_len * p.group <= 8 * kRows) {
+    // short prompts (at most 8 query tiles per head group): two tiles per CTA share each K/V tile
+    // and the per-CTA fixed costs (measured faster: 64 x 234 tokens 162 vs 187 us)
+    dim3 grid((unsigned)((max_q_len + 2 * tpt - 1) / (2 * tpt)), (unsigned)(bs * Hkv));
+    cudaError_t e =
+        cudaFuncSetAttribute(gqa_prefill_pp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPPSmemBytes);
+    if (e != cudaSuccess) return e;
+    return launch_k(gqa_prefill_pp_kernel, grid, dim3(kPPThreads), kPPSmemBytes, st, 1, tmQ, tmK, tmV, p);
+  }
+  // long prompts: one tile per CTA (measured faster: 4096 tokens 231 vs 309 us)
   dim3 grid((unsigned)((max_q_len + tpt - 1) / tpt), (unsigned)(bs * Hkv));
   cudaError_t e = cudaFuncSetAttribute(gqa_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
