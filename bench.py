@@ -7,7 +7,7 @@ retire/refill schedule) -> quantise -> O projection + residual -> RMSNorm+quanti
 MXFP8 SwiGLU MLP (Qwen3-4B shape 2560/9728) + residual -> prev_tokens_shift [64,16,10].
 
 metric/unit: HBM GB/s = algorithmic bytes of the step / step time (the step's KV reads,
-weights and activations; see the design doc for the per-kernel byte counts). The line also
+weights and activations, counted per kernel by the *_bytes functions below). The line also
 carries the MLP-only sweep (M = 1..128: us and GB/s), the attention-only sweep (bs = 1..64:
 GB/s), the paged-attention sweep (bs = 64, pages of 64/128/256), the MXFP8-KV attention sweep
 (bs = 1..64 and paged), the prefill / extend attention sweep (TFLOP/s), the block-scaled FP8

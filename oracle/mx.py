@@ -11,7 +11,7 @@ the OCP MX v1.0 specification:
 3. elements q_i = E4M3(v_i / 2^s), round to nearest even, values above the
    largest finite E4M3 (448) saturate to +-448 (never NaN).
 
-Readings where the spec leaves room (listed in the design doc):
+Readings where the spec leaves room:
 * all-zero block -> s = -127 (scale byte 0x00), elements 0x00 / 0x80 by sign;
 * the sign of zero is kept (-0 and negative values rounding to 0 give 0x80);
 * E4M3 subnormals are m * 2^-9, m = 1..7, reached by the same RNE rule;
