@@ -3,8 +3,9 @@
 Source: [S2.1] "FP8 Quantization Strategy" names bsgemm as 128x128 block-scaled FP8, and
 "What's Open Source" gives its granularity: 1x128 blocks for activations, 128x128 blocks for
 weights. The pages print no rule for the scale, so the plainest reading is taken: each block
-keeps one fp32 scale s = fp32(amax / 448), computed in fp32, and its elements are E4M3(fp32(v / s)) -- the fp32 quotient rounded once to E4M3, nearest-even,
-saturating at +-448; a block whose amax is 0 gets s = 0 and elements E4M3(v) (signed zeros).
+keeps one fp32 scale s = fp32(amax / 448), computed in fp32, and its elements are
+E4M3(fp32(v / s)) -- the fp32 quotient rounded once to E4M3, nearest-even, saturating at
++-448; a block whose amax is 0 gets s = 0 and elements E4M3(v) (signed zeros).
 The product is C[m][n] = sum over 128-wide K blocks kb of
 s_x[m][kb] * s_w[n // 128][kb] * sum_{k in kb} E4M3(xq[m][k]) * E4M3(wq[n][k]).
 """
