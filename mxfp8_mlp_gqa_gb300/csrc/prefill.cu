@@ -342,30 +342,43 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_prefill_kernel(const __grid_c
       wait_ld();
       fence_before_sync();
       mbar_arrive(&s_free[s]);
-      // causal mask (column c is key key0 + c) and the scaled row maximum, base 2
+      // causal mask (column c is key key0 + c), needed only on tiles that reach the diagonal
       const int lim = pos - key0;
-      float mx = -INFINITY;
+      if (!__all_sync(MXG_FULL_MASK, lim >= kKeys - 1)) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (32 * c + i > lim) x[c][i] = -INFINITY;
+      }
+      // row maximum over eight independent partials; the scale is positive (host-checked) and
+      // rounding is monotonic, so max(x) * scale is the maximum of the scaled products
+      float mp[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mp[k] = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float v = (32 * c + i <= lim) ? x[c][i] * p.scale_log2 : -INFINITY;
-          x[c][i] = v;
-          mx = fmaxf(mx, v);
-        }
+        for (int i = 0; i < 32; ++i) mp[i & 7] = fmaxf(mp[i & 7], x[c][i]);
+      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * p.scale_log2;
       const float m_new = mx > m_ref + kRescaleLog2 ? mx : m_ref;
       const bool moved = m_new != m_ref;
       const float alpha = moved ? fast_exp2(m_ref - m_new) : 1.f;
-      const float mu = m_new == -INFINITY ? 0.f : m_new;
-      float rs = 0.f;
+      const float nmu = m_new == -INFINITY ? 0.f : -m_new;
+      // p = 2^(x * scale - m) with one rounding in the exponent's argument; the row sum also
+      // runs over eight partials so that no 128-long chain of dependent adds forms
+      float sp[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) sp[k] = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          x[c][i] = fast_exp2(x[c][i] - mu);
-          rs += x[c][i];
+          x[c][i] = fast_exp2(fmaf(x[c][i], p.scale_log2, nmu));
+          sp[i & 7] += x[c][i];
         }
-      l = l * alpha + rs;
+      l = l * alpha + (((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7])));
       m_ref = m_new;
       // the P tile and O are free once the previous PV product has completed
       if (j >= 1 && !warp_wait(pv_done, (j - 1) & 1, p.err)) {
@@ -679,7 +692,8 @@ __global__ void __launch_bounds__(kPPThreads) gqa_prefill_pp_kernel(const __grid
       fence_after_sync();
       const int lim = pos - key0;  // columns <= lim are visible to this row
       const bool masked = !__all_sync(MXG_FULL_MASK, lim >= kKeys - 1);
-      // pass 1: the scaled row maximum, base 2
+      // pass 1: the row maximum of the raw products; the scale is positive (host-checked) and
+      // rounding is monotonic, so max(s) * scale is the maximum of the scaled products (base 2)
       float mp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -687,17 +701,13 @@ __global__ void __launch_bounds__(kPPThreads) gqa_prefill_pp_kernel(const __grid
         tmem_ld32(sbuf + 32 * c, v);
         wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float t = v[i] * p.scale_log2;
-          if (masked && 32 * c + i > lim) t = -INFINITY;
-          mp[i & 3] = fmaxf(mp[i & 3], t);
-        }
+        for (int i = 0; i < 32; ++i) mp[i & 3] = fmaxf(mp[i & 3], (masked && 32 * c + i > lim) ? -INFINITY : v[i]);
       }
-      const float mx = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3]));
+      const float mx = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])) * p.scale_log2;
       const float m_new = mx > m_ref + kRescaleLog2 ? mx : m_ref;
       const bool moved = m_new != m_ref;
       const float alpha = moved ? fast_exp2(m_ref - m_new) : 1.f;
-      const float mu = m_new == -INFINITY ? 0.f : m_new;
+      const float nmu = m_new == -INFINITY ? 0.f : -m_new;
       if (j >= 1 && __any_sync(MXG_FULL_MASK, moved)) {
         // O holds tiles < j (PV_x(j-1) completed before S_x(j) was committed): rescale moved rows
 #pragma unroll
@@ -727,7 +737,7 @@ __global__ void __launch_bounds__(kPPThreads) gqa_prefill_pp_kernel(const __grid
         }
         zeroed = true;
       }
-      // pass 2: P = 2^(s - mu) in bf16 pairs (column c: keys 2c, 2c+1) over S columns already read
+      // pass 2: P = 2^(s * scale - m) in bf16 pairs (column c: keys 2c, 2c+1) over S columns already read
       float sp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -737,10 +747,10 @@ __global__ void __launch_bounds__(kPPThreads) gqa_prefill_pp_kernel(const __grid
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          float t0 = v[2 * i] * p.scale_log2, t1 = v[2 * i + 1] * p.scale_log2;
+          float t0 = fmaf(v[2 * i], p.scale_log2, nmu), t1 = fmaf(v[2 * i + 1], p.scale_log2, nmu);
           if (masked && 32 * c + 2 * i > lim) t0 = -INFINITY;
           if (masked && 32 * c + 2 * i + 1 > lim) t1 = -INFINITY;
-          const float e0 = fast_exp2(t0 - mu), e1 = fast_exp2(t1 - mu);
+          const float e0 = fast_exp2(t0), e1 = fast_exp2(t1);
           sp[i & 3] += e0 + e1;
           w[i] = pack_bf16x2(e0, e1);
         }
