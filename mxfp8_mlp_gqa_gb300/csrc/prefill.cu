@@ -160,6 +160,32 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Packed fp32 pairs (sm_100 family): each lane rounds exactly as the scalar instruction does.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// max of three (exact, order-free)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) gqa_prefill_kernel(const __grid_constant__ CUtensorMap tmQ,
                                                                   const __grid_constant__ CUtensorMap tmK,
                                                                   const __grid_constant__ CUtensorMap tmV,
@@ -351,33 +377,40 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_prefill_kernel(const __grid_c
           for (int i = 0; i < 32; ++i)
             if (32 * c + i > lim) x[c][i] = -INFINITY;
       }
-      // row maximum over eight independent partials; the scale is positive (host-checked) and
-      // rounding is monotonic, so max(x) * scale is the maximum of the scaled products
+      // row maximum over eight independent partials (three-input max); the scale is positive
+      // (host-checked) and rounding is monotonic, so max(x) * scale is the maximum of the scaled
+      // products
       float mp[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mp[k] = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mp[i & 7] = fmaxf(mp[i & 7], x[c][i]);
-      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * p.scale_log2;
+        for (int i = 0; i < 32; i += 2) mp[(i >> 1) & 7] = fmax3(mp[(i >> 1) & 7], x[c][i], x[c][i + 1]);
+      const float mx = fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7])) *
+                       p.scale_log2;
       const float m_new = mx > m_ref + kRescaleLog2 ? mx : m_ref;
       const bool moved = m_new != m_ref;
       const float alpha = moved ? fast_exp2(m_ref - m_new) : 1.f;
       const float nmu = m_new == -INFINITY ? 0.f : -m_new;
-      // p = 2^(x * scale - m) with one rounding in the exponent's argument; the row sum also
-      // runs over eight partials so that no 128-long chain of dependent adds forms
-      float sp[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) sp[k] = 0.f;
+      // p = 2^(x * scale - m) with one rounding in the exponent's argument (packed pairs); the
+      // row sum runs over eight partials (four packed pairs: partial k holds the elements
+      // i = k mod 8) so that no 128-long chain of dependent adds forms
+      const uint64_t sc2 = pk2(p.scale_log2, p.scale_log2), nm2 = pk2(nmu, nmu);
+      uint64_t sp2[4] = {0, 0, 0, 0};
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          x[c][i] = fast_exp2(fmaf(x[c][i], p.scale_log2, nmu));
-          sp[i & 7] += x[c][i];
+        for (int i = 0; i < 32; i += 2) {
+          float t0, t1;
+          upk2(fma_f32x2(pk2(x[c][i], x[c][i + 1]), sc2, nm2), t0, t1);
+          x[c][i] = fast_exp2(t0);
+          x[c][i + 1] = fast_exp2(t1);
+          sp2[(i >> 1) & 3] = add_f32x2(sp2[(i >> 1) & 3], pk2(x[c][i], x[c][i + 1]));
         }
+      float sp[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) upk2(sp2[k], sp[2 * k], sp[2 * k + 1]);
       l = l * alpha + (((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7])));
       m_ref = m_new;
       // the P tile and O are free once the previous PV product has completed
@@ -701,7 +734,9 @@ __global__ void __launch_bounds__(kPPThreads) gqa_prefill_pp_kernel(const __grid
         tmem_ld32(sbuf + 32 * c, v);
         wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mp[i & 3] = fmaxf(mp[i & 3], (masked && 32 * c + i > lim) ? -INFINITY : v[i]);
+        for (int i = 0; i < 32; i += 2)
+          mp[(i >> 1) & 3] = fmax3(mp[(i >> 1) & 3], (masked && 32 * c + i > lim) ? -INFINITY : v[i],
+                                   (masked && 32 * c + i + 1 > lim) ? -INFINITY : v[i + 1]);
       }
       const float mx = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])) * p.scale_log2;
       const float m_new = mx > m_ref + kRescaleLog2 ? mx : m_ref;
@@ -738,7 +773,8 @@ __global__ void __launch_bounds__(kPPThreads) gqa_prefill_pp_kernel(const __grid
         zeroed = true;
       }
       // pass 2: P = 2^(s * scale - m) in bf16 pairs (column c: keys 2c, 2c+1) over S columns already read
-      float sp[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint64_t sc2 = pk2(p.scale_log2, p.scale_log2), nm2 = pk2(nmu, nmu);
+      uint64_t sp2[2] = {0, 0};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         float v[32];
@@ -747,15 +783,19 @@ __global__ void __launch_bounds__(kPPThreads) gqa_prefill_pp_kernel(const __grid
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          float t0 = fmaf(v[2 * i], p.scale_log2, nmu), t1 = fmaf(v[2 * i + 1], p.scale_log2, nmu);
+          float t0, t1;
+          upk2(fma_f32x2(pk2(v[2 * i], v[2 * i + 1]), sc2, nm2), t0, t1);
           if (masked && 32 * c + 2 * i > lim) t0 = -INFINITY;
           if (masked && 32 * c + 2 * i + 1 > lim) t1 = -INFINITY;
           const float e0 = fast_exp2(t0), e1 = fast_exp2(t1);
-          sp[i & 3] += e0 + e1;
+          sp2[i & 1] = add_f32x2(sp2[i & 1], pk2(e0, e1));
           w[i] = pack_bf16x2(e0, e1);
         }
         tmem_st16(sbuf + 16 * c, w);
       }
+      float sp[4];
+      upk2(sp2[0], sp[0], sp[1]);
+      upk2(sp2[1], sp[2], sp[3]);
       l = l * alpha + ((sp[0] + sp[1]) + (sp[2] + sp[3]));
       m_ref = m_new;
       tmem_wait_st();
