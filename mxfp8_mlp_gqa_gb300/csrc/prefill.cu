@@ -50,8 +50,8 @@ constexpr int kOffK = kOffQ + kTile;
 constexpr int kOffV = kOffK + kStages * kTile;
 constexpr int kOffP = kOffV + kStages * kTile;
 constexpr int kOffBar = kOffP + kTile;
-// q full, k/v full, kv empty, s full/free, p full, pv done, mma drained
-constexpr int kNumBars = 1 + 2 * kStages + kStages + 2 * 2 + 3;
+// q full, k/v full, k/v empty, s full/free, p full, pv done, mma drained
+constexpr int kNumBars = 1 + 4 * kStages + 2 * 2 + 3;
 constexpr int kSmemBytes = 1024 + kOffBar + kNumBars * 8 + 16;
 
 // TMEM columns: S buffers at 0 and 128, O at 256.
@@ -196,8 +196,9 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_prefill_kernel(const __grid_c
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
   uint64_t* v_full = k_full + kStages;
-  uint64_t* kv_empty = v_full + kStages;
-  uint64_t* s_full = kv_empty + kStages;
+  uint64_t* k_empty = v_full + kStages;  // K_j's stage is free once S_j has completed,
+  uint64_t* v_empty = k_empty + kStages;  // V_j's once PV_j has
+  uint64_t* s_full = v_empty + kStages;
   uint64_t* s_free = s_full + 2;
   uint64_t* p_full = s_free + 2;
   uint64_t* pv_done = p_full + 1;
@@ -230,7 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_prefill_kernel(const __grid_c
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_prefill_kernel(const __grid_c
       const int64_t past = p.table ? p.num_pages * p.Hkv * p.page_size : 0;
       for (int j = 0; j < nk && ok; ++j) {
         const int s = j & 1;
-        if (j >= kStages && !mbar_wait(&kv_empty[s], ((j >> 1) - 1) & 1, p.err)) {
+        if (j >= kStages && !mbar_wait(&k_empty[s], ((j >> 1) - 1) & 1, p.err)) {
           ok = false;
           break;
         }
@@ -292,6 +294,11 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_prefill_kernel(const __grid_c
         for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int h = 0; h < 2; ++h) tma_load_2d(kt + c * kBox + h * (kBox / 2), &tmK, &k_full[s], 64 * c, rows[h]);
+        // the K load above goes out a softmax period before this one: V_{j-2} is read later
+        if (j >= kStages && !mbar_wait(&v_empty[s], ((j >> 1) - 1) & 1, p.err)) {
+          ok = false;
+          break;
+        }
         mbar_arrive_expect_tx(&v_full[s], kTile);
 #pragma unroll
         for (int c = 0; c < 2; ++c)
@@ -321,6 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_prefill_kernel(const __grid_c
           for (int ks = 0; ks < kHd / 16; ++ks)
             mma_bf16_tc(tmem + s * kKeys, desc_kmajor(qa, ks), desc_kmajor(ka, ks), kIdS, ks > 0);
           commit(&s_full[s]);
+          commit(&k_empty[s]);
           issued = true;
         }
         if (j >= 1) {
@@ -335,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_prefill_kernel(const __grid_c
           for (int ks = 0; ks < kKeys / 16; ++ks)
             mma_bf16_tc(tmem + kColO, desc_kmajor(pa, ks), desc_v_mn(va, ks), kIdPV, (jj > 0 || ks > 0) ? 1u : 0u);
           commit(pv_done);
-          commit(&kv_empty[s2]);
+          commit(&v_empty[s2]);
         }
       }
       // every MMA this thread issued has finished before TMEM can be released
@@ -504,8 +512,8 @@ constexpr int kPPOffQ = 0;                        // Q_A, Q_B
 constexpr int kPPOffK = kPPOffQ + 2 * kTile;
 constexpr int kPPOffV = kPPOffK + kStages * kTile;
 constexpr int kPPOffBar = kPPOffV + kStages * kTile;
-// q full, k/v full, kv empty, s full[2], p full[2], o done[2], mma drained
-constexpr int kPPNumBars = 1 + 3 * kStages + 2 + 2 + 2 + 1;
+// q full, k/v full, k/v empty, s full[2], p full[2], o done[2], mma drained
+constexpr int kPPNumBars = 1 + 4 * kStages + 2 + 2 + 2 + 1;
 constexpr int kPPSmemBytes = 1024 + kPPOffBar + kPPNumBars * 8 + 16;
 
 __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
@@ -536,8 +544,9 @@ __global__ void __launch_bounds__(kPPThreads) gqa_prefill_pp_kernel(const __grid
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
   uint64_t* v_full = k_full + kStages;
-  uint64_t* kv_empty = v_full + kStages;
-  uint64_t* s_full = kv_empty + kStages;  // [tile]
+  uint64_t* k_empty = v_full + kStages;  // K_j's stage is free once both S products of tile j are,
+  uint64_t* v_empty = k_empty + kStages;  // V_j's once both PV products are
+  uint64_t* s_full = v_empty + kStages;   // [tile]
   uint64_t* p_full = s_full + 2;          // [tile]
   uint64_t* o_done = p_full + 2;          // [tile]
   uint64_t* drained = o_done + 2;
@@ -569,7 +578,8 @@ __global__ void __launch_bounds__(kPPThreads) gqa_prefill_pp_kernel(const __grid
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&s_full[x], 1);
@@ -605,7 +615,7 @@ __global__ void __launch_bounds__(kPPThreads) gqa_prefill_pp_kernel(const __grid
       const int64_t past = p.table ? p.num_pages * p.Hkv * p.page_size : 0;
       for (int j = 0; j < nk; ++j) {
         const int s = j & 1;
-        if (j >= kStages && !mbar_wait(&kv_empty[s], ((j >> 1) - 1) & 1, p.err)) break;
+        if (j >= kStages && !mbar_wait(&k_empty[s], ((j >> 1) - 1) & 1, p.err)) break;
         int rows[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -631,6 +641,7 @@ __global__ void __launch_bounds__(kPPThreads) gqa_prefill_pp_kernel(const __grid
         for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int h = 0; h < 2; ++h) tma_load_2d(kt + c * kBox + h * (kBox / 2), &tmK, &k_full[s], 64 * c, rows[h]);
+        if (j >= kStages && !mbar_wait(&v_empty[s], ((j >> 1) - 1) & 1, p.err)) break;
         mbar_arrive_expect_tx(&v_full[s], kTile);
 #pragma unroll
         for (int c = 0; c < 2; ++c)
@@ -667,6 +678,7 @@ __global__ void __launch_bounds__(kPPThreads) gqa_prefill_pp_kernel(const __grid
         fence_after_sync();
         issue_s(0, 0);
         issue_s(1, 0);
+        commit(&k_empty[0]);
       }
       for (int j = 0; j < nk && ok; ++j) {
         const int s = j & 1;
@@ -693,9 +705,13 @@ __global__ void __launch_bounds__(kPPThreads) gqa_prefill_pp_kernel(const __grid
         }
         fence_after_sync();
         issue_pv(1, j);
-        commit(&kv_empty[s]);
-        if (!more) commit(&o_done[1]);
-        else issue_s(1, j + 1);
+        commit(&v_empty[s]);
+        if (!more) {
+          commit(&o_done[1]);
+        } else {
+          issue_s(1, j + 1);
+          commit(&k_empty[(j + 1) & 1]);
+        }
       }
       if (issued) {
         // every MMA has finished before TMEM is released, also when a wait above ran out
