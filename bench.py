@@ -340,28 +340,28 @@ def run_ours(args, rank, local_rank, world):
         by = statistics.mean(b[n] for b in bytes_steps)
         breakdown[n] = {"us": round(ms * 1e3, 2), "GB_s": round(by / (ms * 1e-3) / 1e9, 1), "bytes": int(by)}
 
-    # e2e through the public API with host buffers: H2D of this step's inputs, the captured
-    # step, D2H of y, every step
-    x_h = torch.empty((BS, D_MODEL), dtype=torch.bfloat16, pin_memory=True)
+    # e2e through the public API with host buffers: every step one graph holding the copy of
+    # the step's packed inputs (x, next tokens, kv_len) from pinned host memory, the step and
+    # the copy of y back to pinned host memory; the host fills the input buffer between steps
+    h_in, (x_h, nxt_h, lens_h), y_h = L.host_io()
     x_h.copy_(L.x.cpu())
-    nxt_h = torch.empty((BS, CW), dtype=torch.int32, pin_memory=True)
     nxt_h.copy_(L.next_tokens.cpu())
-    lens_h = torch.from_numpy(sched).pin_memory()
-    y_h = torch.empty((BS, D_MODEL), dtype=torch.bfloat16, pin_memory=True)
+    L.capture_io(h_in, y_h)
+    for s in range(2):  # graph upload and first-launch costs stay out of the timing
+        lens_h.copy_(torch.from_numpy(sched[args.warmup + s]))
+        L.replay_io()
+    torch.cuda.synchronize()
     e_ms = []
     for i in range(args.steps):
+        lens_h.copy_(torch.from_numpy(sched[args.warmup + i]))
         flush.zero_()
         e0.record()
-        L.x.copy_(x_h, non_blocking=True)
-        L.next_tokens.copy_(nxt_h, non_blocking=True)
-        L.kv_len.copy_(lens_h[args.warmup + i], non_blocking=True)
-        plain.replay()
-        y_h.copy_(L.y, non_blocking=True)
+        L.replay_io()
         e1.record()
         e1.synchronize()
         e_ms.append(e0.elapsed_time(e1))
     e2e_ms = max_over_ranks(sum(e_ms), world, dev)
-    h2d = x_h.numel() * 2 + nxt_h.numel() * 4 + BS * 4
+    h2d = h_in.numel()
     d2h = y_h.numel() * 2
     e2e = {"value": round(world * tot_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / args.steps, 4)}

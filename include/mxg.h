@@ -376,6 +376,19 @@ mxg_status bs_gemm(const uint8_t* xq, const float* xs, const uint8_t* wq, const 
                    int64_t K, void* out, void* workspace, size_t ws_bytes, int32_t* err_flag, void* stream);
 
 /*
+ * copy_bytes -- dst <- src, n bytes, by a kernel on `stream` (16-byte moves). Plumbing for a
+ * decode step fed from the host (not an operation of the pages): either pointer may be
+ * page-locked host memory (cudaHostAlloc / cudaMallocHost / registered), which the kernel
+ * reads or writes through its device mapping, so a step's small host <-> device transfers run
+ * as kernels chained to the step's own (graph-capturable, no copy engine). Device and managed
+ * memory are used as they are. Ownership stays with the caller; the regions must not overlap.
+ * Errors: MXG_EINVAL for a null pointer, n < 0, or memory the device cannot address (pageable
+ * host memory is rejected on the host, never dereferenced); MXG_EALIGN unless both pointers
+ * are 16-byte aligned and n % 16 == 0. n == 0 launches nothing.
+ */
+mxg_status copy_bytes(void* dst, const void* src, int64_t n, void* stream);
+
+/*
  * prev_tokens_shift -- in-place slide of the Dual-AR previous-tokens window ([S2.1]
  * "DualAR: S2-Specific Batching Constraints": prev int32 [bs, W, cw], next_tokens int32
  * [bs, cw], strict shape/dtype contract). prev[b, w] <- prev[b, w+1] for w < W-1 and

@@ -48,6 +48,7 @@ _SIGS = {
                                                c_i64, c_f32, c_vp, c_vp, c_vp]),
     "kv_append": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_i64, c_vp, c_i64, c_i64, c_i64, c_i64, c_vp, c_vp]),
     "prev_tokens_shift": (ctypes.c_int, [c_vp, c_vp, c_i64, c_i64, c_i64, c_vp]),
+    "copy_bytes": (ctypes.c_int, [c_vp, c_vp, c_i64, c_vp]),
     "gqa_decode_attn_paged": (ctypes.c_int, [c_vp, c_i64, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_i64, c_i64,
                                              c_i64, c_i64, c_i64, c_f32, c_vp, c_vp, c_vp, c_sz, c_vp]),
     "kv_append_paged": (ctypes.c_int, [c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_i64, c_vp, c_i64, c_i64,
@@ -610,6 +611,23 @@ def kv_append(k_cache, v_cache, k_new, v_new, kv_len, err=None):
         _check(err, "err", torch.int32, (1,))
     _call("kv_append", _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), lds[0], _ptr(kv_len), bs, Hkv, D,
           cap, _ptr(err), _stream())
+
+
+def copy_bytes(dst, src):
+    """dst <- src (same byte size, contiguous, 16-byte aligned, size a multiple of 16) by a
+    kernel on the current stream; either side may be a pinned CPU tensor (mapped host memory)."""
+    for t, name in ((dst, "dst"), (src, "src")):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name}: expected a torch.Tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name}: must be contiguous")
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError(f"{name}: a CPU tensor must be pinned")
+    n = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != n:
+        raise ValueError("copy_bytes: dst and src differ in byte size")
+    _call("copy_bytes", _ptr(dst), _ptr(src), n, _stream())
+    return dst
 
 
 def prev_tokens_shift(prev, next_tokens):

@@ -547,6 +547,30 @@ mxg_status bs_gemm(const uint8_t* xq, const float* xs, const uint8_t* wq, const 
                                  (cudaStream_t)stream));
 }
 
+// The address a kernel may use for `p`: device or managed memory as it is, page-locked host
+// memory through its mapping into the device address space; nullptr for anything else
+// (pageable host memory is never handed to a kernel).
+static const void* device_view(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return p;
+  if (a.type == cudaMemoryTypeHost) return a.devicePointer;
+  return nullptr;
+}
+
+mxg_status copy_bytes(void* dst, const void* src, int64_t n, void* stream) {
+  if (!dst || !src || n < 0) return MXG_EINVAL;
+  if (n == 0) return MXG_OK;
+  if (n % 16 || !aligned16(dst) || !aligned16(src)) return MXG_EALIGN;
+  const void* s = device_view(src);
+  const void* d = device_view(dst);
+  if (!s || !d || !aligned16(s) || !aligned16(d)) return MXG_EINVAL;
+  return launched(launch_copy16(const_cast<void*>(d), s, n / 16, (cudaStream_t)stream));
+}
+
 mxg_status prev_tokens_shift(int32_t* prev, const int32_t* next_tokens, int64_t bs, int64_t W, int64_t cw,
                              void* stream) {
   if (!prev || !next_tokens) return MXG_EINVAL;

@@ -14,6 +14,7 @@ cudaError_t launch_rmsnorm_mxfp8_quantize(const uint16_t* x, const uint16_t* gam
 
 cudaError_t launch_prev_tokens_shift(int32_t* prev, const int32_t* next, int64_t bs, int64_t W, int64_t cw,
                                      cudaStream_t st);
+cudaError_t launch_copy16(void* dst, const void* src, int64_t n16, cudaStream_t st);
 struct KvPages;
 cudaError_t launch_kv_append(uint16_t* kc, uint16_t* vc, const uint16_t* kn, const uint16_t* vn, int64_t ld_new,
                              const int32_t* kv_len, int64_t bs, int64_t Hkv, int64_t D, int64_t cap, int32_t* err,

@@ -24,6 +24,25 @@ __global__ void __launch_bounds__(256) prev_tokens_shift_kernel(int32_t* __restr
   for (int i = threadIdx.x; i < n; i += blockDim.x) p[i] = i < keep ? win[i + cw] : nx[i - keep];
 }
 
+// Byte copy by a kernel in 16-byte moves. Either side may be page-locked host memory mapped
+// into the device address space (the host entry point resolves the mapping), so a step's small
+// host <-> device transfers cost a kernel that PDL chains to its neighbours instead of a
+// copy-engine operation with its own start-up latency.
+__global__ void __launch_bounds__(256) copy16_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src,
+                                                     int64_t n16) {
+  pdl_trigger();
+  pdl_wait();
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x)
+    dst[i] = src[i];
+}
+
+cudaError_t launch_copy16(void* dst, const void* src, int64_t n16, cudaStream_t st) {
+  int64_t blocks = (n16 + 255) / 256;
+  if (blocks > 4 * 152) blocks = 4 * 152;
+  return launch_k(copy16_kernel, dim3((unsigned)blocks), dim3(256), 0, st, 1, static_cast<uint4*>(dst),
+                  static_cast<const uint4*>(src), n16);
+}
+
 // [FSKV] §5 (kv_cache.update, in place): K/V rows of this step land at position kv_len-1.
 // One warp per (sequence, kv head); each lane moves 16 bytes of K and of V. With a page table
 // the row is looked up as in the paged attention (a bad page id sets the error flag, no write).

@@ -14,7 +14,10 @@ residual stream; RoPE and QK-norm are not on the pages and are left out.
 
 All buffers have stable addresses, so ``capture()`` records the step in a CUDA graph and
 ``replay()`` re-launches it; ``kv_len`` / ``next_tokens`` / ``x`` are updated in place
-between replays.
+between replays. The three per-step inputs are views of one packed device buffer
+(``inputs``), so a caller feeding the layer from the host moves them in one copy:
+``host_io()`` returns pinned host buffers of the same layout and ``capture_io()`` records
+that copy, the step and the copy of ``y`` back to the host as one graph.
 """
 from __future__ import annotations
 
@@ -35,11 +38,13 @@ class DecodeLayer:
         nqkv = (Hq + 2 * Hkv) * D
         self.nqkv = nqkv
         e = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)  # noqa: E731
-        # caller-visible state / inputs
-        self.x = e((bs, d_model), bf)
-        self.kv_len = e((bs,), i32)
+        # caller-visible state; the per-step inputs x, next_tokens, kv_len are views of one
+        # packed byte buffer (16-byte aligned sections) so that one copy brings them in
+        self.bs, self.cw = bs, cw
+        self.in_offsets, nbytes = self._input_layout(bs, d_model, cw)
+        self.inputs = torch.zeros((nbytes,), dtype=u8, device=dev)
+        self.x, self.next_tokens, self.kv_len = self._input_views(self.inputs)
         self.prev = e((bs, W, cw), i32)
-        self.next_tokens = e((bs, cw), i32)
         self.k_cache = e((bs, Hkv, cap, D), bf)
         self.v_cache = e((bs, Hkv, cap, D), bf)
         self.err = torch.zeros((1,), dtype=i32, device=dev)
@@ -64,7 +69,33 @@ class DecodeLayer:
         self.ws_qkv = torch.zeros((max(1, nqkv_ws),), dtype=u8, device=dev)
         self.ws_o = torch.zeros((max(1, api.mxfp8_gemm_workspace(bs, d_model, Hq * D)),), dtype=u8, device=dev)
         self.graph = None
+        self.graph_io = None
         self.side = torch.cuda.Stream(device=dev)
+
+    @staticmethod
+    def _input_layout(bs, d_model, cw):
+        """Byte offsets of x (bf16 [bs, d_model]), next_tokens (int32 [bs, cw]) and kv_len
+        (int32 [bs]) in the packed input buffer, each section 16-byte aligned, and its size."""
+        r16 = lambda n: (n + 15) // 16 * 16  # noqa: E731
+        o_x = 0
+        o_next = o_x + r16(bs * d_model * 2)
+        o_len = o_next + r16(bs * cw * 4)
+        return (o_x, o_next, o_len), o_len + r16(bs * 4)
+
+    def _input_views(self, buf):
+        o_x, o_next, o_len = self.in_offsets
+        bs, d_model, cw = self.bs, self.d_model, self.cw
+        x = buf[o_x:o_x + bs * d_model * 2].view(torch.bfloat16).view(bs, d_model)
+        nxt = buf[o_next:o_next + bs * cw * 4].view(torch.int32).view(bs, cw)
+        lens = buf[o_len:o_len + bs * 4].view(torch.int32)
+        return x, nxt, lens
+
+    def host_io(self):
+        """Pinned host buffers for feeding the layer from the host: (packed input bytes, its x /
+        next_tokens / kv_len views, y). Fill the views, then ``replay_io()``."""
+        h_in = torch.zeros((self.inputs.numel(),), dtype=torch.uint8, pin_memory=True)
+        h_y = torch.empty((self.bs, self.d_model), dtype=torch.bfloat16, pin_memory=True)
+        return h_in, self._input_views(h_in), h_y
 
     def load_weights(self, wqkv_bf16, wo_bf16, w13_bf16, w2_bf16, gamma1, gamma2):
         """bf16 weights on the device -> MXFP8 once (weight prep, not part of a step)."""
@@ -106,3 +137,32 @@ class DecodeLayer:
     def replay(self):
         self.graph.replay()
         return self.y
+
+    def capture_io(self, h_in, h_y, kernel_copy=True):
+        """Record [packed inputs host -> device, one step, y device -> host] in one CUDA graph
+        (h_in / h_y pinned, as from ``host_io()``). kernel_copy: move the bytes with the
+        library's copy kernel through the host memory's device mapping (chained to the step's
+        kernels); False: copy-engine copies."""
+        if not (h_in.is_pinned() and h_y.is_pinned()) or h_in.numel() != self.inputs.numel():
+            raise ValueError("capture_io needs the pinned buffers of host_io()")
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.graph_io = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.graph_io, stream=s):
+                if kernel_copy:
+                    api.copy_bytes(self.inputs, h_in)
+                else:
+                    self.inputs.copy_(h_in, non_blocking=True)
+                self.step()
+                if kernel_copy:
+                    api.copy_bytes(h_y, self.y)
+                else:
+                    h_y.copy_(self.y, non_blocking=True)
+        torch.cuda.current_stream().wait_stream(s)
+        return self.graph_io
+
+    def replay_io(self):
+        """One step fed from and returning to the host buffers given to ``capture_io`` (the
+        caller synchronises before reading y)."""
+        self.graph_io.replay()

@@ -115,3 +115,63 @@ def test_graph_replay_matches_eager():
         assert torch.equal(y.view(torch.int16), outs[s].view(torch.int16)), s
     torch.cuda.synchronize()
     assert int(L.err.item()) == 0
+
+
+def test_copy_bytes_host_and_device():
+    from mxfp8_mlp_gqa_gb300 import api
+    n = 4096 * 16 + 48
+    src_h = torch.from_numpy(np.random.default_rng(0).integers(0, 256, n, dtype=np.uint8)).pin_memory()
+    d = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    api.copy_bytes(d, src_h)                      # host -> device
+    back = torch.zeros(n, dtype=torch.uint8).pin_memory()
+    d2 = torch.empty_like(d)
+    api.copy_bytes(d2, d)                         # device -> device
+    api.copy_bytes(back, d2)                      # device -> host
+    torch.cuda.synchronize()
+    assert torch.equal(back, src_h)
+    pageable = torch.zeros(n, dtype=torch.uint8)
+    with pytest.raises(ValueError):               # the binding refuses unpinned CPU tensors
+        api.copy_bytes(d, pageable)
+    # so does the C entry point (checked on the host, nothing launched): MXG_EINVAL
+    import ctypes
+    st = api.lib().copy_bytes(ctypes.c_void_p(d.data_ptr()), ctypes.c_void_p(pageable.data_ptr()), n,
+                              ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 1
+    with pytest.raises(api.MxgError):             # size not a multiple of 16
+        api.copy_bytes(d[:40], d2[:40])
+
+
+@pytest.mark.parametrize("kernel_copy", [True, False])
+def test_host_io_graph_matches_device_graph(kernel_copy):
+    # one graph holding the packed input copy from pinned host memory, the step and the copy
+    # of y back: the same y and caches as the device-resident graph fed the same inputs
+    bs, cap = 8, 4096
+    L, _ = _layer(bs, cap, 1100, d=256, dff=768)
+    lens = synth.kv_lens(bs, 234, 1000, seed=2)
+    x, _, _, _, nxt = _fill(L, lens, 2)
+    kc0, vc0, prev0 = L.k_cache.clone(), L.v_cache.clone(), L.prev.clone()
+    L.capture()
+    ref = []
+    for s in range(3):
+        L.kv_len.copy_(dev((lens + s).astype(np.int32)))
+        ref.append(L.replay().clone())
+    kc1, vc1, prev1 = L.k_cache.clone(), L.v_cache.clone(), L.prev.clone()
+    L.k_cache.copy_(kc0)
+    L.v_cache.copy_(vc0)
+    L.prev.copy_(prev0)
+    h_in, (hx, hnext, hlen), h_y = L.host_io()
+    assert L.inputs.data_ptr() % 16 == 0 and all(t.data_ptr() % 16 == 0 for t in (L.x, L.next_tokens, L.kv_len))
+    L.x.zero_()  # the host copy must bring every input in
+    L.next_tokens.zero_()
+    hx.view(torch.int16).copy_(torch.from_numpy(x.view(np.int16)))
+    hnext.copy_(torch.from_numpy(nxt))
+    L.capture_io(h_in, h_y, kernel_copy=kernel_copy)
+    for s in range(3):
+        hlen.copy_(torch.from_numpy((lens + s).astype(np.int32)))
+        L.replay_io()
+        torch.cuda.synchronize()
+        assert torch.equal(h_y.view(torch.int16), ref[s].cpu().view(torch.int16)), s
+    assert torch.equal(L.k_cache.view(torch.int16), kc1.view(torch.int16))
+    assert torch.equal(L.v_cache.view(torch.int16), vc1.view(torch.int16))
+    assert torch.equal(L.prev, prev1)
+    assert int(L.err.item()) == 0
