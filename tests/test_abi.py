@@ -86,3 +86,25 @@ def test_attention_and_cache_reject_bad_shapes(lib):
     assert lib.prev_tokens_shift(FAKE, FAKE, 1, 0, 10, None) == 2
     assert lib.prev_tokens_shift(FAKE, FAKE, 1, 2000, 10, None) == 2                       # W*cw > 12288
     assert lib.prev_tokens_shift(None, FAKE, 1, 8, 10, None) == 1
+
+
+def test_copy_bytes_host_checks(lib):
+    # rejected on the host before anything is launched: null pointers, negative or ragged sizes
+    st = ctypes.c_void_p(0)
+    assert lib.copy_bytes(None, ctypes.c_void_p(16), 16, st) == 1         # MXG_EINVAL
+    assert lib.copy_bytes(ctypes.c_void_p(16), ctypes.c_void_p(16), -16, st) == 1
+    assert lib.copy_bytes(ctypes.c_void_p(16), ctypes.c_void_p(16), 0, st) == 0   # nothing to do
+    assert lib.copy_bytes(ctypes.c_void_p(16), ctypes.c_void_p(16), 24, st) == 3  # MXG_EALIGN: 24 % 16
+    assert lib.copy_bytes(ctypes.c_void_p(8), ctypes.c_void_p(16), 32, st) == 3   # unaligned dst
+
+
+def test_decode_layer_input_layout():
+    # x, next_tokens and kv_len share one packed buffer: sections in order, 16-byte aligned,
+    # non-overlapping, and the bench shape's total is the bytes the host copies in per step
+    from mxfp8_mlp_gqa_gb300.step import DecodeLayer
+    for bs, d, cw in ((64, 2560, 10), (1, 256, 10), (3, 72, 7)):
+        (o_x, o_n, o_l), total = DecodeLayer._input_layout(bs, d, cw)
+        assert o_x == 0 and o_n >= bs * d * 2 and o_l >= o_n + bs * cw * 4 and total >= o_l + bs * 4
+        assert o_n % 16 == 0 and o_l % 16 == 0 and total % 16 == 0
+        assert total - (o_l + bs * 4) < 16
+    assert DecodeLayer._input_layout(64, 2560, 10)[1] == 330496
