@@ -742,6 +742,14 @@ def run_profile(args):
         c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         wsb = torch.zeros(max(1, api.mxfp8_gemm_workspace(M, N, K_)), dtype=torch.uint8, device=dev)
         fn = lambda: api.mxfp8_gemm(aq, as_, bq, bs_, c=c, workspace=wsb)  # noqa: E731
+    elif kind == "bsgemm":
+        # block-scaled FP8 GEMM (1x128 activation / 128x128 weight blocks, fp32 scales)
+        M, N, K_ = (int(v) for v in arg.split("x"))
+        xq, xs = api.bs_quantize_act(rn((M, K_)))
+        wq, ws_ = api.bs_quantize_weight(rn((N, K_), 0.02))
+        c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        wsb = torch.zeros(max(1, api.bs_gemm_workspace(M, N, K_)), dtype=torch.uint8, device=dev)
+        fn = lambda: api.bs_gemm(xq, xs, wq, ws_, out=c, workspace=wsb)  # noqa: E731
     elif kind == "cublas":
         # context only: cuBLAS's MXFP8 GEMM (torch._scaled_mm, UE8M0 block scales of 2^0) on
         # the same shape, for a side-by-side capture of a library kernel
