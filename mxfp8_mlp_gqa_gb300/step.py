@@ -143,7 +143,9 @@ class DecodeLayer:
         (h_in / h_y pinned, as from ``host_io()``). kernel_copy: move the bytes with the
         library's copy kernel through the host memory's device mapping (chained to the step's
         kernels); False: copy-engine copies."""
-        if not (h_in.is_pinned() and h_y.is_pinned()) or h_in.numel() != self.inputs.numel():
+        if (not (h_in.is_pinned() and h_y.is_pinned()) or h_in.dtype != torch.uint8 or
+                h_in.numel() != self.inputs.numel() or h_y.dtype != self.y.dtype or h_y.shape != self.y.shape or
+                not (h_in.is_contiguous() and h_y.is_contiguous())):
             raise ValueError("capture_io needs the pinned buffers of host_io()")
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
