@@ -40,7 +40,7 @@ class DecodeLayer:
         e = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)  # noqa: E731
         # caller-visible state; the per-step inputs x, next_tokens, kv_len are views of one
         # packed byte buffer (16-byte aligned sections) so that one copy brings them in
-        self.bs, self.cw = bs, cw
+        self.cw = cw
         self.in_offsets, nbytes = self._input_layout(bs, d_model, cw)
         self.inputs = torch.zeros((nbytes,), dtype=u8, device=dev)
         self.x, self.next_tokens, self.kv_len = self._input_views(self.inputs)
@@ -65,8 +65,6 @@ class DecodeLayer:
         self.y = e((bs, d_model), bf)
         self.ws_attn = e((max(1, api.gqa_decode_attn_workspace(bs, Hq, Hkv, D, max_kv_len)),), u8)
         self.ws_mlp = torch.zeros((api.mlp_swiglu_mxfp8_workspace(bs, d_model, d_ff),), dtype=u8, device=dev)
-        nqkv_ws = api.mxfp8_gemm_workspace(bs, nqkv, d_model)
-        self.ws_qkv = torch.zeros((max(1, nqkv_ws),), dtype=u8, device=dev)
         self.ws_o = torch.zeros((max(1, api.mxfp8_gemm_workspace(bs, d_model, Hq * D)),), dtype=u8, device=dev)
         self.graph = None
         self.graph_io = None
