@@ -206,11 +206,14 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
   const int ntiles = (t1 - t0 + kTileTok - 1) / kTileTok;
   const int row0 = (int)((int64_t)bg * p.cap + t0);  // host guarantees bs*Hkv*cap < 2^31 (contiguous)
 
+  // set by a consumer warp whose wait ran out; read by all consumers after the merge barrier
+  __shared__ volatile int merge_abort;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumers);
     }
+    merge_abort = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -330,7 +333,10 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
   bool ok = true;
   for (int i = 0; i < ntiles; ++i) {
     const int s = i % S::kStages;
-    if (!mbar_wait(&full[s], (i / S::kStages) & 1, p.err)) { ok = false; break; }
+    if (!__all_sync(MXG_FULL_MASK, mbar_wait(&full[s], (i / S::kStages) & 1, p.err))) {
+      ok = false;
+      break;
+    }
     const uint32_t kbase = smem_u32(ring + s * S::kCodeStageBytes);
     const uint32_t vbase = kbase + S::kTileBytes;
     const uint32_t ksbase = smem_u32(ring + S::kScaleRingOff + s * 2 * S::kScaleTileBytes);
@@ -510,7 +516,10 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
   }
-  if (!ok) return;
+  // A warp whose wait ran out still meets the other consumer warps at the named barrier below
+  // (leaving would hold them there for good): it publishes the failure before the barrier, and
+  // all consumer warps leave together after it.
+  if (!ok) merge_abort = 1;
 
   // l partial sums: reduce over the 8 lanes that share a head pair
 #pragma unroll
@@ -521,6 +530,7 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
   // merge the consumer warps through shared memory (the ring is idle now: every issued tile
   // was consumed before the named barrier below)
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+  if (merge_abort) return;
   float* os = reinterpret_cast<float*>(ring);                 // [warp][8 heads][D]
   float* ml = os + kConsumers * 8 * D;                         // [warp][8 heads][m, l]
   const float oscale = kMx ? 0x1p64f : 1.f;                    // MXFP8 V: O carried 2^-64
