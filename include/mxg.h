@@ -28,9 +28,12 @@
  *   - Launch failures return MXG_ELAUNCH.
  *   - Alignment: every pointer 16-byte aligned; ld values multiples of 8 (bf16) / 16 (bytes).
  *   - Kernels are chained with programmatic dependent launch: a GEMM / MLP call starts copying
- *     its WEIGHT operand (bq/bs of mxfp8_gemm, the W13/W2/Wqkv codes and scales) before the
- *     previous kernel on the stream has finished, so a weight must not be written by the
- *     kernel that immediately precedes the call on that stream (prepare weights at setup).
+ *     its WEIGHT operand (bq/bs of mxfp8_gemm, the W13/W2/Wqkv codes and scales, the RMSNorm
+ *     gain) before the previous kernel on the stream has finished, so a weight must not be
+ *     written by the kernel that immediately precedes the call on that stream (prepare
+ *     weights at setup). Every kernel of the library lets its successor start only after
+ *     its own predecessor has completed, so at most two library kernels of a stream are in
+ *     flight at once and everything before the immediately preceding kernel is complete.
  *     Activations and outputs are touched only after the previous kernel completes.
  *     Environment variable MXG_PDL=0 turns the chaining off.
  */
@@ -66,6 +69,15 @@ int mxg_version(void);
  * (K % 128 == 0); enable == 0 forces the CUDA-core kernels. Process-wide, not thread-safe;
  * returns the previous setting. */
 int mxg_set_tensor_core_path(int enable);
+/* Failure-detection test hook. on != 0: until it is called again with 0, the split-KV decode
+ * attention kernels (every gqa_decode_attn* entry point) issue no K/V loads, so their
+ * consumer warps wait on pipeline stages that nothing fills; each such wait gives up after
+ * its bound (2 s), the kernel records MXG_ETIMEOUT in err_flag, writes zeros for the heads it
+ * owns and returns -- the device-side wind-down path, exercised without a fault and with no
+ * copy in flight. The setting lives in device memory of the current device and is written
+ * synchronously (all prior work on the legacy default stream completes first). Returns
+ * MXG_OK or MXG_ELAUNCH. Not for production use. */
+mxg_status mxg_debug_stall_attn_loads(int on);
 
 /*
  * mxfp8_quantize -- fused activation quantisation + UE8M0 scale pack in one launch

@@ -28,6 +28,7 @@ _SIGS = {
     "mxg_status_str": (ctypes.c_char_p, [ctypes.c_int]),
     "mxg_version": (ctypes.c_int, []),
     "mxg_set_tensor_core_path": (ctypes.c_int, [ctypes.c_int]),
+    "mxg_debug_stall_attn_loads": (ctypes.c_int, [ctypes.c_int]),
     "mxfp8_quantize": (ctypes.c_int, [c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_vp]),
     "rmsnorm_mxfp8_quantize": (ctypes.c_int, [c_vp, c_vp, c_f32, c_i64, c_i64, c_i64, c_vp, c_vp, c_vp]),
     "mxfp8_gemm_workspace": (c_sz, [c_i64, c_i64, c_i64]),
@@ -572,11 +573,12 @@ def bs_gemm(xq, xs, wq, ws, out=None, workspace=None, err=None):
     return out
 
 
-def gqa_decode_attn_noalloc(q, k_cache, v_cache, kv_len, max_kv_len, scale, out):
+def gqa_decode_attn_noalloc(q, k_cache, v_cache, kv_len, max_kv_len, scale, out, err=None):
     """gqa_decode_attn without a workspace: for callers that cannot allocate device memory
     (inside CUDA-graph capture, real-time threads, hosts that own the memory budget). Its
     split-KV scratch is the library's fixed device array (gqa_decode_attn_noalloc_capacity()
-    bytes, shared by all calls); `out` must be passed in, so nothing is allocated here."""
+    bytes, shared by all calls); `out` (and the optional int32 [1] device error flag `err`)
+    must be passed in, so nothing is allocated here."""
     _check(k_cache, "k_cache", torch.bfloat16, ndim=4)
     bs, Hkv, cap, D = k_cache.shape
     _check(v_cache, "v_cache", torch.bfloat16, (bs, Hkv, cap, D))
@@ -585,8 +587,10 @@ def gqa_decode_attn_noalloc(q, k_cache, v_cache, kv_len, max_kv_len, scale, out)
     Hq = q.shape[1]
     _check(q, "q", torch.bfloat16, (bs, Hq, D))
     _check(out, "out", torch.bfloat16, (bs, Hq, D))
+    if err is not None:
+        _check(err, "err", torch.int32, (1,))
     _call("gqa_decode_attn_noalloc", _ptr(q), Hq * D, _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), bs, Hq, Hkv, D,
-          cap, int(max_kv_len), float(scale), _ptr(out), None, _stream())
+          cap, int(max_kv_len), float(scale), _ptr(out), _ptr(err), _stream())
     return out
 
 

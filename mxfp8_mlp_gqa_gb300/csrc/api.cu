@@ -89,6 +89,8 @@ int mxg_set_tensor_core_path(int enable) {
   return prev;
 }
 
+mxg_status mxg_debug_stall_attn_loads(int on) { return launched(set_attn_load_stall(on)); }
+
 mxg_status mxfp8_quantize(const void* x, int64_t M, int64_t K, int64_t ld_x, uint8_t* q, uint8_t* s, void* stream) {
   if (M < 0 || K <= 0 || K % 32 || ld_x < K) return MXG_ESHAPE;
   if (M == 0) return MXG_OK;  // nothing to read or write (empty tensors may carry null pointers)
@@ -322,6 +324,22 @@ mxg_status check_pages(const int32_t* table, int64_t max_pages, int64_t page_siz
 }
 
 }  // namespace
+
+}  // extern "C"
+
+namespace mxg {
+// The checks, tensor maps and launch of gqa_decode_attn, for other entry points of the library
+// that supply the workspace themselves.
+mxg_status decode_attn_call(const void* q, int64_t ld_q, const void* k_cache, const void* v_cache,
+                            const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t cap,
+                            int64_t max_kv_len, float scale, void* out, int32_t* err_flag, void* workspace,
+                            size_t ws_bytes, void* stream) {
+  return attn_call(q, ld_q, k_cache, v_cache, kv_len, bs, Hq, Hkv, D, cap, max_kv_len, scale, out, nullptr, nullptr,
+                   err_flag, workspace, ws_bytes, stream);
+}
+}  // namespace mxg
+
+extern "C" {
 
 mxg_status gqa_decode_attn(const void* q, int64_t ld_q, const void* k_cache, const void* v_cache,
                            const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t cap,

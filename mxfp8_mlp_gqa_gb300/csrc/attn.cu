@@ -150,6 +150,12 @@ struct SplitParams {
   int64_t num_pages;
 };
 
+// Failure-detection test hook (mxg_debug_stall_attn_loads): while it is nonzero the copy warp
+// of the split kernel issues no loads, so the consumer warps wait on stages that nothing will
+// fill; their bounded waits run out and the kernel winds down with MXG_ETIMEOUT. No copy is
+// in flight when the CTA leaves, and nothing faults.
+__device__ int g_stall_attn_loads = 0;
+
 }  // namespace
 
 // One CTA = one (split, b, g). tmK/tmV map the K/V rows (bf16 [rows, D], or E4M3 codes
@@ -179,8 +185,8 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBodyBytes + S::kPBytes);
   uint64_t* empty = full + S::kStages;
 
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int split = blockIdx.x;
   const int bg = blockIdx.y;
   const int b = bg / p.Hkv, g = bg - b * p.Hkv;
@@ -247,7 +253,8 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
         prefetch_tensormap(&tmVS);
       }
       const uint64_t pol = l2_policy_evict_first();
-      for (int i = 0; i < ntiles; ++i) {
+      const int nissue = *reinterpret_cast<volatile int*>(&g_stall_attn_loads) ? 0 : ntiles;
+      for (int i = 0; i < nissue; ++i) {
         const int s = i % S::kStages;
         if (i >= S::kStages && !mbar_wait(&empty[s], ((i / S::kStages) - 1) & 1, p.err)) break;
         const int row = p.table ? tile_row[i] : row0 + i * kTileTok;
@@ -530,7 +537,25 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
   // merge the consumer warps through shared memory (the ring is idle now: every issued tile
   // was consumed before the named barrier below)
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
-  if (merge_abort) return;
+  if (merge_abort) {
+    // the error flag holds MXG_ETIMEOUT; leave nothing stale behind: zeros for a single
+    // split, otherwise a split of weight zero (lse = -inf), which the combine pass skips
+    for (int idx = threadIdx.x; idx < p.group * D; idx += kConsumers * 32) {
+      const int h = idx / D, d = idx - h * D;
+      const int64_t bh = (int64_t)b * p.Hq + h0 + h;
+      if (p.max_splits == 1) {
+        p.out[bh * D + d] = 0;
+        if (p.oq) {
+          p.oq[bh * D + d] = 0;
+          if ((d & 31) == 0) p.os[(bh * D + d) >> 5] = 0;
+        }
+      } else {
+        p.o_part[(bh * p.max_splits + split) * D + d] = 0.f;
+        if (d == 0) p.lse[bh * p.max_splits + split] = -INFINITY;
+      }
+    }
+    return;
+  }
   float* os = reinterpret_cast<float*>(ring);                 // [warp][8 heads][D]
   float* ml = os + kConsumers * 8 * D;                         // [warp][8 heads][m, l]
   const float oscale = kMx ? 0x1p64f : 1.f;                    // MXFP8 V: O carried 2^-64
@@ -584,8 +609,8 @@ __global__ void __launch_bounds__(D) gqa_combine_kernel(const float* __restrict_
                                                         int chunk, int max_splits, int max_kv_len,
                                                         uint16_t* __restrict__ out, uint8_t* __restrict__ oq,
                                                         uint8_t* __restrict__ os) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int64_t bh = blockIdx.x;
   const int b = (int)(bh / Hq);
   const int d = threadIdx.x;
@@ -603,17 +628,26 @@ __global__ void __launch_bounds__(D) gqa_combine_kernel(const float* __restrict_
   float M = -INFINITY;
   for (int i = 0; i < ns; ++i) M = fmaxf(M, l[i]);
   float W = 0.f, acc = 0.f;
-  for (int i = 0; i < ns; ++i) {
-    const float w = exp2f(l[i] - M);
-    W += w;
-    acc += w * o_part[(bh * max_splits + i) * D + d];
+  // a split that gave up on a bounded wait left lse = -inf (weight 0); if every split did,
+  // the output is zero (the error flag says why)
+  if (M != -INFINITY) {
+    for (int i = 0; i < ns; ++i) {
+      const float w = exp2f(l[i] - M);
+      W += w;
+      acc += w * o_part[(bh * max_splits + i) * D + d];
+    }
   }
-  const __nv_bfloat16 ob = __float2bfloat16_rn(acc / W);
+  const __nv_bfloat16 ob = __float2bfloat16_rn(M == -INFINITY ? 0.f : acc / W);
   out[bh * D + d] = __bfloat16_as_ushort(ob);
   if (oq) mx_quant_warp_store(__bfloat162float(ob), oq + bh * D + d, os + ((bh * D + d) >> 5));
 }
 
 // ---------------------------------------------------------------------------------- host
+cudaError_t set_attn_load_stall(int on) {
+  const int v = on ? 1 : 0;
+  return cudaMemcpyToSymbol(g_stall_attn_loads, &v, sizeof(v));
+}
+
 int attn_chunk(int64_t bs, int64_t Hkv, int64_t max_kv_len) {
   // aim for ~3000 (b, g, split) work items at the bound, 64..1024 tokens per split
   int64_t c = (bs * Hkv * max_kv_len + 2999) / 3000;

@@ -49,8 +49,6 @@ cudaError_t scratch_for_current_device(void** out) {
   return cudaSuccess;
 }
 
-inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
 
 }  // namespace mxg
@@ -64,28 +62,13 @@ size_t gqa_decode_attn_noalloc_capacity(void) { return kNoAllocScratchBytes; }
 mxg_status gqa_decode_attn_noalloc(const void* q, int64_t ld_q, const void* k_cache, const void* v_cache,
                                    const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t cap,
                                    int64_t max_kv_len, float scale, void* out, int32_t* err_flag, void* stream) {
-  if (!q || !k_cache || !v_cache || !kv_len || !out) return MXG_EINVAL;
-  if (!(scale > 0.f) || !(scale < 1e30f)) return MXG_EINVAL;
-  if (bs < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || Hq / Hkv > 8 || (D != 64 && D != 128) || cap <= 0 ||
-      max_kv_len <= 0 || ld_q < Hq * D)
-    return MXG_ESHAPE;
-  if (bs * Hkv * cap >= ((int64_t)1 << 31) || bs * Hkv > 65535 || max_kv_len > ((int64_t)1 << 30)) return MXG_ESHAPE;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || ld_q % 8) return MXG_EALIGN;
-  if (bs == 0) return MXG_OK;
-  if (attn_workspace_bytes(bs, Hq, Hkv, D, max_kv_len) > kNoAllocScratchBytes) return MXG_ESCRATCH;
   void* scratch = nullptr;
   if (scratch_for_current_device(&scratch) != cudaSuccess) return MXG_ELAUNCH;
-  CUtensorMap tk, tv;
-  const uint64_t rows = (uint64_t)(bs * Hkv * cap);
-  if (!make_tensor_map_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_cache, (uint64_t)D, rows, (uint64_t)D * 2, 64, 64,
-                          CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tensor_map_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v_cache, (uint64_t)D, rows, (uint64_t)D * 2, 64, 64,
-                          CU_TENSOR_MAP_SWIZZLE_128B))
-    return MXG_ENOTSUP;
-  const cudaError_t e = launch_gqa_decode_attn(tk, tv, static_cast<const uint16_t*>(q), ld_q, kv_len, bs, Hq, Hkv, D,
-                                               cap, max_kv_len, scale, static_cast<uint16_t*>(out), err_flag, scratch,
-                                               (cudaStream_t)stream);
-  return e == cudaSuccess ? MXG_OK : MXG_ELAUNCH;
+  // the same checks and launch as gqa_decode_attn, with the fixed array as the workspace; a
+  // problem whose partials do not fit in it is refused before anything is enqueued
+  const mxg_status st = decode_attn_call(q, ld_q, k_cache, v_cache, kv_len, bs, Hq, Hkv, D, cap, max_kv_len, scale,
+                                         out, err_flag, scratch, kNoAllocScratchBytes, stream);
+  return st == MXG_EWORKSPACE ? MXG_ESCRATCH : st;
 }
 
 }  // extern "C"

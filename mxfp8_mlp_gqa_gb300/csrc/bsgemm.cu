@@ -77,8 +77,8 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
 __global__ void __launch_bounds__(256) bs_quantize_act_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
                                                               int64_t ld_x, uint8_t* __restrict__ q,
                                                               float* __restrict__ s) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t nb = K / kGK;
@@ -101,8 +101,8 @@ __global__ void __launch_bounds__(256) bs_quantize_act_kernel(const uint16_t* __
 __global__ void __launch_bounds__(256) bs_quantize_weight_kernel(const uint16_t* __restrict__ w, int64_t N, int64_t K,
                                                                  uint8_t* __restrict__ q, float* __restrict__ s) {
   __shared__ float red[8];
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int64_t kb = blockIdx.x, nb = blockIdx.y;
   const int64_t row = nb * 128 + (threadIdx.x >> 1);
   const int64_t col = kb * kGK + 64 * (threadIdx.x & 1);
@@ -190,7 +190,6 @@ __global__ void __launch_bounds__(192, 1) bs_gemm_kernel(const __grid_constant__
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = *tmem_sh;
-  pdl_trigger();
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer (TMA)
@@ -207,6 +206,7 @@ __global__ void __launch_bounds__(192, 1) bs_gemm_kernel(const __grid_constant__
         tma_load_2d(st + 64 * kGK, &tmW, &full[i], (g0 + i) * kGK, n0 + 64);
       }
       pdl_wait();
+      pdl_trigger();
       for (int i = 0; i < ng; ++i) {
         const int s = i % S::kStages;
         if (i >= S::kStages && !mbar_wait(&empty[s], ((i / S::kStages) - 1) & 1, a.err)) break;
@@ -306,8 +306,8 @@ __global__ void __launch_bounds__(192, 1) bs_gemm_kernel(const __grid_constant__
 // out[m][n] = bf16(sum_z part[z][m][n]), z in order.
 __global__ void __launch_bounds__(256) bs_reduce_kernel(const float* __restrict__ part, int splits, int64_t MN,
                                                         uint16_t* __restrict__ out) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < MN; i += (int64_t)gridDim.x * blockDim.x) {
     float y = 0.f;
     for (int z = 0; z < splits; ++z) y += part[(int64_t)z * MN + i];

@@ -50,8 +50,8 @@ __global__ void __launch_bounds__(256) mx_gemm_simt_kernel(const uint8_t* __rest
                                                            uint8_t* __restrict__ hq, uint8_t* __restrict__ hs) {
   __shared__ float As[kBK][kBM + 4];
   __shared__ float Bs[kBK][kBN + 4];
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int tid = threadIdx.x;
   const int m0 = blockIdx.y * kBM;
   const int n0 = blockIdx.x * kBN;

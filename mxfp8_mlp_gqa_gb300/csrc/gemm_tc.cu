@@ -92,8 +92,8 @@ struct TcArgs {
 // k-blocks of group g of row rt*128 + (w >> 2) + 32 * (w & 3); rows past `rows` are zero.
 __global__ void __launch_bounds__(256) pack_scales_kernel(const uint8_t* __restrict__ s, int64_t rows, int64_t KB,
                                                           int rt_pad, int groups, uint32_t* __restrict__ out) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int64_t total = (int64_t)groups * rt_pad * 128;
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
@@ -196,7 +196,6 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
   const uint32_t tmem = *tmem_sh;
   const uint32_t t_d = tmem;
 
-  pdl_trigger();
   if (warp == 0) {
     // ----------------------------------------------------------------- producer
     if (lane == 0) {
@@ -217,6 +216,8 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
       }
     }
     pdl_wait();
+    // the next kernel may start its own weight prefetch only once the previous one is complete
+    pdl_trigger();
     for (int i = 0; i < ng; ++i) {
       const int s = i % S::kStages;
       if (i >= S::kStages && !mbar_wait(&empty[s], ((i / S::kStages) - 1) & 1, a.err)) break;
@@ -289,7 +290,8 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
     const int q = warp & 3;  // the TMEM lane quadrant this warp may read
     const int r = 32 * q + lane;
     pdl_wait();  // outputs and the residual are touched only after the previous kernel is done
-    const bool ok = mbar_wait(tmem_full, 0, a.err);
+    // warp-uniform outcome: the SwiGLU epilogue below shuffles with the full mask
+    const bool ok = __all_sync(MXG_FULL_MASK, mbar_wait(tmem_full, 0, a.err));
     tc::fence_after_sync();
     const uint32_t trow = t_d + ((uint32_t)(32 * q) << 16);
     if (EPI == kEpiStore) {
@@ -502,7 +504,6 @@ __global__ void __launch_bounds__(192) mx_gemm_tc2_kernel(const __grid_constant_
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_sh;
 
-  pdl_trigger();
   if (warp == 0) {
     // ----------------------------------------------------------------- producer (both CTAs)
     if (lane == 0) {
@@ -520,6 +521,7 @@ __global__ void __launch_bounds__(192) mx_gemm_tc2_kernel(const __grid_constant_
         tma_load_2d_pair(st, &tmW, fb, i * kKG, n0);  // the weight map's box is 128 rows here
       }
       pdl_wait();
+      pdl_trigger();
       int i = 0;
       for (; i < ng; ++i) {
         const int s = i % S::kStages;

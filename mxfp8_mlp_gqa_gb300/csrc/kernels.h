@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "mxg.h"
+
 namespace mxg {
 
 cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t M, int64_t K, int64_t ld_x, uint8_t* q, uint8_t* s,
@@ -33,6 +35,15 @@ cudaError_t launch_gqa_decode_attn(const CUtensorMap& tmK, const CUtensorMap& tm
                                    int64_t max_kv_len, float scale, uint16_t* out, int32_t* err, void* ws,
                                    cudaStream_t st, uint8_t* oq = nullptr, uint8_t* os = nullptr,
                                    const KvPages* pages = nullptr);
+// Test hook: on != 0 makes the split-KV decode kernel's copy warp issue no loads (its waits
+// then run out: MXG_ETIMEOUT). Synchronous copy to a device variable of the current device.
+cudaError_t set_attn_load_stall(int on);
+// gqa_decode_attn's host checks, tensor maps and launch (api.cu), for entry points that
+// provide the workspace themselves (gqa_decode_attn_noalloc).
+mxg_status decode_attn_call(const void* q, int64_t ld_q, const void* k_cache, const void* v_cache,
+                            const int32_t* kv_len, int64_t bs, int64_t Hq, int64_t Hkv, int64_t D, int64_t cap,
+                            int64_t max_kv_len, float scale, void* out, int32_t* err_flag, void* workspace,
+                            size_t ws_bytes, void* stream);
 // MXFP8 K/V: tmK/tmV map E4M3 codes [rows, D]; tmKS/tmVS the UE8M0 scales [rows, D/32] as
 // 16-byte lines [rows * D/32 / 16, 16].
 cudaError_t launch_gqa_decode_attn_kv_mx(const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmKS,

@@ -1,12 +1,14 @@
 // Kernel launch helper: programmatic dependent launch (PDL) and optional thread-block clusters.
 //
-// Every kernel of the library starts with pdl_trigger() / pdl_wait() (common.cuh): with the
-// programmatic-stream-serialization attribute a kernel may be scheduled while its predecessor
-// on the stream is still draining; it runs its prologue (barrier setup, TMEM allocation, the
-// first weight TMA loads, which read no data produced upstream) and then waits in
-// griddepcontrol.wait until the predecessor has completed and its writes are visible.
-// Without the attribute both instructions are no-ops. MXG_PDL=0 in the environment turns the
-// attribute off (plain stream order).
+// Every kernel of the library executes pdl_wait() and then pdl_trigger() (common.cuh): with
+// the programmatic-stream-serialization attribute a kernel may be scheduled while its
+// predecessor on the stream is still draining; it runs its prologue (barrier setup, TMEM
+// allocation, the first weight TMA loads, which read no data produced upstream) and then
+// waits in griddepcontrol.wait until the predecessor has completed and its writes are
+// visible. Only after that wait does it let its own successor be scheduled, so a kernel's
+// pre-wait reads overlap its immediate predecessor alone: every earlier kernel of the chain
+// has completed by then. Without the attribute both instructions are no-ops. MXG_PDL=0 in
+// the environment turns the attribute off (plain stream order).
 #pragma once
 #include <cuda_runtime.h>
 #include <stdlib.h>

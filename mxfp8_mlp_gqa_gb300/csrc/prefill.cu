@@ -205,8 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_prefill_kernel(const __grid_c
   uint64_t* drained = pv_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
 
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bg = blockIdx.y;
   const int b = bg / p.Hkv, g = bg - b * p.Hkv;
@@ -552,8 +552,8 @@ __global__ void __launch_bounds__(kPPThreads) gqa_prefill_pp_kernel(const __grid
   uint64_t* drained = o_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kPPNumBars);
 
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bg = blockIdx.y;
   const int b = bg / p.Hkv, g = bg - b * p.Hkv;
@@ -860,8 +860,8 @@ __global__ void __launch_bounds__(256) kv_append_extend_kernel(uint16_t* __restr
                                                                const int32_t* __restrict__ kv_len, int Hkv, int D,
                                                                int64_t cap, int64_t total_q, int max_q_len,
                                                                int32_t* err, KvPages pg) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.y;
   const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;

@@ -41,8 +41,8 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& w, float (&v)[8]) {
 __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
                                                              int64_t ld_x, uint8_t* __restrict__ q,
                                                              uint8_t* __restrict__ s) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int64_t cpr = K >> 3;  // 8-element chunks per row (a multiple of 4)
   const int64_t total = M * cpr;
   const int64_t step = (int64_t)gridDim.x * blockDim.x;
@@ -92,7 +92,6 @@ __global__ void __launch_bounds__(kRmsThreads) rmsnorm_mxfp8_quantize_kernel(con
                                                                              float eps, int64_t K, int64_t ld_x,
                                                                              uint8_t* __restrict__ q,
                                                                              uint8_t* __restrict__ s) {
-  pdl_trigger();
   const int64_t row = blockIdx.x;
   const uint16_t* xr = x + row * ld_x;
   const int cpr = (int)(K >> 3);
@@ -104,6 +103,7 @@ __global__ void __launch_bounds__(kRmsThreads) rmsnorm_mxfp8_quantize_kernel(con
     gw[i] = c < cpr ? __ldg(reinterpret_cast<const uint4*>(gamma + ((int64_t)c << 3))) : make_uint4(0, 0, 0, 0);
   }
   pdl_wait();
+  pdl_trigger();
   uint4 xw[kRmsChunks];
 #pragma unroll
   for (int i = 0; i < kRmsChunks; ++i) {

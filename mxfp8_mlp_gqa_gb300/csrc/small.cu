@@ -13,8 +13,8 @@ namespace mxg {
 __global__ void __launch_bounds__(256) prev_tokens_shift_kernel(int32_t* __restrict__ prev,
                                                                 const int32_t* __restrict__ next, int W, int cw) {
   extern __shared__ int32_t win[];
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int n = W * cw;
   int32_t* p = prev + (int64_t)blockIdx.x * n;
   const int32_t* nx = next + (int64_t)blockIdx.x * cw;
@@ -30,8 +30,8 @@ __global__ void __launch_bounds__(256) prev_tokens_shift_kernel(int32_t* __restr
 // copy-engine operation with its own start-up latency.
 __global__ void __launch_bounds__(256) copy16_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src,
                                                      int64_t n16) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x)
     dst[i] = src[i];
 }
@@ -51,8 +51,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint16_t* __restrict__ k
                                                         const uint16_t* __restrict__ vn, int64_t ld_new,
                                                         const int32_t* __restrict__ kv_len, int bs, int Hkv, int D,
                                                         int64_t cap, int32_t* err, KvPages pg) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int gw = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (gw >= bs * Hkv) return;
@@ -93,8 +93,8 @@ __global__ void __launch_bounds__(256) kv_append_mx_kernel(uint8_t* __restrict__
                                                            const uint16_t* __restrict__ vn, int64_t ld_new,
                                                            const int32_t* __restrict__ kv_len, int bs, int Hkv, int D,
                                                            int64_t cap, int32_t* err, KvPages pg) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int gw = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (gw >= bs * Hkv) return;

@@ -1,7 +1,8 @@
 """The fused entry points of the decoder-layer step against the unfused calls they replace:
 gqa_decode_attn_mxfp8 == gqa_decode_attn + mxfp8_quantize (bit-exact), and
 mxfp8_gemm_qkv_kv_append == mxfp8_gemm + kv_append (bit-exact), including the error path
-of an out-of-range kv_len."""
+of an out-of-range kv_len; and the programmatic-dependent-launch chain of a weight quantiser
+followed by a GEMM that reads the weight."""
 import math
 
 import numpy as np
@@ -9,7 +10,8 @@ import pytest
 import torch
 
 from mxfp8_mlp_gqa_gb300 import api, synth
-from tests.gpu_util import dev, dev_bf16
+from oracle import mx, ops
+from tests.gpu_util import assert_float_close, dev, dev_bf16, host_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -58,3 +60,29 @@ def test_qkv_projection_with_fused_kv_append_is_bit_exact():
     api.mxfp8_gemm_qkv_kv_append(xq, xs, wq, ws, Hq, Hkv, kc3, vc, dev(bad), err=err)
     assert int(err.item()) == 7
     assert torch.equal(kc3[5].view(torch.int16), kc[5].view(torch.int16))
+
+
+def test_back_to_back_weight_quantise_then_gemm():
+    """mxfp8_quantize(W); mxfp8_quantize(x); mxfp8_gemm(x, W) enqueued with nothing in between:
+    the GEMM may start copying W before its immediate predecessor (the x quantiser) has
+    finished, but never before the W quantiser two launches back has completed. W's buffers
+    first hold the codes of another matrix, so a read that came too early would show."""
+    M, N, K = 16, 19456, 2560
+    w_old = dev_bf16(synth.weights(N, K, 1, synth.TID["w13"], 0.5))
+    w_new = synth.weights(N, K, 0, synth.TID["w13"])
+    x = synth.activations(M, K, 0, outlier_frac=0.01)
+    wq = torch.empty((N, K), dtype=torch.uint8, device="cuda")
+    ws = torch.empty((N, K // 32), dtype=torch.uint8, device="cuda")
+    xq = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+    xs = torch.empty((M, K // 32), dtype=torch.uint8, device="cuda")
+    c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    w_dev, x_dev = dev_bf16(w_new), dev_bf16(x)
+    ref = ops.mx_gemm(*mx.mx_quantize(mx.bf16_to_f64(x)), *mx.mx_quantize(mx.bf16_to_f64(w_new)))
+    for _ in range(3):
+        api.mxfp8_quantize(w_old, q=wq, s=ws)
+        torch.cuda.synchronize()
+        api.mxfp8_quantize(w_dev, q=wq, s=ws)
+        api.mxfp8_quantize(x_dev, q=xq, s=xs)
+        api.mxfp8_gemm(xq, xs, wq, ws, c=c)
+        torch.cuda.synchronize()
+        assert_float_close(host_f64(c), ref)

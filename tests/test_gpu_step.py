@@ -10,7 +10,7 @@ import torch
 from mxfp8_mlp_gqa_gb300 import synth
 from mxfp8_mlp_gqa_gb300.step import DecodeLayer
 from oracle import mx, ops
-from tests.gpu_util import assert_float_close, dev, dev_bf16, host_bits, host_f64
+from tests.gpu_util import assert_attn_close, assert_float_close, dev, dev_bf16, host_bits, host_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -55,6 +55,72 @@ def _q(w):
     return mx.mx_quantize(mx.bf16_to_f64(w))
 
 
+def _appended_rows(L, lens):
+    """The K and V rows this step wrote at position kv_len-1 (bf16 bits [bs, Hkv, D])."""
+    idx_b = torch.arange(L.bs, device="cuda")
+    idx_t = torch.from_numpy(np.asarray(lens) - 1).long().cuda()
+    return host_bits(L.k_cache[idx_b, :, idx_t]), host_bits(L.v_cache[idx_b, :, idx_t])
+
+
+def _check_step(L, w, wq, x, kp, vp, lens, prev, nxt, eps=1e-6):
+    """One step of the layer against the oracle. The chain is broken at every intermediate the
+    kernels store: each stage is fed the GPU's own input and held to the bound of that stage
+    (bit-exact quantisation, attention max |err| <= 2e-3, GEMM / MLP relative Frobenius error
+    <= 1e-2 and max |err| <= 3e-2 * rms). The end-to-end oracle step is checked as well, with
+    the looser bound that the accumulated roundings allow. Returns the appended K/V rows."""
+    bs, Hq, Hkv, D = L.bs, L.Hq, L.Hkv, L.D
+    qd = Hq * D
+    scale = 1 / math.sqrt(D)
+    ref = ops.decode_layer_step(x, w["g1"], w["g2"], wq["wqkv"], wq["wo"], wq["w13"], wq["w2"], kp, vp, lens, prev,
+                                nxt, Hq, Hkv, D, eps, scale)
+    np.testing.assert_array_equal(L.prev.cpu().numpy(), ref["prev"])
+    # stage 1: RMSNorm + MX quantise of this step's x (bit-exact), QKV projection on those codes
+    xq, xs = ops.rmsnorm_mx_quantize(x, w["g1"], eps)
+    np.testing.assert_array_equal(L.xq.cpu().numpy(), xq)
+    np.testing.assert_array_equal(L.xs.cpu().numpy(), xs)
+    qkv_ref = mx.bf16_to_f64(ref["qkv"])
+    assert_float_close(host_f64(L.qkv)[:, :qd], qkv_ref[:, :qd])
+    # stage 2: the appended rows are the projection's k / v columns, at position kv_len-1
+    kn, vn = _appended_rows(L, lens)
+    assert_float_close(np.concatenate([mx.bf16_to_f64(kn).reshape(bs, -1), mx.bf16_to_f64(vn).reshape(bs, -1)], 1),
+                       qkv_ref[:, qd:])
+    # stage 3: attention over the cache as the GPU holds it (prefix + appended row) with the
+    # GPU's q
+    q_g = host_f64(L.qkv)[:, :qd].reshape(bs, Hq, D)
+    kfull = [np.concatenate([mx.bf16_to_f64(kp[b]), mx.bf16_to_f64(kn[b])[:, None, :]], axis=1) for b in range(bs)]
+    vfull = [np.concatenate([mx.bf16_to_f64(vp[b]), mx.bf16_to_f64(vn[b])[:, None, :]], axis=1) for b in range(bs)]
+    assert_attn_close(host_f64(L.o), ops.gqa_decode_attention(q_g, kfull, vfull, scale))
+    # stage 4: MX quantisation of the GPU's o (bit-exact)
+    oq, os_ = mx.mx_quantize(host_f64(L.o).reshape(bs, qd))
+    np.testing.assert_array_equal(L.oq.cpu().numpy(), oq)
+    np.testing.assert_array_equal(L.os.cpu().numpy(), os_)
+    # stage 5: O projection on the GPU's codes + residual x
+    x1_ref = mx.bf16_to_f64(x) + ops.mx_gemm(oq, os_, *wq["wo"])
+    x1 = host_f64(L.x1)
+    assert_float_close(x1, x1_ref)
+    # stage 6: RMSNorm + MX quantise of the GPU's x1 (bit-exact: both sides take the rounding
+    # decisions at the same precision)
+    hq_in, hs_in = ops.rmsnorm_mx_quantize(host_bits(L.x1), w["g2"], eps)
+    np.testing.assert_array_equal(L.hq_in.cpu().numpy(), hq_in)
+    np.testing.assert_array_equal(L.hs_in.cpu().numpy(), hs_in)
+    # stage 7: the MLP on the GPU's input codes, residual the GPU's x1 -- the north star's bound
+    mlp = ops.swiglu_mlp(hq_in, hs_in, *wq["w13"], *wq["w2"], residual_bf16=host_bits(L.x1))
+    assert_float_close(host_f64(L.y), mlp["y"])
+    # end to end against the oracle's own chain: o differs in the last bf16 bit where fp32 and
+    # fp64 accumulation round differently, which moves a few MX codes downstream, so o and y
+    # are held to 0.1 * rms here (each stage alone meets its own bound above)
+    assert_float_close(host_f64(L.o).reshape(bs, -1), mx.bf16_to_f64(ref["o"]), max_rel_rms=0.1)
+    assert_float_close(x1, mx.bf16_to_f64(ref["x1"]))
+    oq_e2e, _ = ops.rmsnorm_mx_quantize(ref["x1"], w["g2"], eps)
+    assert np.mean(L.hq_in.cpu().numpy() != oq_e2e) <= 1e-3
+    assert_float_close(host_f64(L.y), ref["y"], max_rel_rms=0.1)
+    return kn, vn
+
+
+def _wq(w):
+    return {k: _q(w[k]) for k in ("wqkv", "wo", "w13", "w2")}
+
+
 def test_decode_layer_step_bs64():
     bs, cap = 64, 32768
     L, w = _layer(bs, cap, 4097)
@@ -64,33 +130,51 @@ def test_decode_layer_step_bs64():
     L.step()
     torch.cuda.synchronize()
     assert int(L.err.item()) == 0
-    ref = ops.decode_layer_step(x, w["g1"], w["g2"], _q(w["wqkv"]), _q(w["wo"]), _q(w["w13"]), _q(w["w2"]), kp, vp,
-                                lens, prev, nxt, 32, 8, 128, 1e-6, 1 / math.sqrt(128))
-    np.testing.assert_array_equal(L.prev.cpu().numpy(), ref["prev"])
-    # q columns of the projection (K/V columns go straight into the caches)
-    assert_float_close(host_f64(L.qkv)[:, :4096], mx.bf16_to_f64(ref["qkv"])[:, :4096])
-    # o is downstream of the projection's bf16 roundings, which differ from the oracle's on
-    # near-ties, so it is checked as an intermediate (the attention bound itself is tested on
-    # identical inputs in test_gpu_attn)
-    assert_float_close(host_f64(L.o).reshape(bs, -1), mx.bf16_to_f64(ref["o"]), max_rel_rms=0.1)
-    assert_float_close(host_f64(L.x1), mx.bf16_to_f64(ref["x1"]))
-    # the MLP's input codes: x1 differs from the oracle's in the last bf16 bit where the fp32
-    # and fp64 accumulations round differently, so a few codes differ -- held to the same
-    # <= 0.1 % allowance as the down projection's input (near zero a sign change of x1 can
-    # move a code by several subnormal steps, so the distance is not bounded here)
-    oq, os_ = ops.rmsnorm_mx_quantize(ref["x1"], w["g2"], 1e-6)
-    assert np.mean(L.hq_in.cpu().numpy() != oq) <= 1e-3
-    assert np.mean(L.hs_in.cpu().numpy() != os_) <= 1e-3
-    # y: the MLP bound on the relative Frobenius error; the elementwise bound is widened to
-    # 0.1 * rms because one flipped input code moves every output of its token (the MLP alone,
-    # on identical inputs, meets 3e-2 * rms in test_gpu_mlp)
-    assert_float_close(host_f64(L.y), ref["y"], max_rel_rms=0.1)
-    # the appended cache rows are this step's projected K/V
-    idx_b = torch.arange(bs, device="cuda")
-    idx_t = torch.from_numpy(lens - 1).long().cuda()
-    kv_new = np.concatenate([host_f64(L.k_cache[idx_b, :, idx_t]).reshape(bs, -1),
-                             host_f64(L.v_cache[idx_b, :, idx_t]).reshape(bs, -1)], axis=1)
-    assert_float_close(kv_new, mx.bf16_to_f64(ref["qkv"])[:, 4096:])
+    _check_step(L, w, _wq(w), x, kp, vp, lens, prev, nxt)
+
+
+def test_decode_layer_schedule_with_refill():
+    """Four consecutive steps of the bs-64 layer under the continuous-batching schedule
+    (kv_len ~ U[234, 4096] at admission, lifetimes ~ U[1, 256] steps): slots grow by one row
+    per step, and a retired slot is refilled between steps with a fresh prefix in the cache
+    (the prefill's K/V rows) and a zeroed prev window. Every step is checked against the
+    oracle stage by stage, with the cache contents the GPU holds at that step."""
+    bs, cap, steps, seed = 64, 32768, 4, 1
+    sched, refill = synth.slot_schedule(bs, steps, 234, 4096, 256, seed)
+    assert refill[1:].any()  # the schedule retires and refills at least one slot
+    L, w = _layer(bs, cap, 4096 + steps)
+    wq = _wq(w)
+    lens = sched[0]
+    _, kp, vp, prev, _ = _fill(L, lens, seed)
+    kp, vp = list(kp), list(vp)
+    for s in range(steps):
+        lens = sched[s]
+        for b in np.nonzero(refill[s])[0]:
+            # a new request takes slot b: its prompt's K/V rows fill positions 0 .. kv_len-2
+            # and its prev window starts from zeros
+            n = int(lens[b]) - 1
+            kp[b] = synth.kv_prefix(1, L.Hkv, L.D, [n], seed + 100 + s, synth.TID["k"])[0]
+            vp[b] = synth.kv_prefix(1, L.Hkv, L.D, [n], seed + 100 + s, synth.TID["v"])[0]
+            L.k_cache[b, :, :n].copy_(dev_bf16(kp[b]))
+            L.v_cache[b, :, :n].copy_(dev_bf16(vp[b]))
+            prev[b] = 0
+            L.prev[b].zero_()
+        for b in range(bs):
+            assert kp[b].shape[1] == lens[b] - 1
+        x = synth.activations(bs, L.d_model, seed + 10 + s)
+        nxt = synth.codes((bs, L.prev.shape[2]), 4096, seed + 10 + s, synth.TID["next"])
+        L.x.copy_(dev_bf16(x))
+        L.next_tokens.copy_(dev(nxt))
+        L.kv_len.copy_(dev(lens.astype(np.int32)))
+        L.err.zero_()
+        L.step()
+        torch.cuda.synchronize()
+        assert int(L.err.item()) == 0, s
+        kn, vn = _check_step(L, w, wq, x, kp, vp, lens, prev, nxt)
+        # the cache now holds the appended rows: they are part of the next step's prefix
+        kp = [np.concatenate([kp[b], kn[b][:, None, :]], axis=1) for b in range(bs)]
+        vp = [np.concatenate([vp[b], vn[b][:, None, :]], axis=1) for b in range(bs)]
+        prev = ops.prev_tokens_shift(prev, nxt)
 
 
 def test_graph_replay_matches_eager():

@@ -335,3 +335,63 @@ def test_decode_step_composition():
     qkv = mx.bf16_to_f64(out["qkv"])
     assert qkv.shape == (2, (4 + 4) * 16)
     assert np.isfinite(out["y"]).all() and not np.array_equal(out["y_bf16"], x)
+
+
+def test_decode_step_closed_form():
+    """The layer step on hand-built weights whose result is known in closed form, so that a
+    wiring mistake in the composition (k and v slices swapped or offset, the new row appended
+    at the wrong position or not at all, o used without its MX quantisation, the wrong
+    residual) changes the result:
+
+    x = 1 and gamma = 1, so RMSNorm gives 1.0 exactly and its MX codes are exact; the k rows
+    of Wqkv are zero and every cached K row is zero, so all scores are 0 and attention is the
+    plain mean of the V rows (kv_len rows, the appended one included); the v rows of Wqkv pick
+    input channel j, so the appended V row is all ones; Wo is the identity and W13 is zero,
+    so x1 = x + MX(o) and y = x1. The V prefix is chosen so that o hits E4M3 rounding ties at
+    the block's scale (amax 1.75: codes step by 2^-3 in [1, 2), 2^-4 in [0.5, 1))."""
+    bs, d, dff, Hq, Hkv, D = 2, 64, 32, 2, 1, 32
+    E4M3_ONE = 0x38  # 1.0 = 2^(7-7) x 1.000
+    x = np.full((bs, d), 0x3F80, np.uint16)     # bf16 1.0
+    ones = np.full((d,), 0x3F80, np.uint16)
+    wq = mx.mx_quantize(mx.bf16_to_f64(synth.weights(Hq * D, d, 0, synth.TID["wqkv"], 0.5)))
+    wqkv_q = np.zeros(((Hq + 2 * Hkv) * D, d), np.uint8)
+    wqkv_s = np.full(((Hq + 2 * Hkv) * D, d // 32), 127, np.uint8)
+    wqkv_q[:Hq * D], wqkv_s[:Hq * D] = wq
+    for j in range(D):                         # v row j = input channel j
+        wqkv_q[(Hq + Hkv) * D + j, j] = E4M3_ONE
+    wo_q = np.zeros((d, Hq * D), np.uint8)
+    wo_q[np.arange(d), np.arange(d)] = E4M3_ONE
+    wo_s = np.full((d, Hq * D // 32), 127, np.uint8)
+    w13 = (np.zeros((2 * dff, d), np.uint8), np.full((2 * dff, d // 32), 127, np.uint8))
+    w2 = mx.mx_quantize(mx.bf16_to_f64(synth.weights(d, dff, 0, synth.TID["w2"], 0.5)))
+    # sequence 0: kv_len 4 (3 cached rows + the appended one), sequence 1: kv_len 2
+    o0 = np.full(D, 0.25)
+    o0[:5] = [1.75, 1.0625, 1.1875, 0.53125, -0.75]
+    o1 = np.full(D, 0.5)
+    o1[0] = -1.5
+    lens = np.array([4, 2])
+    vp0 = np.zeros((Hkv, 3, D))
+    vp0[0, 0] = 4 * o0 - 1                      # mean over {4 o - 1, 0, 0, 1} = o
+    vp1 = (2 * o1 - 1).reshape(Hkv, 1, D)       # mean over {2 o - 1, 1} = o
+    kp = [np.zeros((Hkv, 3, D), np.uint16), np.zeros((Hkv, 1, D), np.uint16)]
+    vp = [mx.f64_to_bf16(vp0), mx.f64_to_bf16(vp1)]
+    prev = synth.codes((bs, 4, 10), 4096, 0, synth.TID["prev"])
+    nxt = synth.codes((bs, 10), 4096, 0, synth.TID["next"])
+    out = ops.decode_layer_step(x, ones, ones, (wqkv_q, wqkv_s), (wo_q, wo_s), w13, w2, kp, vp, lens, prev, nxt,
+                                Hq, Hkv, D, 1e-6, 1 / math.sqrt(D))
+    qkv = mx.bf16_to_f64(out["qkv"])
+    np.testing.assert_array_equal(qkv[:, Hq * D:(Hq + Hkv) * D], 0.0)      # k of the new row
+    np.testing.assert_array_equal(qkv[:, (Hq + Hkv) * D:], 1.0)           # v of the new row
+    o = mx.bf16_to_f64(out["o"]).reshape(bs, Hq, D)
+    for h in range(Hq):                                                    # both heads read kv head 0
+        np.testing.assert_array_equal(o[0, h], o0)
+        np.testing.assert_array_equal(o[1, h], o1)
+    # MX(o) at block amax 1.75 (scale 2^-8): 1.0625 -> 1.0 and 1.1875 -> 1.25 (ties to the even
+    # code), 0.53125 -> 0.5 (tie), the rest exact
+    oq0 = np.full(D, 0.25)
+    oq0[:5] = [1.75, 1.0, 1.25, 0.5, -0.75]
+    x1 = mx.bf16_to_f64(out["x1"])
+    np.testing.assert_array_equal(x1[0], 1.0 + np.tile(oq0, Hq))
+    np.testing.assert_array_equal(x1[1], 1.0 + np.tile(o1, Hq))
+    np.testing.assert_array_equal(out["y"], x1)                             # h = 0: y is the residual
+    np.testing.assert_array_equal(out["y_bf16"], out["x1"])
