@@ -69,10 +69,6 @@ int mxg_version(void);
  * (K % 128 == 0); enable == 0 forces the CUDA-core kernels. Process-wide, not thread-safe;
  * returns the previous setting. */
 int mxg_set_tensor_core_path(int enable);
-/* Path switch for cross-checks: enable == 0 makes mlp_swiglu_mxfp8 run as two launches
- * (gate/up + SwiGLU, then the down GEMM) even where the one-launch kernel applies; returns the
- * previous setting (default 1). Process-wide, not thread-safe. */
-int mxg_set_mlp_fused(int enable);
 /* Failure-detection test hook. on != 0: until it is called again with 0, the split-KV decode
  * attention kernels (every gqa_decode_attn* entry point) issue no K/V loads, so their
  * consumer warps wait on pipeline stages that nothing fills; each such wait gives up after
@@ -133,21 +129,12 @@ mxg_status mlp_gate_up_swiglu_mxfp8(const uint8_t* xq, const uint8_t* xs, int64_
 
 /*
  * mlp_swiglu_mxfp8 -- the whole Qwen3-4B-shaped SwiGLU MLP ([S2.1] "Kernel Benchmark
- * Results": quantise -> gate/up -> SwiGLU -> quantise -> down): h = MX(silu(X W_g^T) *
- * X W_u^T) into the workspace, then y = H' W2'^T (+ residual) in bf16.
+ * Results": quantise -> gate/up -> SwiGLU -> quantise -> down): the call above into the
+ * workspace, then y = H' W2'^T (+ residual) in bf16.
  *   w2q [d_model, d_ff], w2s [d_model, d_ff/32]; residual bf16 [M, d_model] or NULL;
  *   y bf16 [M, d_model].
- *   workspace: mlp_swiglu_mxfp8_workspace(M, d_model, d_ff) bytes, ZEROED by the caller
- *   before its first use (each call leaves its control words zero again). It holds hq at
- *   offset 0 (M*d_ff bytes) and hs right after (M*d_ff/32 bytes), then scratch.
- * Decode sizes (M <= 128, d_model and d_ff multiples of 128, d_ff/64 <= the SM count) run as
- * ONE persistent kernel: one CTA per SM streams its share of W13 and then of W2 without a
- * break; the down projection is split along d_ff and its partials are summed in a fixed
- * order -- the same splits and order as the two-launch path, so both give identical bits.
- * Its CTAs wait on one another with bounded waits: a wait that runs out records MXG_ETIMEOUT
- * in the int32 status word at byte offset mlp_swiglu_mxfp8_workspace(...) - 128 of the
- * workspace (first error wins; the caller reads and clears it). Other shapes run as the
- * gate/up launch above followed by mxfp8_gemm.
+ *   workspace: mlp_swiglu_mxfp8_workspace(M, d_model, d_ff) bytes; it holds hq at offset 0
+ *   (M*d_ff bytes) and hs right after (M*d_ff/32 bytes), then the down GEMM's scratch.
  */
 size_t mlp_swiglu_mxfp8_workspace(int64_t M, int64_t d_model, int64_t d_ff);
 mxg_status mlp_swiglu_mxfp8(const uint8_t* xq, const uint8_t* xs, int64_t M, int64_t d_model, int64_t d_ff,

@@ -29,7 +29,6 @@ _SIGS = {
     "mxg_version": (ctypes.c_int, []),
     "mxg_set_tensor_core_path": (ctypes.c_int, [ctypes.c_int]),
     "mxg_debug_stall_attn_loads": (ctypes.c_int, [ctypes.c_int]),
-    "mxg_set_mlp_fused": (ctypes.c_int, [ctypes.c_int]),
     "mxfp8_quantize": (ctypes.c_int, [c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_vp]),
     "rmsnorm_mxfp8_quantize": (ctypes.c_int, [c_vp, c_vp, c_f32, c_i64, c_i64, c_i64, c_vp, c_vp, c_vp]),
     "mxfp8_gemm_workspace": (c_sz, [c_i64, c_i64, c_i64]),
@@ -259,7 +258,7 @@ def mlp_swiglu_mxfp8(xq, xs, w13q, w13s, w2q, w2s, residual=None, y=None, worksp
     y = _out(y, "y", torch.bfloat16, (M, d_model), xq.device)
     need = mlp_swiglu_mxfp8_workspace(M, d_model, d_ff)
     if workspace is None:
-        workspace = torch.zeros(need, dtype=torch.uint8, device=xq.device)  # control words start at 0
+        workspace = torch.zeros(need, dtype=torch.uint8, device=xq.device)  # split-K counters start at 0
     _check(workspace, "workspace", torch.uint8, ndim=1)
     _call("mlp_swiglu_mxfp8", _ptr(xq), _ptr(xs), M, d_model, d_ff, _ptr(w13q), _ptr(w13s), _ptr(w2q), _ptr(w2s),
           _ptr(residual), _ptr(y), _ptr(workspace), workspace.numel(), _stream())

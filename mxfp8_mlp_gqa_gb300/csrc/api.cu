@@ -29,7 +29,6 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline mxg_status launched(cudaError_t e) { return e == cudaSuccess ? MXG_OK : MXG_ELAUNCH; }
 
 int g_tc_path = 1;  // 1: tcgen05 kernels where the shape allows, 0: CUDA-core kernels only
-int g_mlp_fused = 1;  // 1: mlp_swiglu_mxfp8 runs the one-launch kernel where the shape allows
 
 }  // namespace
 
@@ -87,12 +86,6 @@ int mxg_version(void) { return 100; }
 int mxg_set_tensor_core_path(int enable) {
   const int prev = g_tc_path;
   g_tc_path = enable ? 1 : 0;
-  return prev;
-}
-
-int mxg_set_mlp_fused(int enable) {
-  const int prev = g_mlp_fused;
-  g_mlp_fused = enable ? 1 : 0;
   return prev;
 }
 
@@ -161,26 +154,10 @@ mxg_status mlp_gate_up_swiglu_mxfp8(const uint8_t* xq, const uint8_t* xs, int64_
   return launched(launch_gate_up_swiglu_simt(xq, xs, M, d_model, d_ff, w13q, w13s, hq, hs, (cudaStream_t)stream));
 }
 
-namespace {
-// Workspace of mlp_swiglu_mxfp8: hq [M, d_ff] at 0, hs [M, d_ff/32] right after; from `off`
-// the down GEMM's scratch (two-launch path) or the fused kernel's split partials; the fused
-// kernel's control words sit in the last mlp_fused_ctrl_bytes of the workspace size.
-size_t mlp_h_bytes(int64_t M, int64_t d_ff) {
-  const size_t h = (size_t)M * (size_t)d_ff;
-  return (h + h / 32 + 255) / 256 * 256;
-}
-size_t mlp_fused_bytes(int64_t M, int64_t d_model, int64_t d_ff) {
-  if (!mlp_fused_supported(M, d_model, d_ff)) return 0;
-  return mlp_h_bytes(M, d_ff) + (mlp_fused_part_bytes(M, d_model, d_ff) + 255) / 256 * 256 +
-         mlp_fused_ctrl_bytes(d_model);
-}
-}  // namespace
-
 size_t mlp_swiglu_mxfp8_workspace(int64_t M, int64_t d_model, int64_t d_ff) {
-  if (M <= 0 || d_model <= 0 || d_ff <= 0) return 0;
-  const size_t two = mlp_h_bytes(M, d_ff) + mxfp8_gemm_workspace(M, d_model, d_ff);
-  const size_t fused = mlp_fused_bytes(M, d_model, d_ff);
-  return two > fused ? two : fused;
+  const size_t h = (size_t)M * (size_t)d_ff;
+  size_t off = (h + h / 32 + 255) / 256 * 256;
+  return off + mxfp8_gemm_workspace(M, d_model, d_ff);
 }
 
 mxg_status mlp_swiglu_mxfp8(const uint8_t* xq, const uint8_t* xs, int64_t M, int64_t d_model, int64_t d_ff,
@@ -193,18 +170,7 @@ mxg_status mlp_swiglu_mxfp8(const uint8_t* xq, const uint8_t* xs, int64_t M, int
   if (!aligned16(workspace)) return MXG_EALIGN;
   uint8_t* hq = static_cast<uint8_t*>(workspace);
   uint8_t* hs = hq + M * d_ff;
-  const size_t off = mlp_h_bytes(M, d_ff);
-  if (g_tc_path && g_mlp_fused && mlp_fused_supported(M, d_model, d_ff) && d_model % 128 == 0 && aligned16(xq) &&
-      aligned16(w13q) && aligned16(w2q) && (!residual || aligned16(residual)) && aligned16(y)) {
-    const size_t ws_total = mlp_swiglu_mxfp8_workspace(M, d_model, d_ff);
-    float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + off);
-    int* ctrl = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + ws_total - mlp_fused_ctrl_bytes(d_model));
-    bool unsupported = false;
-    const cudaError_t e = launch_mlp_fused(xq, xs, M, d_model, d_ff, w13q, w13s, w2q, w2s,
-                                           static_cast<const uint16_t*>(residual), static_cast<uint16_t*>(y), hq, hs,
-                                           part, ctrl, (cudaStream_t)stream, &unsupported);
-    if (!unsupported) return launched(e);
-  }
+  const size_t off = ((size_t)M * d_ff + (size_t)M * d_ff / 32 + 255) / 256 * 256;
   mxg_status st = mlp_gate_up_swiglu_mxfp8(xq, xs, M, d_model, d_ff, w13q, w13s, hq, hs, stream);
   if (st != MXG_OK) return st;
   return mxfp8_gemm(hq, hs, w2q, w2s, M, d_model, d_ff, residual, y, static_cast<uint8_t*>(workspace) + off,

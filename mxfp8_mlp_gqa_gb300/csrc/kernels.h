@@ -35,17 +35,6 @@ cudaError_t launch_gqa_decode_attn(const CUtensorMap& tmK, const CUtensorMap& tm
                                    int64_t max_kv_len, float scale, uint16_t* out, int32_t* err, void* ws,
                                    cudaStream_t st, uint8_t* oq = nullptr, uint8_t* os = nullptr,
                                    const KvPages* pages = nullptr);
-// The whole decode-size MLP in one persistent kernel (mlp_fused.cu): M <= 128, d_model and d_ff
-// multiples of 128, and enough SMs for one gate/up tile (64 d_ff columns) per CTA. Scratch:
-// hq, hs, the fp32 split partials (mlp_fused_part_bytes) and the control words
-// (mlp_fused_ctrl_bytes, zero before the first call; every call leaves them zero).
-bool mlp_fused_supported(int64_t M, int64_t d_model, int64_t d_ff);
-size_t mlp_fused_part_bytes(int64_t M, int64_t d_model, int64_t d_ff);
-size_t mlp_fused_ctrl_bytes(int64_t d_model);
-cudaError_t launch_mlp_fused(const uint8_t* xq, const uint8_t* xs, int64_t M, int64_t d_model, int64_t d_ff,
-                             const uint8_t* w13q, const uint8_t* w13s, const uint8_t* w2q, const uint8_t* w2s,
-                             const uint16_t* residual, uint16_t* y, uint8_t* hq, uint8_t* hs, float* part, int* ctrl,
-                             cudaStream_t st, bool* unsupported);
 // Test hook: on != 0 makes the split-KV decode kernel's copy warp issue no loads (its waits
 // then run out: MXG_ETIMEOUT). Synchronous copy to a device variable of the current device.
 cudaError_t set_attn_load_stall(int on);
