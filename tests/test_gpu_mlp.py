@@ -64,6 +64,28 @@ def test_ragged_m_with_residual(M):
     assert_float_close(y, ref["y"])
 
 
+@pytest.mark.parametrize("M,d_model,d_ff", [(1, 2560, 9728), (2, 2560, 9728), (1, 256, 768), (2, 512, 1536)])
+@pytest.mark.parametrize("residual", [False, True])
+def test_one_and_two_token_path(M, d_model, d_ff, residual):
+    """One or two tokens through mlp_swiglu_mxfp8: the h it leaves in its workspace is the
+    oracle's re-quantised h (<= 1 E4M3 step on <= 0.1 % of elements), y meets the MLP bound,
+    and repeated calls on one workspace give the same bits."""
+    gw13, gw2, ow13, ow2 = _weights(d_model, d_ff)
+    x = synth.activations(M, d_model, 5, outlier_frac=0.01)
+    xq, xs = api.mxfp8_quantize(dev_bf16(x))
+    res = synth.activations(M, d_model, 5, tid=synth.TID["residual"]) if residual else None
+    ws = torch.zeros(api.mlp_swiglu_mxfp8_workspace(M, d_model, d_ff), dtype=torch.uint8, device="cuda")
+    y = api.mlp_swiglu_mxfp8(xq, xs, *gw13, *gw2, residual=None if res is None else dev_bf16(res), workspace=ws)
+    y2 = api.mlp_swiglu_mxfp8(xq, xs, *gw13, *gw2, residual=None if res is None else dev_bf16(res), workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+    ref = ops.swiglu_mlp(*mx.mx_quantize(mx.bf16_to_f64(x)), *ow13, *ow2, residual_bf16=res)
+    hq = ws[:M * d_ff].view(M, d_ff).cpu().numpy()
+    hs = ws[M * d_ff:M * d_ff + M * d_ff // 32].view(M, d_ff // 32).cpu().numpy()
+    assert_requant_close(hq, hs, ref["hq"], ref["hs"])
+    assert_float_close(host_f64(y), ref["y"])
+
+
 def test_mlp_empty_batch():
     gw13, gw2, _, _ = _weights(256, 768)
     xq = torch.empty((0, 256), dtype=torch.uint8, device="cuda")
