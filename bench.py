@@ -181,7 +181,7 @@ class ClockSampler:
 
 
 # DRAM traffic of the attention split kernel per algorithmic byte, from one ncu capture of the
-# same kernel on a smaller cache (profiles/gqa_split_kernel_bs64_cap4096.md: 634.95 MB of
+# same kernel on a smaller cache (the bs-64, 4096-position capture: 634.95 MB of
 # dram__bytes_read.sum + dram__bytes_write.sum for 622.54 MB of algorithmic bytes). Traffic
 # grows in proportion to the prefix tokens read, so it is scaled to the step's launch. Set to
 # None whenever the kernel changes until it is captured again.
@@ -271,10 +271,22 @@ def run_ours(args, rank, local_rank, world):
 
     api.lib()
     total_steps = args.warmup + args.steps
-    sched, _refill = synth.slot_schedule(BS, total_steps + 1, KV_LO, KV_HI, LIFE_HI, seed=0)
+    sched, refill = synth.slot_schedule(BS, total_steps + 1, KV_LO, KV_HI, LIFE_HI, seed=0)
     max_kv_len = int(sched.max())
     L = build_layer(dev, max_kv_len)
     sched_d = torch.from_numpy(sched).to(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+
+    def admit(s):
+        # between steps (untimed): a slot retired by the schedule takes a new request -- its
+        # prompt's K/V rows (positions 0 .. kv_len-2, what the prefill leaves) and a zeroed
+        # prev window
+        for b in np.nonzero(refill[s])[0]:
+            n = int(sched[s][b]) - 1
+            for c in (L.k_cache, L.v_cache):
+                c[b, :, :n].copy_(torch.randn((HKV, n, HD), generator=gen, device=dev).to(torch.bfloat16))
+            L.prev[b].zero_()
     flush = L2Flush(dev)
     peak_gbs, peak_src = measured_peaks()
 
@@ -294,6 +306,7 @@ def run_ours(args, rank, local_rank, world):
     torch.cuda.current_stream().wait_stream(cap)
     plain = L.capture()  # the same step without event nodes: the headline timing
     for s in range(args.warmup):
+        admit(s)
         L.kv_len.copy_(sched_d[s])
         plain.replay()
         graph.replay()
@@ -306,7 +319,8 @@ def run_ours(args, rank, local_rank, world):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     step_ms = []
     for i in range(args.steps):
-        L.kv_len.copy_(sched_d[args.warmup + i])   # schedule advance (retire/refill), not timed
+        admit(args.warmup + i)                # retire / refill per the schedule, not timed
+        L.kv_len.copy_(sched_d[args.warmup + i])   # schedule advance, not timed
         flush()                               # L2 flush, not timed
         e0.record()
         plain.replay()
@@ -841,6 +855,95 @@ def run_cpu_baseline(bs_sample=1):
             "seconds": round(sec, 3), "bytes": by}
 
 
+# The oracle per configuration (the pages' workloads, timed on this host's cores): each case runs
+# in a child process so that the BLAS thread count is fixed before numpy loads -- once with one
+# thread, once with every core.
+CPU_CASES = ("config1_step", "config2_mlp_M1", "config2_mlp_M128", "config3_attn_bs64", "config5_gemm_4096_sampled")
+THREAD_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS")
+
+
+def cpu_case(name):
+    """One timed oracle call of the named configuration; returns seconds, value, unit, sample."""
+    from mxfp8_mlp_gqa_gb300 import synth
+    from oracle import mx, ops
+
+    def mxq(bits):
+        return mx.mx_quantize(mx.bf16_to_f64(bits))
+
+    if name == "config1_step":
+        d, dff, hq, hkv, hd = 256, 768, 4, 2, 64
+        w = {k: mxq(synth.weights(n, kk, 0, synth.TID[k])) for k, n, kk in
+             (("wqkv", (hq + 2 * hkv) * hd, d), ("wo", d, hq * hd), ("w13", 2 * dff, d), ("w2", d, dff))}
+        lens = np.array([100])
+        args = (synth.activations(1, d, 0), synth.gamma(d, 0, synth.TID["gamma1"]),
+                synth.gamma(d, 0, synth.TID["gamma2"]), w["wqkv"], w["wo"], w["w13"], w["w2"],
+                synth.kv_prefix(1, hkv, hd, lens - 1, 0, synth.TID["k"]),
+                synth.kv_prefix(1, hkv, hd, lens - 1, 0, synth.TID["v"]), lens,
+                synth.codes((1, 8, 10), 1024, 0, synth.TID["prev"]), synth.codes((1, 10), 1024, 0, synth.TID["next"]),
+                hq, hkv, hd, EPS, 1 / 8)
+        t0 = time.perf_counter()
+        ops.decode_layer_step(*args)
+        sec = time.perf_counter() - t0
+        return {"seconds": sec, "value": round(sec * 1e3, 3), "unit": "ms per step",
+                "sample": "the whole tiny decode-layer step (d_model 256, d_ff 768, 4/2 heads x 64, kv_len 100)"}
+    if name.startswith("config2_mlp_M"):
+        M = int(name[len("config2_mlp_M"):])
+        w13 = mxq(synth.weights(2 * D_FF, D_MODEL, 0, synth.TID["w13"]))
+        w2 = mxq(synth.weights(D_MODEL, D_FF, 0, synth.TID["w2"]))
+        xq, xs = mxq(synth.activations(M, D_MODEL, 0, outlier_frac=0.01))
+        t0 = time.perf_counter()
+        ops.swiglu_mlp(xq, xs, *w13, *w2)
+        sec = time.perf_counter() - t0
+        return {"seconds": sec, "value": round(mlp_bytes(M) / sec / 1e9, 4), "unit": "GB/s",
+                "sample": f"the whole MLP at M = {M} (2560 / 9728, weights already MX-quantised)"}
+    if name == "config3_attn_bs64":
+        lens = synth.kv_lens(BS, KV_LO, KV_HI, seed=0)
+        q = mx.bf16_to_f64(synth.normal_bf16((BS, HQ, HD), 1.0, 0, synth.TID["q"]))
+        kp = [mx.bf16_to_f64(a) for a in synth.kv_prefix(BS, HKV, HD, lens, 0, synth.TID["k"])]
+        vp = [mx.bf16_to_f64(a) for a in synth.kv_prefix(BS, HKV, HD, lens, 0, synth.TID["v"])]
+        t0 = time.perf_counter()
+        ops.gqa_decode_attention(q, kp, vp, 1 / math.sqrt(HD))
+        sec = time.perf_counter() - t0
+        return {"seconds": sec, "value": round(attn_bytes(lens) / sec / 1e9, 4), "unit": "GB/s",
+                "sample": "GQA decode attention, bs 64, kv_len ~U[234, 4096] (sum %d)" % int(lens.sum())}
+    if name == "config5_gemm_4096_sampled":
+        N = 4096
+        g = synth.rng(0, synth.TID["sample"])
+        rows = np.sort(g.choice(N, 256, replace=False))
+        cols = np.sort(g.choice(N, 256, replace=False))
+        a = synth.normal_bf16((N, N), 1.0, 0, synth.TID["a"])[rows]
+        b = synth.normal_bf16((N, N), 1.0, 0, synth.TID["b"])[cols]
+        aq, bq = mxq(a), mxq(b)
+        t0 = time.perf_counter()
+        ops.mx_gemm(*aq, *bq)
+        sec = time.perf_counter() - t0
+        return {"seconds": sec, "value": round(2 * 256 * 256 * N / sec / 1e9, 3), "unit": "GFLOP/s",
+                "sample": "256 sampled rows x 256 sampled columns of the 4096^3 MXFP8 GEMM (fp64 dot products)"}
+    raise ValueError(name)
+
+
+def run_cpu_cases():
+    """Every CPU case twice in child processes: one BLAS thread, then all cores."""
+    out = {}
+    for name in CPU_CASES:
+        row = {}
+        for label, n in (("1_thread", "1"), ("all_cores", None)):
+            env = dict(os.environ)
+            for v in THREAD_VARS:
+                if n is None:
+                    env.pop(v, None)
+                else:
+                    env[v] = n
+            r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-case", name], env=env,
+                               capture_output=True, text=True, timeout=600)
+            try:
+                row[label] = json.loads(r.stdout.strip().splitlines()[-1])
+            except (IndexError, ValueError):
+                row[label] = {"error": (r.stderr or r.stdout)[-300:]}
+        out[name] = row
+    return {"cores": os.cpu_count(), "kind": "oracle", "cases": out}
+
+
 def run_reference(args, rank, world):
     """--impl reference: the oracle timed on the host cores, on this workload, one bounded
     sample (one of the 64 sequences, all weights) per step. Rank 0 only."""
@@ -883,10 +986,14 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sweeps", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-case", default=None, help=argparse.SUPPRESS)
     ap.add_argument("--profile", default=None,
                     help="run one kernel family only (for ncu captures): mlp:<M> | attn:<bs>[:<cap>] | "
                          "gemm:<M>x<N>x<K> | cublas:<M>x<N>x<K> (library kernel, context)")
     args = ap.parse_args(argv)
+    if args.cpu_case:  # child process of run_cpu_cases: one oracle timing, no GPU
+        print(json.dumps(cpu_case(args.cpu_case)))
+        return 0
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, local_rank, world = dist_env()
@@ -908,9 +1015,10 @@ def main(argv=None):
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     res = run_ours(args, rank, local_rank, world)
-    cpu = None
+    cpu = cpu_cases = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = run_cpu_baseline()
+        cpu_cases = run_cpu_cases()
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(res["value"], 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -922,7 +1030,8 @@ def main(argv=None):
                              "~0.68 GB > 129 MB L2", "timing": "one captured CUDA graph per step, events around each replay on the launching "
                                            "stream; per-kernel breakdown from a second graph with timing events "
                                            "between its kernels"},
-            "e2e": res["e2e"], "roofline": res["roofline"], "cpu_baseline": cpu, "clocks": res["clocks"],
+            "e2e": res["e2e"], "roofline": res["roofline"], "cpu_baseline": cpu,
+            "cpu_baseline_configs": cpu_cases, "clocks": res["clocks"],
             "gpu_launches": res["gpu_launches"], "eager_ms_per_step": round(res["eager_ms_per_step"], 4),
             "evented_ms_per_step": round(res["evented_ms_per_step"], 4),
             "breakdown": res["breakdown"], "sweeps": res["sweeps"],
