@@ -29,6 +29,8 @@ namespace {
 
 constexpr int kTileTok = 64;        // tokens per pipeline stage
 constexpr int kMaxSplitTiles = 16;  // a split covers at most 1024 tokens (attn_chunk)
+constexpr int kSplitTok = 768;      // split length (attn_chunk)
+constexpr int kMinSplitItems = 128; // fewest (split, b, g) items at the kv_len bound (attn_chunk)
 constexpr int kConsumers = 4;       // consumer warps (16 tokens each per tile)
 constexpr int kThreads = (kConsumers + 1) * 32;
 
@@ -158,6 +160,321 @@ __device__ int g_stall_attn_loads = 0;
 
 }  // namespace
 
+// B fragments of Q^T (k = dim, n = head); lane holds head r4.
+//  bf16 cache: k-step ks, dims ks*16 + 2*c4 (+1) and +8 (+9).
+//  MXFP8 cache: k-steps 2j, 2j+1 cover MX block j; the thread's k slots of step 2j+e hold
+//  dims 32j + 8*c4 + 4e + {0, 1} and + {2, 3} (the K fragments below use the same order, so
+//  the dot product is unchanged), as f16 after scaling q by 2^qa.
+template <int D, bool kMx>
+__device__ __forceinline__ void load_q_frags(const uint16_t* __restrict__ q, int64_t ld_q, int b, int h0, int group,
+                                             float scale_log2, int lane, uint32_t (&qb)[D / 16][2], float& sl2) {
+  constexpr int KS = D / 16;
+  constexpr int NB = D / 32;
+  const int c4 = lane & 3, r4 = lane >> 2;
+  sl2 = scale_log2;
+  const bool hv = r4 < group;
+  const uint16_t* qh = q + (int64_t)b * ld_q + (int64_t)(h0 + (hv ? r4 : 0)) * D;
+  if constexpr (!kMx) {
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qb[ks][0] = hv ? *reinterpret_cast<const uint32_t*>(qh + ks * 16 + 2 * c4) : 0u;
+      qb[ks][1] = hv ? *reinterpret_cast<const uint32_t*>(qh + ks * 16 + 8 + 2 * c4) : 0u;
+    }
+  } else {
+    uint4 qw[NB];
+    float am = 0.f;
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      qw[j] = hv ? *reinterpret_cast<const uint4*>(qh + 32 * j + 8 * c4) : make_uint4(0, 0, 0, 0);
+      const uint32_t w[4] = {qw[j].x, qw[j].y, qw[j].z, qw[j].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) am = fmaxf(am, fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
+    }
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) am = fmaxf(am, __shfl_xor_sync(MXG_FULL_MASK, am, off));
+    // 2^qa brings the group's largest |q| into [2^14, 2^15): every bf16 q is then an f16 exactly
+    // unless it sits 2^38 below that maximum
+    int qa = 0;
+    if (am > 0.f) qa = min(100, max(-100, 14 - ((int)((__float_as_uint(am) >> 23) & 0xFF) - 127)));
+    const float f = __uint_as_float((uint32_t)(qa + 127) << 23);
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      const uint32_t w[4] = {qw[j].x, qw[j].y, qw[j].z, qw[j].w};
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        qb[2 * j + e][0] = pack_f16x2(bf16_lo(w[2 * e]) * f, bf16_hi(w[2 * e]) * f);
+        qb[2 * j + e][1] = pack_f16x2(bf16_lo(w[2 * e + 1]) * f, bf16_hi(w[2 * e + 1]) * f);
+      }
+    }
+    sl2 = scale_log2 * __uint_as_float((uint32_t)(127 - qa) << 23);
+  }
+}
+
+// Copy the K and V tile starting at cache row `row` (and, for an MXFP8 cache, their scales)
+// into ring stage s; the stage's full barrier expects all of its bytes.
+template <int D, bool kMx>
+__device__ __forceinline__ void issue_tile(uint8_t* ring, int s, int row, uint64_t* full_s, const CUtensorMap* tmK,
+                                           const CUtensorMap* tmV, const CUtensorMap* tmKS, const CUtensorMap* tmVS,
+                                           uint64_t pol) {
+  using S = AttnShape<D, kMx>;
+  mbar_arrive_expect_tx(full_s, S::kStageBytes);
+  uint8_t* kt = ring + s * S::kCodeStageBytes;
+  uint8_t* vt = kt + S::kTileBytes;
+  if constexpr (kMx) {
+    uint8_t* kst = ring + S::kScaleRingOff + s * 2 * S::kScaleTileBytes;
+    tma_load_2d_hint(kt, tmK, full_s, 0, row, pol);
+    tma_load_2d_hint(vt, tmV, full_s, 0, row, pol);
+    // row is a multiple of 64, so its scales start on a 16-byte line
+    const int line = row / (16 / (D / 32));
+    tma_load_2d_hint(kst, tmKS, full_s, 0, line, pol);
+    tma_load_2d_hint(kst + S::kScaleTileBytes, tmVS, full_s, 0, line, pol);
+  } else {
+#pragma unroll
+    for (int h = 0; h < S::kHalves; ++h) {
+      tma_load_2d_hint(kt + h * kTileTok * 128, tmK, full_s, h * 64, row, pol);
+      tma_load_2d_hint(vt + h * kTileTok * 128, tmV, full_s, h * 64, row, pol);
+    }
+  }
+}
+
+// One consumer warp's share of a 64-token K/V tile in ring stage s: its 16 tokens tb .. tb+15
+// (tokens at or past t1 are masked), S^T = K Q^T, the online-softmax update of (m, l) per head
+// and O^T += V^T P^T.
+template <int D, bool kMx>
+__device__ __forceinline__ void consume_tile(uint8_t* ring, int s, int tb, int t1, int r0, int lane,
+                                             const uint32_t (&qb)[D / 16][2], float sl2, float& m_a, float& m_b,
+                                             float& l_a, float& l_b, float (&o)[D / 16][4], uint16_t* ps,
+                                             uint16_t* pl) {
+  using S = AttnShape<D, kMx>;
+  constexpr int KS = D / 16;
+  constexpr int NB = D / 32;
+  const int c4 = lane & 3, r4 = lane >> 2;
+  const uint32_t kbase = smem_u32(ring + s * S::kCodeStageBytes);
+  const uint32_t vbase = kbase + S::kTileBytes;
+  const uint32_t ksbase = smem_u32(ring + S::kScaleRingOff + s * 2 * S::kScaleTileBytes);
+  const uint32_t vsbase = ksbase + S::kScaleTileBytes;
+
+  // S^T[16 tok x 8 heads] = K[16 x D] Q^T[D x 8]
+  float sc[4] = {0.f, 0.f, 0.f, 0.f};
+  if constexpr (!kMx) {
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t a0, a1, a2, a3;
+      ldmatrix_x4(tile_addr(kbase, r0 + (lane & 7) + 8 * ((lane >> 3) & 1), ks * 16 + 8 * (lane >> 4)), a0, a1,
+                  a2, a3);
+      mma_bf16_16816(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+    }
+  } else {
+    float acc[NB][4];
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+      const uint2 ka = lds_u32x2(code_addr<D>(kbase, r0 + r4, 32 * j + 8 * c4));
+      const uint2 kb = lds_u32x2(code_addr<D>(kbase, r0 + r4 + 8, 32 * j + 8 * c4));
+      uint32_t a0, a1, a2, a3;
+      e4m3x4_to_f16(ka.x, a0, a2);
+      e4m3x4_to_f16(kb.x, a1, a3);
+      mma_f16_16816(acc[j], a0, a1, a2, a3, qb[2 * j][0], qb[2 * j][1]);
+      e4m3x4_to_f16(ka.y, a0, a2);
+      e4m3x4_to_f16(kb.y, a1, a3);
+      mma_f16_16816(acc[j], a0, a1, a2, a3, qb[2 * j + 1][0], qb[2 * j + 1][1]);
+    }
+    // per-block exponents of tokens r4 and r4+8
+    uint32_t ska, skb;
+    if constexpr (D == 128) {
+      ska = lds_u32(ksbase + (r0 + r4) * NB);
+      skb = lds_u32(ksbase + (r0 + r4 + 8) * NB);
+    } else {
+      ska = lds_u16(ksbase + (r0 + r4) * NB);
+      skb = lds_u16(ksbase + (r0 + r4 + 8) * NB);
+    }
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      const float fa = ue8m0_f32((ska >> (8 * j)) & 0xFF), fb = ue8m0_f32((skb >> (8 * j)) & 0xFF);
+      sc[0] = fmaf(acc[j][0], fa, sc[0]);
+      sc[1] = fmaf(acc[j][1], fa, sc[1]);
+      sc[2] = fmaf(acc[j][2], fb, sc[2]);
+      sc[3] = fmaf(acc[j][3], fb, sc[3]);
+    }
+  }
+  const bool va = tb + r4 < t1, vb = tb + r4 + 8 < t1;
+  const float x0 = va ? sc[0] * sl2 : -INFINITY;  // token r4,   head 2c4
+  const float x1 = va ? sc[1] * sl2 : -INFINITY;  // token r4,   head 2c4+1
+  const float x2 = vb ? sc[2] * sl2 : -INFINITY;  // token r4+8, head 2c4
+  const float x3 = vb ? sc[3] * sl2 : -INFINITY;  // token r4+8, head 2c4+1
+  float ma = fmaxf(x0, x2), mb = fmaxf(x1, x3);
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    ma = fmaxf(ma, __shfl_xor_sync(MXG_FULL_MASK, ma, off));
+    mb = fmaxf(mb, __shfl_xor_sync(MXG_FULL_MASK, mb, off));
+  }
+  const float na = fmaxf(m_a, ma), nb = fmaxf(m_b, mb);
+  const float ua = na == -INFINITY ? 0.f : na, ub = nb == -INFINITY ? 0.f : nb;
+  const float alpha_a = exp2f(m_a - ua), alpha_b = exp2f(m_b - ub);
+  m_a = na;
+  m_b = nb;
+  const float f0 = exp2f(x0 - ua), f1 = exp2f(x1 - ub), f2 = exp2f(x2 - ua), f3 = exp2f(x3 - ub);
+  const __nv_bfloat16 p0 = __float2bfloat16_rn(f0), p1 = __float2bfloat16_rn(f1);
+  const __nv_bfloat16 p2 = __float2bfloat16_rn(f2), p3 = __float2bfloat16_rn(f3);
+  const __nv_bfloat16 q0 = __float2bfloat16_rn(f0 - __bfloat162float(p0));
+  const __nv_bfloat16 q1 = __float2bfloat16_rn(f1 - __bfloat162float(p1));
+  const __nv_bfloat16 q2 = __float2bfloat16_rn(f2 - __bfloat162float(p2));
+  const __nv_bfloat16 q3 = __float2bfloat16_rn(f3 - __bfloat162float(p3));
+  l_a = l_a * alpha_a + (f0 + f2);
+  l_b = l_b * alpha_b + (f1 + f3);
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt) {
+    o[mt][0] *= alpha_a;
+    o[mt][1] *= alpha_b;
+    o[mt][2] *= alpha_a;
+    o[mt][3] *= alpha_b;
+  }
+  ps[(2 * c4) * 16 + r4] = __bfloat16_as_ushort(p0);
+  ps[(2 * c4 + 1) * 16 + r4] = __bfloat16_as_ushort(p1);
+  ps[(2 * c4) * 16 + r4 + 8] = __bfloat16_as_ushort(p2);
+  ps[(2 * c4 + 1) * 16 + r4 + 8] = __bfloat16_as_ushort(p3);
+  pl[(2 * c4) * 16 + r4] = __bfloat16_as_ushort(q0);
+  pl[(2 * c4 + 1) * 16 + r4] = __bfloat16_as_ushort(q1);
+  pl[(2 * c4) * 16 + r4 + 8] = __bfloat16_as_ushort(q2);
+  pl[(2 * c4 + 1) * 16 + r4 + 8] = __bfloat16_as_ushort(q3);
+  // rows past the split end may hold anything; P is 0 there, and V (codes and scales) is
+  // zeroed so that a non-finite value cannot turn 0 * V into NaN
+  if (tb + 16 > t1) {
+    uint8_t* vt = ring + s * S::kCodeStageBytes + S::kTileBytes;
+    if constexpr (!kMx) {
+      for (int rr = lane >> 4; rr < 16; rr += 2) {
+        if (tb + rr >= t1) {
+          const int row = r0 + rr;
+          const int cb = (lane & 15) * 16;  // 16 lanes x 16 bytes cover 256 bytes (two 128-byte halves)
+          if (cb < D * 2) {
+            const int half = cb >> 7;
+            *reinterpret_cast<uint4*>(vt + half * (kTileTok * 128) + row * 128 + (cb & 127)) = make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
+    } else {
+      // a row's D code bytes stay inside its own D-byte span under the swizzle
+      for (int idx = lane; idx < 16 * (D / 16); idx += 32) {
+        const int rr = idx / (D / 16);
+        if (tb + rr >= t1) *reinterpret_cast<uint4*>(vt + (r0 + rr) * D + (idx % (D / 16)) * 16) = make_uint4(0, 0, 0, 0);
+      }
+      uint8_t* vst = ring + S::kScaleRingOff + s * 2 * S::kScaleTileBytes + S::kScaleTileBytes;
+      if (lane < 16 && tb + lane >= t1) {
+#pragma unroll
+        for (int j = 0; j < NB; ++j) vst[(r0 + lane) * NB + j] = 0;
+      }
+    }
+    fence_proxy_async_smem();
+  }
+  __syncwarp();
+  const uint32_t b0 = *reinterpret_cast<const uint32_t*>(ps + r4 * 16 + 2 * c4);
+  const uint32_t b1 = *reinterpret_cast<const uint32_t*>(ps + r4 * 16 + 8 + 2 * c4);
+  const uint32_t l0 = *reinterpret_cast<const uint32_t*>(pl + r4 * 16 + 2 * c4);
+  const uint32_t l1 = *reinterpret_cast<const uint32_t*>(pl + r4 * 16 + 8 + 2 * c4);
+  // O^T[D x 8] += V^T[D x 16 tok] P^T[16 tok x 8]
+  if constexpr (!kMx) {
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      uint32_t a0, a1, a2, a3;
+      ldmatrix_x4_trans(tile_addr(vbase, r0 + (lane & 7) + 8 * (lane >> 4), mt * 16 + 8 * ((lane >> 3) & 1)), a0,
+                        a1, a2, a3);
+      mma_bf16_16816(o[mt], a0, a1, a2, a3, b0, b1);
+      mma_bf16_16816(o[mt], a0, a1, a2, a3, l0, l1);
+    }
+  } else {
+    // m-tile 2j+f of block j: A row r4 is dim 32j + 4*r4 + 2f, row r4+8 is that dim + 1; the
+    // k slots are tokens 2*c4 (+1) and 2*c4 + 8 (+9), as in P^T.
+    uint32_t s01[NB], s89[NB];  // (token 2c4, 2c4+1) / (2c4+8, 2c4+9) exponent bytes of block j at bits 0 / 16
+    if constexpr (D == 128) {
+      const uint2 x01 = lds_u32x2(vsbase + (r0 + 2 * c4) * NB);
+      const uint2 x89 = lds_u32x2(vsbase + (r0 + 2 * c4 + 8) * NB);
+#pragma unroll
+      for (int j = 0; j < NB; ++j) {
+        s01[j] = __byte_perm(x01.x, x01.y, 0x0400 + j * 0x0101);
+        s89[j] = __byte_perm(x89.x, x89.y, 0x0400 + j * 0x0101);
+      }
+    } else {
+      const uint32_t x01 = lds_u32(vsbase + (r0 + 2 * c4) * NB);
+      const uint32_t x89 = lds_u32(vsbase + (r0 + 2 * c4 + 8) * NB);
+#pragma unroll
+      for (int j = 0; j < NB; ++j) {
+        s01[j] = __byte_perm(x01, 0, 0x0200 + j * 0x0101);
+        s89[j] = __byte_perm(x89, 0, 0x0200 + j * 0x0101);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      const uint32_t f01 = pscale_pair(s01[j]), f89 = pscale_pair(s89[j]);
+      const uint32_t bh0 = bmul2(b0, f01), bh1 = bmul2(b1, f89), bl0 = bmul2(l0, f01), bl1 = bmul2(l1, f89);
+      const uint32_t w0 = lds_u32(code_addr<D>(vbase, r0 + 2 * c4, 32 * j + 4 * r4));
+      const uint32_t w1 = lds_u32(code_addr<D>(vbase, r0 + 2 * c4 + 1, 32 * j + 4 * r4));
+      const uint32_t w8 = lds_u32(code_addr<D>(vbase, r0 + 2 * c4 + 8, 32 * j + 4 * r4));
+      const uint32_t w9 = lds_u32(code_addr<D>(vbase, r0 + 2 * c4 + 9, 32 * j + 4 * r4));
+      {
+        const uint32_t a0 = e4m3_pair_bf16<0>(w0, w1), a1 = e4m3_pair_bf16<1>(w0, w1);
+        const uint32_t a2 = e4m3_pair_bf16<0>(w8, w9), a3 = e4m3_pair_bf16<1>(w8, w9);
+        mma_bf16_16816(o[2 * j], a0, a1, a2, a3, bh0, bh1);
+        mma_bf16_16816(o[2 * j], a0, a1, a2, a3, bl0, bl1);
+      }
+      {
+        const uint32_t a0 = e4m3_pair_bf16<2>(w0, w1), a1 = e4m3_pair_bf16<3>(w0, w1);
+        const uint32_t a2 = e4m3_pair_bf16<2>(w8, w9), a3 = e4m3_pair_bf16<3>(w8, w9);
+        mma_bf16_16816(o[2 * j + 1], a0, a1, a2, a3, bh0, bh1);
+        mma_bf16_16816(o[2 * j + 1], a0, a1, a2, a3, bl0, bl1);
+      }
+    }
+  }
+}
+
+// Stage a consumer warp's (m, l) of its 8 (padded) heads into ml [warp][8][2] and its O of
+// heads h_lo .. h_lo + HR - 1 into os [warp][HR][D] (fp32; an MXFP8 cache's O loses its 2^-64).
+template <int D, bool kMx, int HR>
+__device__ __forceinline__ void stage_warp(float* os, float* ml, int warp, int lane, const float (&o)[D / 16][4],
+                                           float m_a, float l_a, float m_b, float l_b, int h_lo) {
+  constexpr int KS = D / 16;
+  const int c4 = lane & 3, r4 = lane >> 2;
+  const float oscale = kMx ? 0x1p64f : 1.f;
+  const int ha = 2 * c4 - h_lo, hb = ha + 1;  // this thread's two heads, relative to the round
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt) {
+    const int d = kMx ? 32 * (mt >> 1) + 4 * r4 + 2 * (mt & 1) : mt * 16 + r4;
+    const int d2 = kMx ? d + 1 : d + 8;
+    if (ha >= 0 && ha < HR) {
+      os[(warp * HR + ha) * D + d] = o[mt][0] * oscale;
+      os[(warp * HR + ha) * D + d2] = o[mt][2] * oscale;
+    }
+    if (hb >= 0 && hb < HR) {
+      os[(warp * HR + hb) * D + d] = o[mt][1] * oscale;
+      os[(warp * HR + hb) * D + d2] = o[mt][3] * oscale;
+    }
+  }
+  if (r4 == 0) {
+    ml[(warp * 8 + 2 * c4) * 2] = m_a;
+    ml[(warp * 8 + 2 * c4) * 2 + 1] = l_a;
+    ml[(warp * 8 + 2 * c4 + 1) * 2] = m_b;
+    ml[(warp * 8 + 2 * c4 + 1) * 2 + 1] = l_b;
+  }
+}
+
+// Merge the consumer warps' staged state for head h (round-relative hr) and dimension d: the
+// running maximum M, the softmax denominator L and the unnormalised output O.
+template <int D, int HR>
+__device__ __forceinline__ void merge_warps(const float* os, const float* ml, int h, int hr, int d, float& M,
+                                            float& L, float& O) {
+  M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, ml[(w * 8 + h) * 2]);
+  L = 0.f;
+  O = 0.f;
+#pragma unroll
+  for (int w = 0; w < kConsumers; ++w) {
+    const float mw = ml[(w * 8 + h) * 2];
+    const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
+    L += ml[(w * 8 + h) * 2 + 1] * f;
+    O += os[(w * HR + hr) * D + d] * f;
+  }
+}
+
 // One CTA = one (split, b, g). tmK/tmV map the K/V rows (bf16 [rows, D], or E4M3 codes
 // [rows, D] when kMx); tmKS/tmVS map the UE8M0 scales of an MXFP8 cache as 16-byte lines
 // ([rows * D/32 / 16, 16]) and are unused for bf16.
@@ -177,7 +494,6 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
                                                              const SplitParams p) {
   using S = AttnShape<D, kMx>;
   constexpr int KS = D / 16;  // k-steps of the QK^T product / m-tiles of O^T
-  constexpr int NB = D / 32;  // MX blocks per row
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
@@ -185,6 +501,9 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBodyBytes + S::kPBytes);
   uint64_t* empty = full + S::kStages;
 
+  // the test hook is written by the host alone, so it is read before the wait, where its
+  // latency overlaps the predecessor kernel and the kv_len read below
+  const int stall = *reinterpret_cast<volatile int*>(&g_stall_attn_loads);
   pdl_wait();
   pdl_trigger();
   const int split = blockIdx.x;
@@ -253,82 +572,22 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
         prefetch_tensormap(&tmVS);
       }
       const uint64_t pol = l2_policy_evict_first();
-      const int nissue = *reinterpret_cast<volatile int*>(&g_stall_attn_loads) ? 0 : ntiles;
+      const int nissue = stall ? 0 : ntiles;
       for (int i = 0; i < nissue; ++i) {
         const int s = i % S::kStages;
         if (i >= S::kStages && !mbar_wait(&empty[s], ((i / S::kStages) - 1) & 1, p.err)) break;
-        const int row = p.table ? tile_row[i] : row0 + i * kTileTok;
-        mbar_arrive_expect_tx(&full[s], S::kStageBytes);
-        uint8_t* kt = ring + s * S::kCodeStageBytes;
-        uint8_t* vt = kt + S::kTileBytes;
-        if constexpr (kMx) {
-          uint8_t* kst = ring + S::kScaleRingOff + s * 2 * S::kScaleTileBytes;
-          tma_load_2d_hint(kt, &tmK, &full[s], 0, row, pol);
-          tma_load_2d_hint(vt, &tmV, &full[s], 0, row, pol);
-          // row is a multiple of 64, so its scales start on a 16-byte line
-          const int line = row / (16 / NB);
-          tma_load_2d_hint(kst, &tmKS, &full[s], 0, line, pol);
-          tma_load_2d_hint(kst + S::kScaleTileBytes, &tmVS, &full[s], 0, line, pol);
-        } else {
-#pragma unroll
-          for (int h = 0; h < S::kHalves; ++h) {
-            tma_load_2d_hint(kt + h * kTileTok * 128, &tmK, &full[s], h * 64, row, pol);
-            tma_load_2d_hint(vt + h * kTileTok * 128, &tmV, &full[s], h * 64, row, pol);
-          }
-        }
+        issue_tile<D, kMx>(ring, s, p.table ? tile_row[i] : row0 + i * kTileTok, &full[s], &tmK, &tmV, &tmKS, &tmVS,
+                           pol);
       }
     }
     return;
   }
 
   // --------------------------------------------------------------- consumers
-  const int c4 = lane & 3, r4 = lane >> 2;
   const int h0 = g * p.group;
-  // B fragments of Q^T (k = dim, n = head); lane holds head r4.
-  //  bf16 cache: k-step ks, dims ks*16 + 2*c4 (+1) and +8 (+9).
-  //  MXFP8 cache: k-steps 2j, 2j+1 cover MX block j; the thread's k slots of step 2j+e hold
-  //  dims 32j + 8*c4 + 4e + {0, 1} and + {2, 3} (the K fragments below use the same order, so
-  //  the dot product is unchanged), as f16 after scaling q by 2^qa.
   uint32_t qb[KS][2];
-  float sl2 = p.scale_log2;
-  {
-    const bool hv = r4 < p.group;
-    const uint16_t* qh = p.q + (int64_t)b * p.ld_q + (int64_t)(h0 + (hv ? r4 : 0)) * D;
-    if constexpr (!kMx) {
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        qb[ks][0] = hv ? *reinterpret_cast<const uint32_t*>(qh + ks * 16 + 2 * c4) : 0u;
-        qb[ks][1] = hv ? *reinterpret_cast<const uint32_t*>(qh + ks * 16 + 8 + 2 * c4) : 0u;
-      }
-    } else {
-      uint4 qw[NB];
-      float am = 0.f;
-#pragma unroll
-      for (int j = 0; j < NB; ++j) {
-        qw[j] = hv ? *reinterpret_cast<const uint4*>(qh + 32 * j + 8 * c4) : make_uint4(0, 0, 0, 0);
-        const uint32_t w[4] = {qw[j].x, qw[j].y, qw[j].z, qw[j].w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) am = fmaxf(am, fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
-      }
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) am = fmaxf(am, __shfl_xor_sync(MXG_FULL_MASK, am, off));
-      // 2^qa brings the group's largest |q| into [2^14, 2^15): every bf16 q is then an f16 exactly
-      // unless it sits 2^38 below that maximum
-      int qa = 0;
-      if (am > 0.f) qa = min(100, max(-100, 14 - ((int)((__float_as_uint(am) >> 23) & 0xFF) - 127)));
-      const float f = __uint_as_float((uint32_t)(qa + 127) << 23);
-#pragma unroll
-      for (int j = 0; j < NB; ++j) {
-        const uint32_t w[4] = {qw[j].x, qw[j].y, qw[j].z, qw[j].w};
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          qb[2 * j + e][0] = pack_f16x2(bf16_lo(w[2 * e]) * f, bf16_hi(w[2 * e]) * f);
-          qb[2 * j + e][1] = pack_f16x2(bf16_lo(w[2 * e + 1]) * f, bf16_hi(w[2 * e + 1]) * f);
-        }
-      }
-      sl2 = p.scale_log2 * __uint_as_float((uint32_t)(127 - qa) << 23);
-    }
-  }
+  float sl2;
+  load_q_frags<D, kMx>(p.q, p.ld_q, b, h0, p.group, p.scale_log2, lane, qb, sl2);
   float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
   float o[KS][4];
 #pragma unroll
@@ -344,182 +603,7 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
       ok = false;
       break;
     }
-    const uint32_t kbase = smem_u32(ring + s * S::kCodeStageBytes);
-    const uint32_t vbase = kbase + S::kTileBytes;
-    const uint32_t ksbase = smem_u32(ring + S::kScaleRingOff + s * 2 * S::kScaleTileBytes);
-    const uint32_t vsbase = ksbase + S::kScaleTileBytes;
-    const int tb = t0 + i * kTileTok + r0;  // first token of this warp's 16 rows
-
-    // S^T[16 tok x 8 heads] = K[16 x D] Q^T[D x 8]
-    float sc[4] = {0.f, 0.f, 0.f, 0.f};
-    if constexpr (!kMx) {
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        uint32_t a0, a1, a2, a3;
-        ldmatrix_x4(tile_addr(kbase, r0 + (lane & 7) + 8 * ((lane >> 3) & 1), ks * 16 + 8 * (lane >> 4)), a0, a1,
-                    a2, a3);
-        mma_bf16_16816(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-      }
-    } else {
-      float acc[NB][4];
-#pragma unroll
-      for (int j = 0; j < NB; ++j) {
-        acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-        const uint2 ka = lds_u32x2(code_addr<D>(kbase, r0 + r4, 32 * j + 8 * c4));
-        const uint2 kb = lds_u32x2(code_addr<D>(kbase, r0 + r4 + 8, 32 * j + 8 * c4));
-        uint32_t a0, a1, a2, a3;
-        e4m3x4_to_f16(ka.x, a0, a2);
-        e4m3x4_to_f16(kb.x, a1, a3);
-        mma_f16_16816(acc[j], a0, a1, a2, a3, qb[2 * j][0], qb[2 * j][1]);
-        e4m3x4_to_f16(ka.y, a0, a2);
-        e4m3x4_to_f16(kb.y, a1, a3);
-        mma_f16_16816(acc[j], a0, a1, a2, a3, qb[2 * j + 1][0], qb[2 * j + 1][1]);
-      }
-      // per-block exponents of tokens r4 and r4+8
-      uint32_t ska, skb;
-      if constexpr (D == 128) {
-        ska = lds_u32(ksbase + (r0 + r4) * NB);
-        skb = lds_u32(ksbase + (r0 + r4 + 8) * NB);
-      } else {
-        ska = lds_u16(ksbase + (r0 + r4) * NB);
-        skb = lds_u16(ksbase + (r0 + r4 + 8) * NB);
-      }
-#pragma unroll
-      for (int j = 0; j < NB; ++j) {
-        const float fa = ue8m0_f32((ska >> (8 * j)) & 0xFF), fb = ue8m0_f32((skb >> (8 * j)) & 0xFF);
-        sc[0] = fmaf(acc[j][0], fa, sc[0]);
-        sc[1] = fmaf(acc[j][1], fa, sc[1]);
-        sc[2] = fmaf(acc[j][2], fb, sc[2]);
-        sc[3] = fmaf(acc[j][3], fb, sc[3]);
-      }
-    }
-    const bool va = tb + r4 < t1, vb = tb + r4 + 8 < t1;
-    const float x0 = va ? sc[0] * sl2 : -INFINITY;  // token r4,   head 2c4
-    const float x1 = va ? sc[1] * sl2 : -INFINITY;  // token r4,   head 2c4+1
-    const float x2 = vb ? sc[2] * sl2 : -INFINITY;  // token r4+8, head 2c4
-    const float x3 = vb ? sc[3] * sl2 : -INFINITY;  // token r4+8, head 2c4+1
-    float ma = fmaxf(x0, x2), mb = fmaxf(x1, x3);
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      ma = fmaxf(ma, __shfl_xor_sync(MXG_FULL_MASK, ma, off));
-      mb = fmaxf(mb, __shfl_xor_sync(MXG_FULL_MASK, mb, off));
-    }
-    const float na = fmaxf(m_a, ma), nb = fmaxf(m_b, mb);
-    const float ua = na == -INFINITY ? 0.f : na, ub = nb == -INFINITY ? 0.f : nb;
-    const float alpha_a = exp2f(m_a - ua), alpha_b = exp2f(m_b - ub);
-    m_a = na;
-    m_b = nb;
-    const float f0 = exp2f(x0 - ua), f1 = exp2f(x1 - ub), f2 = exp2f(x2 - ua), f3 = exp2f(x3 - ub);
-    const __nv_bfloat16 p0 = __float2bfloat16_rn(f0), p1 = __float2bfloat16_rn(f1);
-    const __nv_bfloat16 p2 = __float2bfloat16_rn(f2), p3 = __float2bfloat16_rn(f3);
-    const __nv_bfloat16 q0 = __float2bfloat16_rn(f0 - __bfloat162float(p0));
-    const __nv_bfloat16 q1 = __float2bfloat16_rn(f1 - __bfloat162float(p1));
-    const __nv_bfloat16 q2 = __float2bfloat16_rn(f2 - __bfloat162float(p2));
-    const __nv_bfloat16 q3 = __float2bfloat16_rn(f3 - __bfloat162float(p3));
-    l_a = l_a * alpha_a + (f0 + f2);
-    l_b = l_b * alpha_b + (f1 + f3);
-#pragma unroll
-    for (int mt = 0; mt < KS; ++mt) {
-      o[mt][0] *= alpha_a;
-      o[mt][1] *= alpha_b;
-      o[mt][2] *= alpha_a;
-      o[mt][3] *= alpha_b;
-    }
-    ps[(2 * c4) * 16 + r4] = __bfloat16_as_ushort(p0);
-    ps[(2 * c4 + 1) * 16 + r4] = __bfloat16_as_ushort(p1);
-    ps[(2 * c4) * 16 + r4 + 8] = __bfloat16_as_ushort(p2);
-    ps[(2 * c4 + 1) * 16 + r4 + 8] = __bfloat16_as_ushort(p3);
-    pl[(2 * c4) * 16 + r4] = __bfloat16_as_ushort(q0);
-    pl[(2 * c4 + 1) * 16 + r4] = __bfloat16_as_ushort(q1);
-    pl[(2 * c4) * 16 + r4 + 8] = __bfloat16_as_ushort(q2);
-    pl[(2 * c4 + 1) * 16 + r4 + 8] = __bfloat16_as_ushort(q3);
-    // rows past the split end may hold anything; P is 0 there, and V (codes and scales) is
-    // zeroed so that a non-finite value cannot turn 0 * V into NaN
-    if (tb + 16 > t1) {
-      uint8_t* vt = ring + s * S::kCodeStageBytes + S::kTileBytes;
-      if constexpr (!kMx) {
-        for (int rr = lane >> 4; rr < 16; rr += 2) {
-          if (tb + rr >= t1) {
-            const int row = r0 + rr;
-            const int cb = (lane & 15) * 16;  // 16 lanes x 16 bytes cover 256 bytes (two 128-byte halves)
-            if (cb < D * 2) {
-              const int half = cb >> 7;
-              *reinterpret_cast<uint4*>(vt + half * (kTileTok * 128) + row * 128 + (cb & 127)) = make_uint4(0, 0, 0, 0);
-            }
-          }
-        }
-      } else {
-        // a row's D code bytes stay inside its own D-byte span under the swizzle
-        for (int idx = lane; idx < 16 * (D / 16); idx += 32) {
-          const int rr = idx / (D / 16);
-          if (tb + rr >= t1) *reinterpret_cast<uint4*>(vt + (r0 + rr) * D + (idx % (D / 16)) * 16) = make_uint4(0, 0, 0, 0);
-        }
-        uint8_t* vst = ring + S::kScaleRingOff + s * 2 * S::kScaleTileBytes + S::kScaleTileBytes;
-        if (lane < 16 && tb + lane >= t1) {
-#pragma unroll
-          for (int j = 0; j < NB; ++j) vst[(r0 + lane) * NB + j] = 0;
-        }
-      }
-      fence_proxy_async_smem();
-    }
-    __syncwarp();
-    const uint32_t b0 = *reinterpret_cast<const uint32_t*>(ps + r4 * 16 + 2 * c4);
-    const uint32_t b1 = *reinterpret_cast<const uint32_t*>(ps + r4 * 16 + 8 + 2 * c4);
-    const uint32_t l0 = *reinterpret_cast<const uint32_t*>(pl + r4 * 16 + 2 * c4);
-    const uint32_t l1 = *reinterpret_cast<const uint32_t*>(pl + r4 * 16 + 8 + 2 * c4);
-    // O^T[D x 8] += V^T[D x 16 tok] P^T[16 tok x 8]
-    if constexpr (!kMx) {
-#pragma unroll
-      for (int mt = 0; mt < KS; ++mt) {
-        uint32_t a0, a1, a2, a3;
-        ldmatrix_x4_trans(tile_addr(vbase, r0 + (lane & 7) + 8 * (lane >> 4), mt * 16 + 8 * ((lane >> 3) & 1)), a0,
-                          a1, a2, a3);
-        mma_bf16_16816(o[mt], a0, a1, a2, a3, b0, b1);
-        mma_bf16_16816(o[mt], a0, a1, a2, a3, l0, l1);
-      }
-    } else {
-      // m-tile 2j+f of block j: A row r4 is dim 32j + 4*r4 + 2f, row r4+8 is that dim + 1; the
-      // k slots are tokens 2*c4 (+1) and 2*c4 + 8 (+9), as in P^T.
-      uint32_t s01[NB], s89[NB];  // (token 2c4, 2c4+1) / (2c4+8, 2c4+9) exponent bytes of block j at bits 0 / 16
-      if constexpr (D == 128) {
-        const uint2 x01 = lds_u32x2(vsbase + (r0 + 2 * c4) * NB);
-        const uint2 x89 = lds_u32x2(vsbase + (r0 + 2 * c4 + 8) * NB);
-#pragma unroll
-        for (int j = 0; j < NB; ++j) {
-          s01[j] = __byte_perm(x01.x, x01.y, 0x0400 + j * 0x0101);
-          s89[j] = __byte_perm(x89.x, x89.y, 0x0400 + j * 0x0101);
-        }
-      } else {
-        const uint32_t x01 = lds_u32(vsbase + (r0 + 2 * c4) * NB);
-        const uint32_t x89 = lds_u32(vsbase + (r0 + 2 * c4 + 8) * NB);
-#pragma unroll
-        for (int j = 0; j < NB; ++j) {
-          s01[j] = __byte_perm(x01, 0, 0x0200 + j * 0x0101);
-          s89[j] = __byte_perm(x89, 0, 0x0200 + j * 0x0101);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < NB; ++j) {
-        const uint32_t f01 = pscale_pair(s01[j]), f89 = pscale_pair(s89[j]);
-        const uint32_t bh0 = bmul2(b0, f01), bh1 = bmul2(b1, f89), bl0 = bmul2(l0, f01), bl1 = bmul2(l1, f89);
-        const uint32_t w0 = lds_u32(code_addr<D>(vbase, r0 + 2 * c4, 32 * j + 4 * r4));
-        const uint32_t w1 = lds_u32(code_addr<D>(vbase, r0 + 2 * c4 + 1, 32 * j + 4 * r4));
-        const uint32_t w8 = lds_u32(code_addr<D>(vbase, r0 + 2 * c4 + 8, 32 * j + 4 * r4));
-        const uint32_t w9 = lds_u32(code_addr<D>(vbase, r0 + 2 * c4 + 9, 32 * j + 4 * r4));
-        {
-          const uint32_t a0 = e4m3_pair_bf16<0>(w0, w1), a1 = e4m3_pair_bf16<1>(w0, w1);
-          const uint32_t a2 = e4m3_pair_bf16<0>(w8, w9), a3 = e4m3_pair_bf16<1>(w8, w9);
-          mma_bf16_16816(o[2 * j], a0, a1, a2, a3, bh0, bh1);
-          mma_bf16_16816(o[2 * j], a0, a1, a2, a3, bl0, bl1);
-        }
-        {
-          const uint32_t a0 = e4m3_pair_bf16<2>(w0, w1), a1 = e4m3_pair_bf16<3>(w0, w1);
-          const uint32_t a2 = e4m3_pair_bf16<2>(w8, w9), a3 = e4m3_pair_bf16<3>(w8, w9);
-          mma_bf16_16816(o[2 * j + 1], a0, a1, a2, a3, bh0, bh1);
-          mma_bf16_16816(o[2 * j + 1], a0, a1, a2, a3, bl0, bl1);
-        }
-      }
-    }
+    consume_tile<D, kMx>(ring, s, t0 + i * kTileTok + r0, t1, r0, lane, qb, sl2, m_a, m_b, l_a, l_b, o, ps, pl);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
   }
@@ -556,38 +640,14 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
     }
     return;
   }
-  float* os = reinterpret_cast<float*>(ring);                 // [warp][8 heads][D]
-  float* ml = os + kConsumers * 8 * D;                         // [warp][8 heads][m, l]
-  const float oscale = kMx ? 0x1p64f : 1.f;                    // MXFP8 V: O carried 2^-64
-#pragma unroll
-  for (int mt = 0; mt < KS; ++mt) {
-    const int d = kMx ? 32 * (mt >> 1) + 4 * r4 + 2 * (mt & 1) : mt * 16 + r4;
-    const int d2 = kMx ? d + 1 : d + 8;
-    os[(warp * 8 + 2 * c4) * D + d] = o[mt][0] * oscale;
-    os[(warp * 8 + 2 * c4 + 1) * D + d] = o[mt][1] * oscale;
-    os[(warp * 8 + 2 * c4) * D + d2] = o[mt][2] * oscale;
-    os[(warp * 8 + 2 * c4 + 1) * D + d2] = o[mt][3] * oscale;
-  }
-  if (r4 == 0) {
-    ml[(warp * 8 + 2 * c4) * 2] = m_a;
-    ml[(warp * 8 + 2 * c4) * 2 + 1] = l_a;
-    ml[(warp * 8 + 2 * c4 + 1) * 2] = m_b;
-    ml[(warp * 8 + 2 * c4 + 1) * 2 + 1] = l_b;
-  }
+  float* os = reinterpret_cast<float*>(ring);  // [warp][8 heads][D]
+  float* ml = os + kConsumers * 8 * D;         // [warp][8 heads][m, l]
+  stage_warp<D, kMx, 8>(os, ml, warp, lane, o, m_a, l_a, m_b, l_b, 0);
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
   for (int idx = threadIdx.x; idx < p.group * D; idx += kConsumers * 32) {
     const int h = idx / D, d = idx - h * D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, ml[(w * 8 + h) * 2]);
-    float L = 0.f, O = 0.f;
-#pragma unroll
-    for (int w = 0; w < kConsumers; ++w) {
-      const float mw = ml[(w * 8 + h) * 2];
-      const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
-      L += ml[(w * 8 + h) * 2 + 1] * f;
-      O += os[(w * 8 + h) * D + d] * f;
-    }
+    float M, L, O;
+    merge_warps<D, 8>(os, ml, h, h, d, M, L, O);
     const int64_t bh = (int64_t)b * p.Hq + h0 + h;
     if (p.max_splits == 1) {
       const __nv_bfloat16 ob = __float2bfloat16_rn(O / L);
@@ -649,11 +709,14 @@ cudaError_t set_attn_load_stall(int on) {
 }
 
 int attn_chunk(int64_t bs, int64_t Hkv, int64_t max_kv_len) {
-  // aim for ~3000 (b, g, split) work items at the bound, 64..1024 tokens per split
-  int64_t c = (bs * Hkv * max_kv_len + 2999) / 3000;
+  // Splits of 768 tokens (12 tiles); below ~128 (split, b, g) items at the bound (a few
+  // sequences), shorter splits so that at least that many CTAs stream. Measured on GB300 at
+  // 32/8 heads, kv_len ~ U[234, 4096]: 768-token splits were the fastest of 256..1024 for
+  // bs = 8..64; 256 for bs = 1.
+  int64_t c = (bs * Hkv * max_kv_len + kMinSplitItems - 1) / kMinSplitItems;
   c = (c + kTileTok - 1) / kTileTok * kTileTok;
   if (c < kTileTok) c = kTileTok;
-  if (c > kMaxSplitTiles * kTileTok) c = kMaxSplitTiles * kTileTok;
+  if (c > kSplitTok) c = kSplitTok;
   return (int)c;
 }
 
