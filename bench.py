@@ -978,6 +978,50 @@ def run_reference(args, rank, world):
 
 
 # --------------------------------------------------------------------------- main
+def run_timeline(args):
+    """The decode-layer step's CUDA graph on the instrumented library (libmxg_tl.so): per-launch
+    device timeline (first entry, first return from the programmatic wait, last exit), medians
+    over the timed steps, each step L2-flushed like the bench's."""
+    import torch
+
+    from mxfp8_mlp_gqa_gb300 import api, build as _build, synth, timeline
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    lib = api.lib(_build.build(timeline=True))
+    total_steps = args.warmup + args.steps
+    sched, _refill = synth.slot_schedule(BS, total_steps + 1, KV_LO, KV_HI, LIFE_HI, seed=0)
+    L = build_layer(dev, int(sched.max()))
+    sched_d = torch.from_numpy(sched).to(dev)
+    rec = timeline.Recorder(lib)
+    flush = L2Flush(dev)
+    L.kv_len.copy_(sched_d[0])
+    L.step()
+    torch.cuda.synchronize()
+    plain = L.capture()
+    for s in range(args.warmup):
+        L.kv_len.copy_(sched_d[s])
+        plain.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    steps, ms = [], []
+    for i in range(args.steps):
+        L.kv_len.copy_(sched_d[args.warmup + i])
+        flush()
+        torch.cuda.synchronize()
+        rec.reset()
+        e0.record()
+        plain.replay()
+        e1.record()
+        e1.synchronize()
+        ms.append(e0.elapsed_time(e1))
+        steps.append(rec.records())
+    summ = timeline.summarize(steps)
+    print(f"instrumented step: {statistics.median(ms) * 1e3:.1f} us (event-timed median of {args.steps})")
+    print(timeline.format_table(summ))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -990,6 +1034,9 @@ def main(argv=None):
     ap.add_argument("--profile", default=None,
                     help="run one kernel family only (for ncu captures): mlp:<M> | attn:<bs>[:<cap>] | "
                          "gemm:<M>x<N>x<K> | cublas:<M>x<N>x<K> (library kernel, context)")
+    ap.add_argument("--timeline", action="store_true",
+                    help="print the decode step's per-launch device timeline from the instrumented library "
+                         "(libmxg_tl.so) instead of the JSON line")
     args = ap.parse_args(argv)
     if args.cpu_case:  # child process of run_cpu_cases: one oracle timing, no GPU
         print(json.dumps(cpu_case(args.cpu_case)))
@@ -1006,6 +1053,8 @@ def main(argv=None):
 
     import torch
 
+    if args.timeline:
+        return run_timeline(args)
     if args.profile:
         print(json.dumps(run_profile(args)))
         return 0

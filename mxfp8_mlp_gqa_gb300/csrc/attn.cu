@@ -503,8 +503,10 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
 
   // the test hook is written by the host alone, so it is read before the wait, where its
   // latency overlaps the predecessor kernel and the kv_len read below
+  MXG_TL_SCOPE(kTlSplitAttn);
   const int stall = *reinterpret_cast<volatile int*>(&g_stall_attn_loads);
   pdl_wait();
+  MXG_TL_WAITED();
   pdl_trigger();
   const int split = blockIdx.x;
   const int bg = blockIdx.y;
@@ -603,10 +605,12 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
       ok = false;
       break;
     }
+    MXG_TL_MARK1();  // timeline: first tile landed
     consume_tile<D, kMx>(ring, s, t0 + i * kTileTok + r0, t1, r0, lane, qb, sl2, m_a, m_b, l_a, l_b, o, ps, pl);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
   }
+  MXG_TL_MARK2();  // timeline: last tile consumed
   // A warp whose wait ran out still meets the other consumer warps at the named barrier below
   // (leaving would hold them there for good): it publishes the failure before the barrier, and
   // all consumer warps leave together after it.
@@ -669,7 +673,9 @@ __global__ void __launch_bounds__(D) gqa_combine_kernel(const float* __restrict_
                                                         int chunk, int max_splits, int max_kv_len,
                                                         uint16_t* __restrict__ out, uint8_t* __restrict__ oq,
                                                         uint8_t* __restrict__ os) {
+  MXG_TL_SCOPE(kTlCombine);
   pdl_wait();
+  MXG_TL_WAITED();
   pdl_trigger();
   const int64_t bh = blockIdx.x;
   const int b = (int)(bh / Hq);
@@ -802,3 +808,5 @@ cudaError_t launch_gqa_decode_attn_kv_mx(const CUtensorMap& tmK, const CUtensorM
 }
 
 }  // namespace mxg
+
+MXG_TL_UNIT(attn)

@@ -84,6 +84,88 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // after this the waiting thread records MXG_ETIMEOUT and the kernel winds down.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
+// ------------------------------------------------------------------ optional device timeline
+// Compiled in only with -DMXG_TIMELINE (a separate, instrumented build of the library; the
+// production library holds none of it). Lane 0 of every warp of an instrumented kernel appends
+// one record {kernel id << 48 | linear block << 16 | warp, entry, return from the programmatic
+// wait (0 if the warp does not wait), exit, mark 1, mark 2} in globaltimer ns to the buffer
+// attached through
+// the translation unit's mxg_tl_attach_<unit> entry point. The buffer has one region of `cap`
+// records per SM, each with its own counter (one shared counter would serialise thousands of
+// warps leaving at once); records past a region's end are dropped.
+#ifdef MXG_TIMELINE
+namespace tl {
+static __device__ unsigned long long* g_buf;
+static __device__ unsigned int* g_cnt;
+static __device__ unsigned int g_cap;
+constexpr unsigned kRec = 6;  // u64 per record
+struct Scope {
+  unsigned long long t0, tw, m1, m2;
+  unsigned id;
+  __device__ explicit Scope(unsigned kid) : t0(globaltimer_ns()), tw(0), m1(0), m2(0), id(kid) {}
+  __device__ void waited() { tw = globaltimer_ns(); }
+  // kernel-specific phase points: mark 1 keeps its first time, mark 2 its last
+  __device__ void mark1() {
+    if (!m1) m1 = globaltimer_ns();
+  }
+  __device__ void mark2() { m2 = globaltimer_ns(); }
+  __device__ ~Scope() {
+    if ((threadIdx.x & 31) || !g_buf) return;
+    unsigned sm;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+    const unsigned i = atomicAdd(g_cnt + sm, 1u);
+    if (i >= g_cap) return;
+    const unsigned long long blk = ((unsigned long long)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+    unsigned long long* r = g_buf + kRec * ((unsigned long long)sm * g_cap + i);
+    r[0] = ((unsigned long long)id << 48) | (blk << 16) | (threadIdx.x >> 5);
+    r[1] = t0;
+    r[2] = tw;
+    r[3] = globaltimer_ns();
+    r[4] = m1;
+    r[5] = m2;
+  }
+};
+}  // namespace tl
+#define MXG_TL_SCOPE(id) ::mxg::tl::Scope mxg_tl_scope_(id)
+#define MXG_TL_WAITED() mxg_tl_scope_.waited()
+#define MXG_TL_MARK1() mxg_tl_scope_.mark1()
+#define MXG_TL_MARK2() mxg_tl_scope_.mark2()
+#define MXG_TL_UNIT(name)                                                                            \
+  extern "C" cudaError_t mxg_tl_attach_##name(void* buf, void* cnt, unsigned cap) {                  \
+    cudaError_t e = cudaMemcpyToSymbol(::mxg::tl::g_buf, &buf, sizeof(buf));                         \
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(::mxg::tl::g_cnt, &cnt, sizeof(cnt));               \
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(::mxg::tl::g_cap, &cap, sizeof(cap));               \
+    return e;                                                                                        \
+  }
+#else
+#define MXG_TL_SCOPE(id) \
+  do {                   \
+  } while (0)
+#define MXG_TL_WAITED() \
+  do {                  \
+  } while (0)
+#define MXG_TL_MARK1() \
+  do {                 \
+  } while (0)
+#define MXG_TL_MARK2() \
+  do {                 \
+  } while (0)
+#define MXG_TL_UNIT(name)
+#endif
+// kernel ids of the timeline records
+constexpr unsigned kTlMaxSm = 256;  // regions (and counters) of the timeline buffer
+enum TlKernel : unsigned {
+  kTlQuantize = 1,
+  kTlRmsQuant = 2,
+  kTlShift = 3,
+  kTlCopy16 = 4,
+  kTlKvAppend = 5,
+  kTlSplitAttn = 6,
+  kTlCombine = 7,
+  kTlGemmTc = 16,  // + epilogue kind
+  kTlGemmTc2 = 24,
+};
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }

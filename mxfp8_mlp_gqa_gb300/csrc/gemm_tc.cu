@@ -139,24 +139,34 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Shared::cluster address of the object at `local`'s offset in CTA `rank`'s shared memory.
+__device__ __forceinline__ uint32_t mapa_shared(const void* local, uint32_t rank) {
+  uint32_t raddr;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(smem_u32(local)), "r"(rank));
+  return raddr;
+}
+
 // 4 x fp32 from the shared memory of CTA `rank` of this cluster, at the offset that `local`
-// (16-byte aligned) has in this CTA's shared memory.
+// (16-byte aligned) has in this CTA's shared memory. Only read between the two cluster
+// barriers of the split-K reduction, where the staged partials do not change: volatile keeps
+// the loads between those barriers, and without a memory clobber the compiler may issue the
+// loads of several output groups before the global stores of the first.
 __device__ __forceinline__ float4 ld_dsmem_f32x4(const float* local, uint32_t rank) {
   uint32_t raddr;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(smem_u32(local)), "r"(rank));
   float4 v;
   asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(raddr)
-               : "memory");
+               : "r"(raddr));
   return v;
 }
 
 }  // namespace
 
 template <int BN, int EPI>
-__global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW,
+__global__ void __launch_bounds__(192, 1) mx_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW,
                                                             const __grid_constant__ CUtensorMap tmX, const TcArgs a) {
+  MXG_TL_SCOPE(kTlGemmTc + EPI);
   using S = TcShape<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -195,6 +205,21 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_sh;
   const uint32_t t_d = tmem;
+  // split-K reduction work of an epilogue thread (filled by the epilogue warps, see below)
+  constexpr int kNJ = EPI == kEpiSplit && BN <= 128 ? (BN / 8 > 0 ? BN / 8 : 1) : 1;
+  constexpr bool kBatched = EPI == kEpiSplit && BN <= 128;
+  const int S_ = a.splits;
+  const int rb = 4 * ((split * 32) / (S_ > 0 ? S_ : 1));
+  const int nq = ((split + 1) * 32) / (S_ > 0 ? S_ : 1) - (split * 32) / (S_ > 0 ? S_ : 1);
+  uint16_t* dst[kNJ];
+  uint2 rv[kNJ];
+  int sidx[kNJ];
+#pragma unroll
+  for (int j = 0; j < kNJ; ++j) {
+    dst[j] = nullptr;
+    rv[j] = make_uint2(0u, 0u);
+    sidx[j] = 0;
+  }
 
   if (warp == 0) {
     // ----------------------------------------------------------------- producer
@@ -216,6 +241,7 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
       }
     }
     pdl_wait();
+    MXG_TL_WAITED();
     // the next kernel may start its own weight prefetch only once the previous one is complete
     pdl_trigger();
     for (int i = 0; i < ng; ++i) {
@@ -267,6 +293,7 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
       for (int i = 0; i < ng; ++i) {
         const int s = i % S::kStages;
         if (!mbar_wait(&full[s], (i / S::kStages) & 1, a.err)) break;
+        MXG_TL_MARK1();  // timeline: first stage landed
         if (!a.wsp) fence_proxy_async_smem();  // cp.async (generic proxy) scale words -> tcgen05.cp (async proxy)
         tc::fence_after_sync();
         const uint32_t t_sfa = tmem + BN + (uint32_t)((i % S::kSfSlots) * S::kSfCols), t_sfb = t_sfa + 4;
@@ -283,6 +310,7 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
         tc::commit(&empty[s]);
       }
       tc::commit(tmem_full);
+      MXG_TL_MARK2();  // timeline: last MMA issued
     }
     __syncwarp();
   } else {
@@ -290,8 +318,33 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
     const int q = warp & 3;  // the TMEM lane quadrant this warp may read
     const int r = 32 * q + lane;
     pdl_wait();  // outputs and the residual are touched only after the previous kernel is done
+    MXG_TL_WAITED();
+    // Split-K (BN <= 128): CTA z of the cluster owns the 4-row groups [z*32/S, (z+1)*32/S) of
+    // the 128-row tile; an epilogue thread takes groups e = tid - 64 + 128 j of them (nq <= 16
+    // groups per token for S >= 2, so j < BN/8). Their destinations (for the K/V columns of a
+    // fused QKV projection a kv_len read) and residuals are inputs from upstream: they are read
+    // here, right after the programmatic wait, while the MMAs still run.
+    if (kBatched) {
+      int mj[kNJ], nj[kNJ];
+#pragma unroll
+      for (int j = 0; j < kNJ; ++j) {
+        const int e = threadIdx.x - 64 + 128 * j;
+        const int c = e / nq, rr = rb + 4 * (e - c * nq);
+        mj[j] = -1;
+        nj[j] = n0 + rr;
+        sidx[j] = c * S::kRS + rr;
+        if (e < BN * nq && m0 + c < a.M && nj[j] < a.N) mj[j] = m0 + c;
+      }
+#pragma unroll
+      for (int j = 0; j < kNJ; ++j)
+        if (mj[j] >= 0 && a.residual) rv[j] = *reinterpret_cast<const uint2*>(a.residual + (int64_t)mj[j] * a.N + nj[j]);
+#pragma unroll
+      for (int j = 0; j < kNJ; ++j)
+        if (mj[j] >= 0) dst[j] = out_ptr(a, mj[j], nj[j]);  // 4 consecutive columns never straddle a head
+    }
     // warp-uniform outcome: the SwiGLU epilogue below shuffles with the full mask
     const bool ok = __all_sync(MXG_FULL_MASK, mbar_wait(tmem_full, 0, a.err));
+    MXG_TL_MARK1();  // timeline: accumulator complete
     tc::fence_after_sync();
     const uint32_t trow = t_d + ((uint32_t)(32 * q) << 16);
     if (EPI == kEpiStore) {
@@ -381,43 +434,72 @@ __global__ void __launch_bounds__(192) mx_gemm_tc_kernel(const __grid_constant__
   }
   if (EPI == kEpiSplit) {
     cluster_sync_all();  // every CTA of the cluster has staged its partial tile
-    if (warp >= 2) {
-      // CTA z of the cluster owns the 4-row groups [z*32/S, (z+1)*32/S) of the 128-row tile
-      const int S_ = a.splits;
-      const int rb = 4 * ((split * 32) / S_), nq = ((split + 1) * 32) / S_ - (split * 32) / S_;
+    MXG_TL_MARK2();      // timeline: partial tiles staged cluster-wide
+    if (kBatched && warp >= 2) {
+      // split by split: the partials of all of the thread's groups are loaded before they are
+      // added, so the remote loads overlap (summation order per element: split 0, 1, ...)
+      const float* stg = reinterpret_cast<const float*>(ring);
+      float4 y[kNJ];
+#pragma unroll
+      for (int j = 0; j < kNJ; ++j) y[j] = dst[j] ? ld_dsmem_f32x4(&stg[sidx[j]], 0u) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int z = 1; z < S_; ++z) {
+        float4 p[kNJ];
+#pragma unroll
+        for (int j = 0; j < kNJ; ++j) p[j] = dst[j] ? ld_dsmem_f32x4(&stg[sidx[j]], (uint32_t)z) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < kNJ; ++j) {
+          y[j].x += p[j].x;
+          y[j].y += p[j].y;
+          y[j].z += p[j].z;
+          y[j].w += p[j].w;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kNJ; ++j) {
+        if (!dst[j]) continue;
+        float4 v = y[j];
+        if (a.residual) {
+          v.x += bf16_lo(rv[j].x);
+          v.y += bf16_hi(rv[j].x);
+          v.z += bf16_lo(rv[j].y);
+          v.w += bf16_hi(rv[j].y);
+        }
+        uint2 ov;
+        ov.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.x)) |
+               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.y)) << 16);
+        ov.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.z)) |
+               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.w)) << 16);
+        *reinterpret_cast<uint2*>(dst[j]) = ov;
+      }
+    }
+    if (!kBatched && warp >= 2) {
       const float* stg = reinterpret_cast<const float*>(ring);
       for (int e = threadIdx.x - 64; e < BN * nq; e += 128) {
         const int c = e / nq, rr = rb + 4 * (e - c * nq);
         const int m = m0 + c, n = n0 + rr;
         if (m >= a.M || n >= a.N) continue;
-        float4 part[8];
-#pragma unroll
-        for (int z = 0; z < 8; ++z)
-          if (z < S_) part[z] = ld_dsmem_f32x4(&stg[c * S::kRS + rr], (uint32_t)z);
-        float4 y = part[0];
-#pragma unroll
-        for (int z = 1; z < 8; ++z)
-          if (z < S_) {
-            y.x += part[z].x;
-            y.y += part[z].y;
-            y.z += part[z].z;
-            y.w += part[z].w;
-          }
-        const int64_t o = (int64_t)m * a.N + n;
+        float4 v = ld_dsmem_f32x4(&stg[c * S::kRS + rr], 0u);
+        for (int z = 1; z < S_; ++z) {
+          const float4 p = ld_dsmem_f32x4(&stg[c * S::kRS + rr], (uint32_t)z);
+          v.x += p.x;
+          v.y += p.y;
+          v.z += p.z;
+          v.w += p.w;
+        }
         if (a.residual) {
-          const uint2 rv = *reinterpret_cast<const uint2*>(a.residual + o);
-          y.x += bf16_lo(rv.x);
-          y.y += bf16_hi(rv.x);
-          y.z += bf16_lo(rv.y);
-          y.w += bf16_hi(rv.y);
+          const uint2 r2 = *reinterpret_cast<const uint2*>(a.residual + (int64_t)m * a.N + n);
+          v.x += bf16_lo(r2.x);
+          v.y += bf16_hi(r2.x);
+          v.z += bf16_lo(r2.y);
+          v.w += bf16_hi(r2.y);
         }
         uint2 ov;
-        ov.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.x)) |
-               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.y)) << 16);
-        ov.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.z)) |
-               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.w)) << 16);
-        uint16_t* dst = out_ptr(a, m, n);  // 4 consecutive columns never straddle a head (D % 4 == 0)
-        if (dst) *reinterpret_cast<uint2*>(dst) = ov;
+        ov.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.x)) |
+               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.y)) << 16);
+        ov.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.z)) |
+               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.w)) << 16);
+        uint16_t* d = out_ptr(a, m, n);
+        if (d) *reinterpret_cast<uint2*>(d) = ov;
       }
     }
     cluster_sync_all();  // keep this CTA's shared memory alive until every reader is done
@@ -457,12 +539,6 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
-}
-
-__device__ __forceinline__ uint32_t mapa_shared(const void* local, uint32_t rank) {
-  uint32_t raddr;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(smem_u32(local)), "r"(rank));
-  return raddr;
 }
 
 __global__ void __launch_bounds__(192) mx_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmW,
@@ -856,3 +932,5 @@ cudaError_t launch_gate_up_swiglu_tc(const uint8_t* xq, const uint8_t* xs, int64
 }
 
 }  // namespace mxg
+
+MXG_TL_UNIT(gemm_tc)

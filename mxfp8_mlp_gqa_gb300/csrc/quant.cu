@@ -41,7 +41,9 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& w, float (&v)[8]) {
 __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
                                                              int64_t ld_x, uint8_t* __restrict__ q,
                                                              uint8_t* __restrict__ s) {
+  MXG_TL_SCOPE(kTlQuantize);
   pdl_wait();
+  MXG_TL_WAITED();
   pdl_trigger();
   const int64_t cpr = K >> 3;  // 8-element chunks per row (a multiple of 4)
   const int64_t total = M * cpr;
@@ -79,12 +81,78 @@ __device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float x) {
   lo = __fadd_rn(lo, e);
 }
 
+constexpr int kRmsThreads = 320;  // = K/8 for K = 2560: one chunk per thread
+
+// Error-free fp32 helpers for the RMSNorm factor (double-float arithmetic: a value is an
+// unevaluated sum hi + lo of two fp32 numbers).
+__device__ __forceinline__ void fast_two_sum(float a, float b, float& s, float& e) {  // |a| >= |b|
+  s = __fadd_rn(a, b);
+  e = __fsub_rn(b, __fsub_rn(s, a));
+}
+__device__ __forceinline__ void df_add(float& h, float& l, float ah, float al) {
+  const float s = __fadd_rn(h, ah);
+  const float bp = __fsub_rn(s, h);
+  const float e = __fadd_rn(__fsub_rn(h, __fsub_rn(s, bp)), __fsub_rn(ah, bp));
+  fast_two_sum(s, __fadd_rn(e, __fadd_rn(l, al)), h, l);
+}
+
+// r = fp32(1 / sqrt(T / K + eps)), T = sum over the warps of hi_w + lo_w, as the fp64 sequence
+// fp64 mean -> + eps -> sqrt -> 1 / x -> round to fp32 gives it. fp64 arithmetic costs ~2400
+// cycles on this part (measured), so the value is first estimated in double-float fp32
+// arithmetic (the mean to ~2^-47, then one Newton step for 1/sqrt with its quadratic term,
+// ~2^-44 overall). Unless that estimate lies within 2^-39 (relative) of a point halfway
+// between two fp32 numbers -- then the fp64 result, within ~2^-51 of the exact value, rounds to
+// the same fp32 number -- the estimate's rounding is the answer; otherwise (about one row in
+// 2^14, and every out-of-range case) the fp64 sequence runs.
+__device__ float rms_factor(const float (&wh)[kRmsThreads / 32], const float (&wl)[kRmsThreads / 32], int64_t K,
+                            float eps) {
+  float th = 0.f, tl = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRmsThreads / 32; ++i) df_add(th, tl, wh[i], wl[i]);
+  const float kf = (float)K;  // K < 2^24: exact
+  const float mh = __fdiv_rn(th, kf);
+  const float ph = __fmul_rn(mh, kf), pl = __fmaf_rn(mh, kf, -ph);
+  const float ml = __fdiv_rn(__fadd_rn(__fsub_rn(__fsub_rn(th, ph), pl), tl), kf);
+  float vh, vl;
+  {
+    const float s = __fadd_rn(mh, eps);
+    const float bp = __fsub_rn(s, mh);
+    const float e = __fadd_rn(__fsub_rn(mh, __fsub_rn(s, bp)), __fsub_rn(eps, bp));
+    fast_two_sum(s, __fadd_rn(e, ml), vh, vl);
+  }
+  bool ok = isfinite(th) && vh > 0x1p-100f && vh < 0x1p100f;
+  float r = 0.f;
+  if (ok) {
+    const float y0 = rsqrtf(vh);
+    const float s2h = __fmul_rn(y0, y0), s2l = __fmaf_rn(y0, y0, -s2h);
+    const float qh = __fmul_rn(vh, s2h);
+    const float ql = __fadd_rn(__fmaf_rn(vh, s2h, -qh), __fadd_rn(__fmul_rn(vh, s2l), __fmul_rn(vl, s2h)));
+    const float e = __fsub_rn(__fsub_rn(1.f, qh), ql);  // 1 - v y0^2, |e| ~ 2^-22
+    const float c = __fmul_rn(y0, __fmaf_rn(0.375f * e, e, 0.5f * e));
+    float yh, yl;
+    fast_two_sum(y0, c, yh, yl);
+    const uint32_t yb = __float_as_uint(yh);
+    const int ex = (int)((yb >> 23) & 0xFFu);
+    // half the fp32 spacing at yh (below a power of two the spacing halves)
+    float half = __uint_as_float((uint32_t)(ex - 24) << 23);
+    if ((yb & 0x7FFFFFu) == 0 && yl < 0.f) half *= 0.5f;
+    ok = ex > 64 && ex < 190 && __fsub_rn(half, fabsf(yl)) > __fmul_rn(yh, 0x1p-39f);
+    r = yh;
+  }
+  if (!ok) {
+    double t = 0.0;
+    for (int i = 0; i < kRmsThreads / 32; ++i) t += (double)wh[i] + (double)wl[i];
+    const double ms = t / (double)K;
+    r = (float)(1.0 / sqrt(ms + (double)eps));
+  }
+  return r;
+}
+
 // One CTA per row; each thread keeps its 8-element chunks of x (and gamma) in registers, so
 // the row is read from memory once. Sum of squares: each square of a bf16 value is exact in
-// fp32; they are summed as a two-sum pair (~48-bit), and the ten warp partials in fp64, so the
-// fp64 mean agrees with an fp64 summation far below the fp32 rounding of r. Then
-// y = bf16((x * r) * gamma) with r = fp32(1 / sqrt(mean + eps)), then the MX rule on y.
-constexpr int kRmsThreads = 320;  // = K/8 for K = 2560: one chunk per thread
+// fp32; they are summed as a two-sum pair (~48-bit), and the ten warp partials in fp64
+// (rms_factor), so the fp64 mean agrees with an fp64 summation far below the fp32 rounding of
+// r. Then y = bf16((x * r) * gamma) with r = fp32(1 / sqrt(mean + eps)), then the MX rule on y.
 constexpr int kRmsChunks = 7;     // chunks per thread kept in registers: K <= 8 * 320 * 7 = 17920
 
 __global__ void __launch_bounds__(kRmsThreads) rmsnorm_mxfp8_quantize_kernel(const uint16_t* __restrict__ x,
@@ -92,6 +160,7 @@ __global__ void __launch_bounds__(kRmsThreads) rmsnorm_mxfp8_quantize_kernel(con
                                                                              float eps, int64_t K, int64_t ld_x,
                                                                              uint8_t* __restrict__ q,
                                                                              uint8_t* __restrict__ s) {
+  MXG_TL_SCOPE(kTlRmsQuant);
   const int64_t row = blockIdx.x;
   const uint16_t* xr = x + row * ld_x;
   const int cpr = (int)(K >> 3);
@@ -103,6 +172,7 @@ __global__ void __launch_bounds__(kRmsThreads) rmsnorm_mxfp8_quantize_kernel(con
     gw[i] = c < cpr ? __ldg(reinterpret_cast<const uint4*>(gamma + ((int64_t)c << 3))) : make_uint4(0, 0, 0, 0);
   }
   pdl_wait();
+  MXG_TL_WAITED();
   pdl_trigger();
   uint4 xw[kRmsChunks];
 #pragma unroll
@@ -126,16 +196,14 @@ __global__ void __launch_bounds__(kRmsThreads) rmsnorm_mxfp8_quantize_kernel(con
     two_sum_acc(hi, lo, h2);
     lo = __fadd_rn(lo, l2);
   }
-  __shared__ double red[kRmsThreads / 32];
+  __shared__ float red_h[kRmsThreads / 32], red_l[kRmsThreads / 32];
   __shared__ float r_sh;
-  if (lane == 0) red[warp] = (double)hi + (double)lo;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double t = 0.0;
-    for (int i = 0; i < kRmsThreads / 32; ++i) t += red[i];
-    const double ms = t / (double)K;
-    r_sh = (float)(1.0 / sqrt(ms + (double)eps));
+  if (lane == 0) {
+    red_h[warp] = hi;
+    red_l[warp] = lo;
   }
+  __syncthreads();
+  if (threadIdx.x == 0) r_sh = rms_factor(red_h, red_l, K, eps);
   __syncthreads();
   const float r = r_sh;
 #pragma unroll
@@ -179,3 +247,5 @@ cudaError_t launch_rmsnorm_mxfp8_quantize(const uint16_t* x, const uint16_t* gam
 }
 
 }  // namespace mxg
+
+MXG_TL_UNIT(quant)

@@ -12,8 +12,10 @@ namespace mxg {
 // update never reads a value it has already overwritten.
 __global__ void __launch_bounds__(256) prev_tokens_shift_kernel(int32_t* __restrict__ prev,
                                                                 const int32_t* __restrict__ next, int W, int cw) {
+  MXG_TL_SCOPE(kTlShift);
   extern __shared__ int32_t win[];
   pdl_wait();
+  MXG_TL_WAITED();
   pdl_trigger();
   const int n = W * cw;
   int32_t* p = prev + (int64_t)blockIdx.x * n;
@@ -30,7 +32,9 @@ __global__ void __launch_bounds__(256) prev_tokens_shift_kernel(int32_t* __restr
 // copy-engine operation with its own start-up latency.
 __global__ void __launch_bounds__(256) copy16_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src,
                                                      int64_t n16) {
+  MXG_TL_SCOPE(kTlCopy16);
   pdl_wait();
+  MXG_TL_WAITED();
   pdl_trigger();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x)
     dst[i] = src[i];
@@ -51,7 +55,9 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint16_t* __restrict__ k
                                                         const uint16_t* __restrict__ vn, int64_t ld_new,
                                                         const int32_t* __restrict__ kv_len, int bs, int Hkv, int D,
                                                         int64_t cap, int32_t* err, KvPages pg) {
+  MXG_TL_SCOPE(kTlKvAppend);
   pdl_wait();
+  MXG_TL_WAITED();
   pdl_trigger();
   const int gw = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
@@ -144,3 +150,5 @@ cudaError_t launch_kv_append_mx(uint8_t* kc, uint8_t* ks, uint8_t* vc, uint8_t* 
 }
 
 }  // namespace mxg
+
+MXG_TL_UNIT(small)

@@ -85,3 +85,21 @@ def test_rmsnorm_quantize_bit_exact(M, K):
     oq, os_ = ops.rmsnorm_mx_quantize(x, gam, 1e-6)
     np.testing.assert_array_equal(s.cpu().numpy(), os_)
     np.testing.assert_array_equal(q.cpu().numpy(), oq)
+
+
+def test_rmsnorm_factor_near_a_rounding_midpoint():
+    # Rows of ones with eps = 3 * 2^-24 put 1/sqrt(1 + eps) within ~2^-46 of the point halfway
+    # between the fp32 numbers 1 - 2^-24 and 1 - 2^-23: the kernel's fp32 estimate of the factor
+    # cannot decide that rounding and takes the fp64 sequence. Rows of other values and the
+    # other eps take the estimate. Both must give the oracle's codes and scales bit for bit.
+    K = 2560
+    rng = np.random.default_rng(5)
+    rows = [np.full(K, 1.0), np.full(K, -1.0)] + [rng.standard_normal(K) for _ in range(6)]
+    x = mx.f64_to_bf16(np.array(rows))
+    gam = synth.gamma(K, 5, synth.TID["gamma1"])
+    for eps in (3 * 2.0 ** -24, 2.0 ** -24, 1e-6):
+        eps32 = float(np.float32(eps))
+        q, s = api.rmsnorm_mxfp8_quantize(dev_bf16(x), dev_bf16(gam), eps32)
+        oq, os_ = ops.rmsnorm_mx_quantize(x, gam, eps32)
+        np.testing.assert_array_equal(s.cpu().numpy(), os_)
+        np.testing.assert_array_equal(q.cpu().numpy(), oq)
