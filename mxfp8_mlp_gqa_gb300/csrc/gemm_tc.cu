@@ -702,6 +702,268 @@ __global__ void __launch_bounds__(192) mx_gemm_tc2_kernel(const __grid_constant_
   if (warp == 1) tc::tmem_dealloc2(tmem, S::kTmemCols);
 }
 
+// Persistent form of the CTA-pair kernel for plain bf16 stores (config-5 GEMMs). One cluster
+// (CTA pair) per two SMs walks tiles pair, pair + P, ... of a grouped raster order: `group`
+// token-tile rows at a time, weight-tile columns within a group, so that the tiles in flight
+// together share their weight and token panels in L2. The operand ring streams across tile
+// boundaries without draining. The MMA warp starts a tile once the epilogue warps of both CTAs
+// have read the previous tile's accumulator out of TMEM (acc_empty, in the even CTA, 8
+// arrivals); the epilogue then converts and stores from registers through a double-buffered
+// staging area with TMA while the next tile accumulates. The scale atoms of a stage arrive with
+// its operands; a seventh warp copies them to TMEM (slot stage % kSfStages) and commits to the
+// stage's sf_ready barrier, which is what the MMA thread waits for: with the copies issued by
+// the MMA thread itself, its per-stage issue work (~720 cycles) exceeded the MMAs' (~590).
+struct Tc2pShape {
+  static constexpr int kABytes = 128 * kKG;
+  static constexpr int kBBytes = 128 * kKG;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = 6;
+  static constexpr int kSfBytes = 3 * 512;
+  static constexpr int kSfStages = 8;  // TMEM scale slots
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kSfRingBytes = kStages * kSfBytes;
+  static constexpr int kChunkBytes = 16 * 32 * 2;          // [16 tokens][32 features] bf16
+  static constexpr int kStgBytes = 4 * 2 * kChunkBytes;    // two chunks per epilogue warp
+  static constexpr int kSmemBytes = 1024 + kRingBytes + kSfRingBytes + kStgBytes + 8 * (3 * kStages + 2) + 16;
+  static constexpr int kThreads = 224;  // producer, MMA, 4 epilogue warps, scale copier
+  static constexpr int kSfCols = 12;
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(256 + kSfStages * kSfCols <= 512, "tensor memory budget");
+  // the copier fills TMEM scale slot x % kSfStages after stage x's operands landed, which the
+  // producer could load only once the MMAs of stage x - kStages completed
+  static_assert(kSfStages >= kStages, "TMEM scale slot reuse");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ void bulk_wait_group_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+// arrive on an mbarrier given by its shared::cluster address (this CTA's or a peer's)
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cl) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cl) : "memory");
+}
+
+__device__ __forceinline__ void tc2p_tile(int t, int tiles_m, int tiles_n, int group, int& tm, int& tn) {
+  const int gsz = group * tiles_n;
+  const int g = t / gsz, r = t - g * gsz;
+  const int rows = min(group, tiles_m - g * group);
+  tm = g * group + r % rows;
+  tn = r / rows;
+}
+
+__global__ void __launch_bounds__(Tc2pShape::kThreads, 1) mx_gemm_tc2p_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                                const __grid_constant__ CUtensorMap tmX,
+                                                                const __grid_constant__ CUtensorMap tmSW,
+                                                                const __grid_constant__ CUtensorMap tmSX,
+                                                                const __grid_constant__ CUtensorMap tmO,
+                                                                const TcArgs a, int tiles_m, int tiles_n, int group) {
+  using S = Tc2pShape;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  uint8_t* sfring = smem + S::kRingBytes;
+  uint8_t* stg_base = sfring + S::kSfRingBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(stg_base + S::kStgBytes);  // used in the even CTA
+  uint64_t* empty = full + S::kStages;
+  uint64_t* sf_ready = empty + S::kStages;  // used in the even CTA
+  uint64_t* tmem_full = sf_ready + S::kStages;
+  uint64_t* acc_empty = tmem_full + 1;  // used in the even CTA
+  uint32_t* tmem_sh = reinterpret_cast<uint32_t*>(acc_empty + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const int P = (int)(gridDim.x >> 1), pair = (int)(blockIdx.x >> 1);
+  const int T = tiles_m * tiles_n;
+  const int ng = a.groups;
+  const int my_tiles = pair < T ? (T - 1 - pair) / P + 1 : 0;
+  const int nstages = my_tiles * ng;  // operand stages this pair runs
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&sf_ready[s], 1);
+    }
+    mbar_init(tmem_full, 1);
+    mbar_init(acc_empty, 8);  // four epilogue warps of each CTA
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc2(tmem_sh, S::kTmemCols);
+    tc::tmem_relinquish2();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers and TMEM exist before any cross-CTA signal
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_sh;
+
+  if (warp == 0) {
+    // ----------------------------------------------------------------- producer (both CTAs)
+    if (lane == 0) {
+      prefetch_tensormap(&tmW);
+      prefetch_tensormap(&tmX);
+      prefetch_tensormap(&tmSW);
+      prefetch_tensormap(&tmSX);
+      // the even CTA expects the bytes of both CTAs; the odd CTA's copies complete there too
+      constexpr uint32_t tx = 2 * (S::kStageBytes + S::kSfBytes);
+      int pre = 0;
+      if (pair < T) {  // the first tile's weights read nothing produced upstream
+        int tm, tn;
+        tc2p_tile(pair, tiles_m, tiles_n, group, tm, tn);
+        pre = ng < S::kStages ? ng : S::kStages;
+        for (int i = 0; i < pre; ++i) {
+          const uint32_t fb = mapa_shared(&full[i], 0);
+          if (rank == 0) mbar_arrive_expect_tx(&full[i], tx);
+          tma_load_2d_pair(ring + i * S::kStageBytes, &tmW, fb, i * kKG, (2 * tn + (int)rank) * 128);
+        }
+      }
+      pdl_wait();
+      pdl_trigger();
+      int it = 0;
+      bool live = true;
+      for (int t = pair; t < T && live; t += P) {
+        int tm, tn;
+        tc2p_tile(t, tiles_m, tiles_n, group, tm, tn);
+        const int wrow = (2 * tn + (int)rank) * 128;  // this CTA's 128 weight rows
+        const int xrow = tm * 256 + 128 * (int)rank;  // this CTA's 128-token half
+        for (int k = 0; k < ng; ++k, ++it) {
+          const int s = it % S::kStages;
+          if (it >= S::kStages && !mbar_wait(&empty[s], ((it / S::kStages) - 1) & 1, a.err)) {
+            live = false;
+            break;
+          }
+          uint8_t* st = ring + s * S::kStageBytes;
+          const uint32_t fb = mapa_shared(&full[s], 0);
+          if (it >= pre) {
+            if (rank == 0) mbar_arrive_expect_tx(&full[s], tx);
+            tma_load_2d_pair(st, &tmW, fb, k * kKG, wrow);
+          }
+          tma_load_2d_pair(st + S::kABytes, &tmX, fb, k * kKG, xrow);
+          uint8_t* sf = sfring + s * S::kSfBytes;
+          tma_load_2d_pair(sf, &tmSW, fb, (2 * tn + (int)rank) * 128, k);
+          tma_load_2d_pair(sf + 512, &tmSX, fb, tm * 256, k);
+        }
+      }
+      // Before this CTA may exit, every MMA that reads its stages has signalled (the last phase
+      // of each stage's `empty`); those MMAs were issued only after all copies had landed.
+      for (int j = it - S::kStages < 0 ? 0 : it - S::kStages; j < it; ++j)
+        if (!mbar_wait(&empty[j % S::kStages], (j / S::kStages) & 1, a.err)) break;
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA issuer (even CTA)
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc0 = tc::idesc_mxf8(256, 0, 0, 256);
+      int it = 0, tl = 0;
+      bool live = true;
+      for (int t = pair; t < T && live; t += P, ++tl) {
+        if (tl > 0) {  // both CTAs' epilogues have read the previous tile's accumulator
+          if (!mbar_wait(acc_empty, (tl - 1) & 1, a.err)) break;
+          tc::fence_after_sync();
+        }
+        for (int k = 0; k < ng; ++k, ++it) {
+          const int s = it % S::kStages;
+          // the stage's operands have landed and its scales are in TMEM (the copier's commit)
+          if (!mbar_wait(&sf_ready[s], (it / S::kStages) & 1, a.err)) {
+            live = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t t_sfa = tmem + 256 + (uint32_t)((it % S::kSfStages) * S::kSfCols), t_sfb = t_sfa + 4;
+          const uint32_t sa = smem_u32(ring + s * S::kStageBytes), sb = sa + S::kABytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc::mma_mxf8_2(tmem, tc::desc_k128_sw128(sa + kk * 32), tc::desc_k128_sw128(sb + kk * 32),
+                           idesc0 | ((uint32_t)kk << 4) | ((uint32_t)kk << 29), t_sfa, t_sfb, (k > 0 || kk > 0) ? 1u : 0u);
+          tc::commit2_mc(&empty[s], (uint16_t)0x3);
+        }
+        if (live) tc::commit2_mc(tmem_full, (uint16_t)0x3);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 6) {
+    // ----------------------------------------------------------------- scale copier (even CTA)
+    if (lane == 0 && rank == 0) {
+      for (int it = 0; it < nstages; ++it) {
+        const int s = it % S::kStages, j = it % S::kSfStages;
+        if (!mbar_wait(&full[s], (it / S::kStages) & 1, a.err)) break;
+        tc::fence_after_sync();
+        const uint32_t t_sfa = tmem + 256 + (uint32_t)(j * S::kSfCols), t_sfb = t_sfa + 4;
+        const uint32_t ssf = smem_u32(sfring + s * S::kSfBytes);
+        tc::cp_sf_atom2(t_sfa, tc::desc_sf_atom(ssf));
+        tc::cp_sf_atom2(t_sfb, tc::desc_sf_atom(ssf + 512));
+        tc::cp_sf_atom2(t_sfb + 4, tc::desc_sf_atom(ssf + 1024));
+        tc::commit2_mc(&sf_ready[s], (uint16_t)0x1);  // arrives once the copies are done
+      }
+    }
+    __syncwarp();
+  } else {
+    // ----------------------------------------------------------------- epilogue (both CTAs)
+    const int q = warp & 3;
+    pdl_wait();
+    __shared__ int ok_sh[2];  // one thread polls the accumulator barrier for the four warps
+    uint16_t* stg = reinterpret_cast<uint16_t*>(stg_base + q * 2 * S::kChunkBytes);
+    const uint32_t ae = mapa_shared(acc_empty, 0);  // the even CTA's barrier
+    const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
+    int tl = 0, nchunk = 0;
+    for (int t = pair; t < T; t += P, ++tl) {
+      int tm, tn;
+      tc2p_tile(t, tiles_m, tiles_n, group, tm, tn);
+      const int n0 = (2 * tn + (int)rank) * 128, m0 = tm * 256;
+      if (threadIdx.x == 64) ok_sh[tl & 1] = mbar_wait(tmem_full, tl & 1, a.err) ? 1 : 0;
+      epi_bar();
+      if (!ok_sh[tl & 1]) break;
+      tc::fence_after_sync();
+      // the row's 256 accumulators, as bf16 pairs (token 2i low, 2i + 1 high)
+      uint32_t pk[128];
+#pragma unroll
+      for (int c = 0; c < 256; c += 32) {
+        float v[32];
+        tc::ld16(trow + c, *reinterpret_cast<float(*)[16]>(v));
+        tc::ld16(trow + c + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+        tc::wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; j += 2)
+          pk[(c + j) >> 1] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[j])) |
+                             ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[j + 1])) << 16);
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(ae);  // the accumulator may take the next tile
+      // each warp owns features n0 + 32q .. + 31 (its lanes) of all 256 tokens: 16 chunks of 16
+      // tokens, staged [token][feature] and written by TMA (clipped at the edges)
+#pragma unroll
+      for (int c = 0; c < 256; c += 16, ++nchunk) {
+        uint16_t* ch = stg + (nchunk & 1) * (16 * 32);
+        if (nchunk >= 2) {
+          if (lane == 0) bulk_wait_group_read1();  // the store that last read this buffer is done
+          __syncwarp();
+        }
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+          ch[j * 32 + lane] = (uint16_t)(pk[(c + j) >> 1] & 0xFFFFu);
+          ch[(j + 1) * 32 + lane] = (uint16_t)(pk[(c + j) >> 1] >> 16);
+        }
+        fence_proxy_async_smem();  // generic-proxy writes -> the TMA engine's reads
+        __syncwarp();
+        if (lane == 0) {
+          if (n0 + 32 * q < a.N && m0 + c < a.M) tma_store_2d(&tmO, ch, n0 + 32 * q, m0 + c);
+          bulk_commit_group();
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_group0();
+    __syncwarp();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  cluster_sync_all();  // neither CTA frees its TMEM or leaves while the pair may still use it
+  tc::fence_after_sync();
+  if (warp == 1) tc::tmem_dealloc2(tmem, S::kTmemCols);
+}
+
 // ---------------------------------------------------------------------------------- host
 namespace {
 
@@ -781,6 +1043,35 @@ cudaError_t launch_tc(const CUtensorMap& tw, const CUtensorMap& tx, const TcArgs
   return launch_kc(mx_gemm_tc_kernel<BN, EPI>, grid, dim3(192), S::kSmemBytes, st, cluster, tw, tx, a);
 }
 
+// token-tile rows per raster group of the persistent pair kernel
+constexpr int kRasterGroup = 8;
+
+// CTA pairs of the persistent kernel that are resident at once (queried once)
+int tc2p_pairs() {
+  static int cache = 0;
+  if (cache) return cache;
+  using P2 = Tc2pShape;
+  cudaFuncSetAttribute(mx_gemm_tc2p_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P2::kSmemBytes);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * 76, 1, 1);
+  cfg.blockDim = dim3(P2::kThreads);
+  cfg.dynamicSmemBytes = P2::kSmemBytes;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, mx_gemm_tc2p_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 76;
+  }
+  cache = n > 0 ? n : 1;
+  return cache;
+}
+
 cudaError_t launch_tc2(const CUtensorMap& tw, const CUtensorMap& tx, const TcArgs& a, dim3 grid, cudaStream_t st) {
   using S = Tc2Shape;
   if (!a.wsp || (grid.x & 1) || grid.z != 1) return cudaErrorInvalidValue;
@@ -799,8 +1090,20 @@ cudaError_t launch_tc2(const CUtensorMap& tw, const CUtensorMap& tx, const TcArg
   b.tma_out = a.residual == nullptr && a.kv.kc == nullptr &&
               make_tensor_map_2d(&tso, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.out, (uint64_t)a.N, (uint64_t)a.M,
                                  (uint64_t)a.N * 2, 32, 16, CU_TENSOR_MAP_SWIZZLE_NONE);
-  cudaError_t e =
-      cudaFuncSetAttribute(mx_gemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+  cudaError_t e;
+  if (b.tma_out) {
+    // plain stores: the persistent kernel, one CTA pair per two SMs (all resident at once)
+    using P2 = Tc2pShape;
+    e = cudaFuncSetAttribute(mx_gemm_tc2p_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P2::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int tiles_n = (int)(grid.x / 2), tiles_m = (int)grid.y;
+    const int T = tiles_n * tiles_m;
+    int pairs = tc2p_pairs();
+    if (pairs > T) pairs = T;
+    return launch_kc(mx_gemm_tc2p_kernel, dim3(2u * (unsigned)pairs), dim3(P2::kThreads), P2::kSmemBytes, st, dim3(2, 1, 1),
+                     tw, tx, tsw, tsx, tso, b, tiles_m, tiles_n, kRasterGroup);
+  }
+  e = cudaFuncSetAttribute(mx_gemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
   if (e != cudaSuccess) return e;
   return launch_kc(mx_gemm_tc2_kernel, grid, dim3(192), S::kSmemBytes, st, dim3(2, 1, 1), tw, tx, tsw, tsx, tso, b);
 }

@@ -76,10 +76,12 @@ def test_split_k_cluster_reduction_is_deterministic():
     assert_float_close(host_f64(outs[0]), ops.mx_gemm(xq, xs, wq, ws))
 
 
-@pytest.mark.parametrize("M,N,K", [(1100, 264, 384), (2048, 520, 512), (1500, 1032, 256), (1025, 8, 128)])
+@pytest.mark.parametrize("M,N,K", [(1100, 264, 384), (2048, 520, 512), (1500, 1032, 256), (1025, 8, 128),
+                                   (4100, 2056, 256), (3000, 4104, 384)])
 def test_large_gemm_plain_store(M, N, K):
-    # more than 1024 tokens and no residual: the CTA-pair kernel writes its tile through staged
-    # copy-engine stores, clipped at ragged M / N edges; every output element must be written
+    # more than 1024 tokens and no residual: the persistent CTA-pair kernel writes its tiles
+    # through staged copy-engine stores, clipped at ragged M / N edges (the last two shapes give
+    # each pair two or more tiles, ragged ones included); every output element must be written
     g = synth.rng(12, M + N)
     xq, wq = _codes((M, K), g), _codes((N, K), g)
     xs = (115 + (np.arange(M)[:, None] * 5 + np.arange(K // 32)[None, :]) % 23).astype(np.uint8)
