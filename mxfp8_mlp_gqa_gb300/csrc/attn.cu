@@ -515,6 +515,9 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
   const int n = p.kv_len[b];
   if (n < 1 || (int64_t)n > p.cap || n > p.max_kv_len) {
     if (split == 0 && g == 0 && threadIdx.x == 0) set_error(p.err, MXG_EDEVICE);
+    // several splits: weight zero for every split of the sequence, so the combine writes zeros
+    if (p.max_splits > 1 && threadIdx.x < p.group)
+      p.lse[((int64_t)b * p.Hq + g * p.group + threadIdx.x) * p.max_splits + split] = -INFINITY;
     if (p.max_splits == 1 && warp < kConsumers) {  // single-split mode: no combine pass, zero here
       for (int i = threadIdx.x; i < p.group * D; i += kConsumers * 32) {
         const int64_t o = ((int64_t)b * p.Hq + g * p.group) * D + i;
@@ -528,7 +531,11 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
     return;
   }
   const int t0 = split * p.chunk;
-  if (t0 >= n) return;
+  if (t0 >= n) {  // a split past the prefix: weight zero, so the combine needs no kv_len
+    if (p.max_splits > 1 && threadIdx.x < p.group)
+      p.lse[((int64_t)b * p.Hq + g * p.group + threadIdx.x) * p.max_splits + split] = -INFINITY;
+    return;
+  }
   const int t1 = min(n, t0 + p.chunk);
   const int ntiles = (t1 - t0 + kTileTok - 1) / kTileTok;
   const int row0 = (int)((int64_t)bg * p.cap + t0);  // host guarantees bs*Hkv*cap < 2^31 (contiguous)
@@ -665,43 +672,49 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
   }
 }
 
-// Merge the splits of each (b, h): weights 2^(lse_i - max lse).
+// Merge the splits of each (b, h): weights 2^(lse_i - max lse). Every split writes its lse each
+// call (-inf for a split past the prefix or a sequence whose kv_len is out of range, or one
+// that gave up on a bounded wait), so the kernel reads no kv_len: it loads the lse values and
+// the partial outputs of up to kBatch splits at once (one round trip), skips splits of weight
+// zero, and writes zeros when every split has weight zero. One CTA serves the `group` query
+// heads of one (b, kv head): thread (h, d) of the group.
 template <int D>
-__global__ void __launch_bounds__(D) gqa_combine_kernel(const float* __restrict__ o_part,
-                                                        const float* __restrict__ lse,
-                                                        const int32_t* __restrict__ kv_len, int Hq, int64_t cap,
-                                                        int chunk, int max_splits, int max_kv_len,
+__global__ void __launch_bounds__(8 * D) gqa_combine_kernel(const float* __restrict__ o_part,
+                                                        const float* __restrict__ lse, int max_splits,
                                                         uint16_t* __restrict__ out, uint8_t* __restrict__ oq,
                                                         uint8_t* __restrict__ os) {
   MXG_TL_SCOPE(kTlCombine);
   pdl_wait();
   MXG_TL_WAITED();
   pdl_trigger();
-  const int64_t bh = blockIdx.x;
-  const int b = (int)(bh / Hq);
-  const int d = threadIdx.x;
-  const int n = kv_len[b];
-  if (n < 1 || (int64_t)n > cap || n > max_kv_len) {
-    out[bh * D + d] = 0;
-    if (oq) {
-      oq[bh * D + d] = 0;
-      if ((d & 31) == 0) os[(bh * D + d) >> 5] = 0;
-    }
-    return;
-  }
-  const int ns = (n + chunk - 1) / chunk;
+  constexpr int kBatch = 8;
+  const int64_t bh = (int64_t)blockIdx.x * (blockDim.x / D) + threadIdx.x / D;
+  const int d = threadIdx.x % D;
   const float* l = lse + bh * max_splits;
-  float M = -INFINITY;
-  for (int i = 0; i < ns; ++i) M = fmaxf(M, l[i]);
-  float W = 0.f, acc = 0.f;
-  // a split that gave up on a bounded wait left lse = -inf (weight 0); if every split did,
-  // the output is zero (the error flag says why)
-  if (M != -INFINITY) {
-    for (int i = 0; i < ns; ++i) {
-      const float w = exp2f(l[i] - M);
-      W += w;
-      acc += w * o_part[(bh * max_splits + i) * D + d];
+  const float* op = o_part + bh * max_splits * D + d;
+  float M = -INFINITY, W = 0.f, acc = 0.f;
+  for (int i0 = 0; i0 < max_splits; i0 += kBatch) {
+    float lv[kBatch], ov[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      lv[i] = i0 + i < max_splits ? l[i0 + i] : -INFINITY;
+      ov[i] = i0 + i < max_splits ? op[(int64_t)(i0 + i) * D] : 0.f;
     }
+    float Mb = M;
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) Mb = fmaxf(Mb, lv[i]);
+    if (Mb == -INFINITY) continue;
+    const float r = M == -INFINITY ? 0.f : exp2f(M - Mb);  // rescale what the earlier batches summed
+    W *= r;
+    acc *= r;
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i)
+      if (lv[i] != -INFINITY) {
+        const float w = exp2f(lv[i] - Mb);
+        W += w;
+        acc += w * ov[i];
+      }
+    M = Mb;
   }
   const __nv_bfloat16 ob = __float2bfloat16_rn(M == -INFINITY ? 0.f : acc / W);
   out[bh * D + d] = __bfloat16_as_ushort(ob);
@@ -779,13 +792,13 @@ cudaError_t launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const C
     e = launch_k(gqa_split_kernel<64, kMx>, grid, dim3(kThreads), smem, st, 1, tmK, tmV, tmKS, tmVS, p);
   }
   if (e != cudaSuccess || ms == 1) return e;
+  // one CTA per (b, kv head): its `group` query heads, D threads each
+  const dim3 cgrid((unsigned)(bs * Hkv)), cblock((unsigned)(p.group * D));
   if (D == 128)
-    return launch_k(gqa_combine_kernel<128>, dim3((unsigned)(bs * Hq)), dim3(128), 0, st, 1,
-                    static_cast<const float*>(p.o_part), static_cast<const float*>(p.lse), kv_len, (int)Hq, cap, chunk,
-                    ms, (int)max_kv_len, out, oq, os);
-  return launch_k(gqa_combine_kernel<64>, dim3((unsigned)(bs * Hq)), dim3(64), 0, st, 1,
-                  static_cast<const float*>(p.o_part), static_cast<const float*>(p.lse), kv_len, (int)Hq, cap, chunk, ms,
-                  (int)max_kv_len, out, oq, os);
+    return launch_k(gqa_combine_kernel<128>, cgrid, cblock, 0, st, 1, static_cast<const float*>(p.o_part),
+                    static_cast<const float*>(p.lse), ms, out, oq, os);
+  return launch_k(gqa_combine_kernel<64>, cgrid, cblock, 0, st, 1, static_cast<const float*>(p.o_part),
+                  static_cast<const float*>(p.lse), ms, out, oq, os);
 }
 
 }  // namespace
