@@ -717,8 +717,10 @@ __global__ void __launch_bounds__(8 * D) gqa_combine_kernel(const float* __restr
     M = Mb;
   }
   const __nv_bfloat16 ob = __float2bfloat16_rn(M == -INFINITY ? 0.f : acc / W);
+  MXG_TL_MARK1();  // timeline: merged
   out[bh * D + d] = __bfloat16_as_ushort(ob);
   if (oq) mx_quant_warp_store(__bfloat162float(ob), oq + bh * D + d, os + ((bh * D + d) >> 5));
+  MXG_TL_MARK2();  // timeline: stores issued
 }
 
 // ---------------------------------------------------------------------------------- host

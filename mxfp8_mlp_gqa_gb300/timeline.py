@@ -5,7 +5,7 @@ compiled with ``-DMXG_TIMELINE``, whose decode-step kernels append one record pe
 {kernel id, block, warp, entry, return from the programmatic wait, exit, mark 1, mark 2}
 (globaltimer ns) to a device buffer; the marks are kernel-specific phase points (GEMM: first
 stage landed / accumulator complete, last MMA issued / split-K partials staged; attention:
-first tile landed, last tile consumed). ``bench.py --timeline`` replays the step's CUDA graph on that library and calls
+first tile landed, last tile consumed; combine: merged, stores issued). ``bench.py --timeline`` replays the step's CUDA graph on that library and calls
 :func:`summarize`, which folds the records of each step into launches (the step's kernel order
 is fixed) and reports, per launch, when its first CTA entered, when the first warp came back
 from the programmatic wait (its predecessor had completed), and when its last warp left.
