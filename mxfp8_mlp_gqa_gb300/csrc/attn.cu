@@ -675,51 +675,73 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
 // Merge the splits of each (b, h): weights 2^(lse_i - max lse). Every split writes its lse each
 // call (-inf for a split past the prefix or a sequence whose kv_len is out of range, or one
 // that gave up on a bounded wait), so the kernel reads no kv_len: it loads the lse values and
-// the partial outputs of up to kBatch splits at once (one round trip), skips splits of weight
-// zero, and writes zeros when every split has weight zero. One CTA serves the `group` query
-// heads of one (b, kv head): thread (h, d) of the group.
+// the partial outputs of up to kSplits splits at once, skips splits of weight zero, and writes
+// zeros when every split has weight zero. One D-thread CTA serves the `group` query heads of
+// one (b, kv head) -- thread d takes dimension d of each head, up to kHeads heads' loads in
+// flight together. (Capping it at 64 registers, so that the O projection's CTAs become resident
+// and prefetch during the combine, measured no faster: the prefetch then competes with the
+// combine's own loads.)
 template <int D>
-__global__ void __launch_bounds__(8 * D) gqa_combine_kernel(const float* __restrict__ o_part,
-                                                        const float* __restrict__ lse, int max_splits,
+__global__ void __launch_bounds__(D) gqa_combine_kernel(const float* __restrict__ o_part,
+                                                        const float* __restrict__ lse, int max_splits, int group,
                                                         uint16_t* __restrict__ out, uint8_t* __restrict__ oq,
                                                         uint8_t* __restrict__ os) {
   MXG_TL_SCOPE(kTlCombine);
   pdl_wait();
   MXG_TL_WAITED();
   pdl_trigger();
-  constexpr int kBatch = 8;
-  const int64_t bh = (int64_t)blockIdx.x * (blockDim.x / D) + threadIdx.x / D;
-  const int d = threadIdx.x % D;
-  const float* l = lse + bh * max_splits;
-  const float* op = o_part + bh * max_splits * D + d;
-  float M = -INFINITY, W = 0.f, acc = 0.f;
-  for (int i0 = 0; i0 < max_splits; i0 += kBatch) {
-    float lv[kBatch], ov[kBatch];
+  constexpr int kSplits = 8, kHeads = 4;
+  const int d = threadIdx.x;
+  for (int hb = 0; hb < group; hb += kHeads) {
+    float M[kHeads], W[kHeads], acc[kHeads];
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-      lv[i] = i0 + i < max_splits ? l[i0 + i] : -INFINITY;
-      ov[i] = i0 + i < max_splits ? op[(int64_t)(i0 + i) * D] : 0.f;
+    for (int j = 0; j < kHeads; ++j) {
+      M[j] = -INFINITY;
+      W[j] = 0.f;
+      acc[j] = 0.f;
     }
-    float Mb = M;
+    for (int i0 = 0; i0 < max_splits; i0 += kSplits) {
+      float lv[kHeads][kSplits], ov[kHeads][kSplits];
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i) Mb = fmaxf(Mb, lv[i]);
-    if (Mb == -INFINITY) continue;
-    const float r = M == -INFINITY ? 0.f : exp2f(M - Mb);  // rescale what the earlier batches summed
-    W *= r;
-    acc *= r;
+      for (int j = 0; j < kHeads; ++j) {
+        const int64_t bh = (int64_t)blockIdx.x * group + hb + j;
+        const bool hv = hb + j < group;
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i)
-      if (lv[i] != -INFINITY) {
-        const float w = exp2f(lv[i] - Mb);
-        W += w;
-        acc += w * ov[i];
+        for (int i = 0; i < kSplits; ++i) {
+          const bool v = hv && i0 + i < max_splits;
+          lv[j][i] = v ? lse[bh * max_splits + i0 + i] : -INFINITY;
+          ov[j][i] = v ? o_part[(bh * max_splits + i0 + i) * D + d] : 0.f;
+        }
       }
-    M = Mb;
+#pragma unroll
+      for (int j = 0; j < kHeads; ++j) {
+        float Mb = M[j];
+#pragma unroll
+        for (int i = 0; i < kSplits; ++i) Mb = fmaxf(Mb, lv[j][i]);
+        if (Mb == -INFINITY) continue;
+        const float r = M[j] == -INFINITY ? 0.f : exp2f(M[j] - Mb);  // rescale the earlier batches' sums
+        W[j] *= r;
+        acc[j] *= r;
+#pragma unroll
+        for (int i = 0; i < kSplits; ++i)
+          if (lv[j][i] != -INFINITY) {
+            const float w = exp2f(lv[j][i] - Mb);
+            W[j] += w;
+            acc[j] += w * ov[j][i];
+          }
+        M[j] = Mb;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kHeads; ++j) {
+      if (hb + j >= group) break;
+      const int64_t o = ((int64_t)blockIdx.x * group + hb + j) * D + d;
+      const __nv_bfloat16 ob = __float2bfloat16_rn(M[j] == -INFINITY ? 0.f : acc[j] / W[j]);
+      MXG_TL_MARK1();  // timeline: merged
+      out[o] = __bfloat16_as_ushort(ob);
+      if (oq) mx_quant_warp_store(__bfloat162float(ob), oq + o, os + (o >> 5));
+    }
   }
-  const __nv_bfloat16 ob = __float2bfloat16_rn(M == -INFINITY ? 0.f : acc / W);
-  MXG_TL_MARK1();  // timeline: merged
-  out[bh * D + d] = __bfloat16_as_ushort(ob);
-  if (oq) mx_quant_warp_store(__bfloat162float(ob), oq + bh * D + d, os + ((bh * D + d) >> 5));
   MXG_TL_MARK2();  // timeline: stores issued
 }
 
@@ -794,13 +816,13 @@ cudaError_t launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const C
     e = launch_k(gqa_split_kernel<64, kMx>, grid, dim3(kThreads), smem, st, 1, tmK, tmV, tmKS, tmVS, p);
   }
   if (e != cudaSuccess || ms == 1) return e;
-  // one CTA per (b, kv head): its `group` query heads, D threads each
-  const dim3 cgrid((unsigned)(bs * Hkv)), cblock((unsigned)(p.group * D));
+  // one D-thread CTA per (b, kv head)
+  const dim3 cgrid((unsigned)(bs * Hkv));
   if (D == 128)
-    return launch_k(gqa_combine_kernel<128>, cgrid, cblock, 0, st, 1, static_cast<const float*>(p.o_part),
-                    static_cast<const float*>(p.lse), ms, out, oq, os);
-  return launch_k(gqa_combine_kernel<64>, cgrid, cblock, 0, st, 1, static_cast<const float*>(p.o_part),
-                  static_cast<const float*>(p.lse), ms, out, oq, os);
+    return launch_k(gqa_combine_kernel<128>, cgrid, dim3(128), 0, st, 1, static_cast<const float*>(p.o_part),
+                    static_cast<const float*>(p.lse), ms, p.group, out, oq, os);
+  return launch_k(gqa_combine_kernel<64>, cgrid, dim3(64), 0, st, 1, static_cast<const float*>(p.o_part),
+                  static_cast<const float*>(p.lse), ms, p.group, out, oq, os);
 }
 
 }  // namespace
