@@ -490,7 +490,61 @@ def run_sweeps(dev, flush):
     return {"mlp_M": mlp, "attn_bs": attn, "attn_paged_bs64": paged_attn_sweep(dev, rn, flush),
             "attn_kv_mxfp8_bs": kv_mxfp8_attn_sweep(dev, rn, flush), "prefill": prefill_sweep(dev, rn, flush),
             "bsgemm": bsgemm_sweep(dev, rn, flush),
-            "gemm_square": gemm_square_sweep(dev)}
+            "gemm_square": gemm_square_sweep(dev), "context": context_rows(dev, rn, flush)}
+
+
+def context_rows(dev, rn, flush):
+    """Context only, not targets: the same work through torch's own kernels on this machine.
+    (1) The decode MLP in bf16 (F.linear, SiLU, F.linear: 2x the weight bytes of MXFP8) at
+    M = 1 / 64 / 128. (2) Decode attention at bs = 8 through scaled_dot_product_attention with
+    GQA: over the whole 32768-position cache with a mask (the baseline of the KV-cache write-up's
+    section 4) and over the prefix up to the batch's longest kv_len, ragged rows masked (its
+    section 5); both against this library's call on the same lengths."""
+    import torch
+    import torch.nn.functional as F
+
+    from mxfp8_mlp_gqa_gb300 import api, synth
+
+    out = {}
+    w13 = rn((2 * D_FF, D_MODEL), 0.02)
+    w2 = rn((D_MODEL, D_FF), 0.02)
+    for M in (1, 64, 128):
+        x = rn((M, D_MODEL))
+
+        def mlp_bf16():
+            gu = F.linear(x, w13)
+            return F.linear(F.silu(gu[:, :D_FF]) * gu[:, D_FF:], w2)
+
+        ms = _time_op(mlp_bf16, flush)
+        out[f"torch_bf16_mlp_M{M}"] = {"us": round(ms * 1e3, 2)}
+    del w13, w2
+    bs, cap = 8, 32768
+    lens = synth.kv_lens(bs, KV_LO, KV_HI, seed=0)
+    K = rn((bs, HKV, cap, HD))
+    V = rn((bs, HKV, cap, HD))
+    q = rn((bs, HQ, HD))
+    pos = torch.arange(cap, device=dev)
+    kl = torch.from_numpy(lens).to(dev)
+    scale = 1 / math.sqrt(HD)
+    mask_full = (pos[None, :] < kl[:, None])[:, None, None, :]
+    lmax = int(lens.max())
+    mask_pre = mask_full[..., :lmax]
+    q4 = q[:, :, None, :]
+    try:
+        ms_full = _time_op(lambda: F.scaled_dot_product_attention(q4, K, V, attn_mask=mask_full, scale=scale,
+                                                                   enable_gqa=True), flush)
+        ms_pre = _time_op(lambda: F.scaled_dot_product_attention(q4, K[:, :, :lmax], V[:, :, :lmax],
+                                                                  attn_mask=mask_pre, scale=scale, enable_gqa=True),
+                          flush)
+        out["torch_sdpa_bs8_full_cache_masked"] = {"us": round(ms_full * 1e3, 2)}
+        out["torch_sdpa_bs8_prefix_masked"] = {"us": round(ms_pre * 1e3, 2)}
+    except Exception as ex:  # noqa: BLE001 - context only
+        out["torch_sdpa"] = f"unavailable: {type(ex).__name__}"
+    o = torch.empty((bs, HQ, HD), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(1, api.gqa_decode_attn_workspace(bs, HQ, HKV, HD, KV_HI)), dtype=torch.uint8, device=dev)
+    ms = _time_op(lambda: api.gqa_decode_attn(q, K, V, kl, KV_HI, scale, out=o, workspace=ws), flush)
+    out["ours_attn_bs8"] = {"us": round(ms * 1e3, 2)}
+    return out
 
 
 def bsgemm_bytes(M, N, K):
