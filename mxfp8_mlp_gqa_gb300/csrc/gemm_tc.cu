@@ -442,16 +442,42 @@ __global__ void __launch_bounds__(192, 1) mx_gemm_tc_kernel(const __grid_constan
       float4 y[kNJ];
 #pragma unroll
       for (int j = 0; j < kNJ; ++j) y[j] = dst[j] ? ld_dsmem_f32x4(&stg[sidx[j]], 0u) : make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int z = 1; z < S_; ++z) {
-        float4 p[kNJ];
+      if (S_ >= 4) {
+        // nq <= 8: a thread has at most BN/16 groups (j < kNJ/2), so three splits' partials of
+        // all of them are loaded per round
+        constexpr int kNJ4 = kNJ / 2 > 0 ? kNJ / 2 : 1;
+        for (int z = 1; z < S_; z += 3) {
+          float4 p[kNJ4][3];
 #pragma unroll
-        for (int j = 0; j < kNJ; ++j) p[j] = dst[j] ? ld_dsmem_f32x4(&stg[sidx[j]], (uint32_t)z) : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int j = 0; j < kNJ4; ++j)
 #pragma unroll
-        for (int j = 0; j < kNJ; ++j) {
-          y[j].x += p[j].x;
-          y[j].y += p[j].y;
-          y[j].z += p[j].z;
-          y[j].w += p[j].w;
+            for (int c = 0; c < 3; ++c)
+              p[j][c] = dst[j] && z + c < S_ ? ld_dsmem_f32x4(&stg[sidx[j]], (uint32_t)(z + c))
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int j = 0; j < kNJ4; ++j)
+#pragma unroll
+            for (int c = 0; c < 3; ++c)
+              if (z + c < S_) {
+                y[j].x += p[j][c].x;
+                y[j].y += p[j][c].y;
+                y[j].z += p[j][c].z;
+                y[j].w += p[j][c].w;
+              }
+        }
+      } else {
+        for (int z = 1; z < S_; ++z) {
+          float4 p[kNJ];
+#pragma unroll
+          for (int j = 0; j < kNJ; ++j)
+            p[j] = dst[j] ? ld_dsmem_f32x4(&stg[sidx[j]], (uint32_t)z) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int j = 0; j < kNJ; ++j) {
+            y[j].x += p[j].x;
+            y[j].y += p[j].y;
+            y[j].z += p[j].z;
+            y[j].w += p[j].w;
+          }
         }
       }
 #pragma unroll
