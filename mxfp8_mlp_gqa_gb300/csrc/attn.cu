@@ -30,6 +30,8 @@ namespace {
 constexpr int kTileTok = 64;        // tokens per pipeline stage
 constexpr int kMaxSplitTiles = 16;  // a split covers at most 1024 tokens (attn_chunk)
 constexpr int kSplitTok = 768;      // split length (attn_chunk)
+constexpr int kSplitTokFew = 512;   // split length with at most kFewPairs (b, g) pairs (attn_chunk)
+constexpr int kFewPairs = 32;
 constexpr int kMinSplitItems = 128; // fewest (split, b, g) items at the kv_len bound (attn_chunk)
 constexpr int kConsumers = 4;       // consumer warps (16 tokens each per tile)
 constexpr int kThreads = (kConsumers + 1) * 32;
@@ -752,14 +754,16 @@ cudaError_t set_attn_load_stall(int on) {
 }
 
 int attn_chunk(int64_t bs, int64_t Hkv, int64_t max_kv_len) {
-  // Splits of 768 tokens (12 tiles); below ~128 (split, b, g) items at the bound (a few
-  // sequences), shorter splits so that at least that many CTAs stream. Measured on GB300 at
-  // 32/8 heads, kv_len ~ U[234, 4096]: 768-token splits were the fastest of 256..1024 for
-  // bs = 8..64; 256 for bs = 1.
+  // Splits of 768 tokens (12 tiles), 512 with at most 32 (b, g) pairs; below ~128 (split, b,
+  // g) items at the bound (a few sequences), shorter splits so that at least that many CTAs
+  // stream. Measured on GB300 at 32/8 heads, kv_len ~ U[234, 4096], splits of 128..1024
+  // tokens: 768 the fastest (or within 1 %) for bs = 8..64, 512 for bs = 2..4 (bs = 4: 19.0
+  // against 20.6 us at 768, MXFP8 cache 19.1 against 23.0), 256..640 alike for bs = 1.
+  const int64_t cmax = bs * Hkv <= kFewPairs ? kSplitTokFew : kSplitTok;
   int64_t c = (bs * Hkv * max_kv_len + kMinSplitItems - 1) / kMinSplitItems;
   c = (c + kTileTok - 1) / kTileTok * kTileTok;
   if (c < kTileTok) c = kTileTok;
-  if (c > kSplitTok) c = kSplitTok;
+  if (c > cmax) c = cmax;
   return (int)c;
 }
 
