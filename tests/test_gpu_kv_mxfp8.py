@@ -64,7 +64,7 @@ def _case(bs, Hq, Hkv, D, lens, seed):
     return q, kp, vp
 
 
-@pytest.mark.parametrize("bs", [1, 8, 64])
+@pytest.mark.parametrize("bs", [1, 4, 8, 64])  # bs 4: 512-token splits
 def test_attention_vs_oracle_s2pro_shape(bs):
     Hq, Hkv, D, mkv, cap = 32, 8, 128, 4096, 4096
     lens = synth.kv_lens(bs, 234, mkv, seed=bs)
