@@ -503,19 +503,53 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBodyBytes + S::kPBytes);
   uint64_t* empty = full + S::kStages;
 
-  // the test hook is written by the host alone, so it is read before the wait, where its
-  // latency overlaps the predecessor kernel and the kv_len read below
+  // Read before the programmatic wait, while the previous kernel may still run: the test hook
+  // (written by the host alone), kv_len, and -- contiguous caches -- the first ring-full of
+  // tiles lying wholly below row kv_len - 1. The previous kernel of a decode step is the KV
+  // append, which writes only that row; the library's kernels that write other cache rows or
+  // kv_len (kv_append_extend*, copy_bytes) let their successor start only after they complete.
   MXG_TL_SCOPE(kTlSplitAttn);
   const int stall = *reinterpret_cast<volatile int*>(&g_stall_attn_loads);
-  pdl_wait();
-  MXG_TL_WAITED();
-  pdl_trigger();
   const int split = blockIdx.x;
   const int bg = blockIdx.y;
   const int b = bg / p.Hkv, g = bg - b * p.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = p.kv_len[b];
-  if (n < 1 || (int64_t)n > p.cap || n > p.max_kv_len) {
+  const bool bad_len = n < 1 || (int64_t)n > p.cap || n > p.max_kv_len;
+
+  // set by a consumer warp whose wait ran out; read by all consumers after the merge barrier
+  __shared__ volatile int merge_abort;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumers);
+    }
+    merge_abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  int npre = 0;  // tiles the copy warp issues before the wait
+  if (!bad_len && split * p.chunk < n && !p.table && !stall) {
+    const int t0p = split * p.chunk;
+    const int ntp = (min(n, t0p + p.chunk) - t0p + kTileTok - 1) / kTileTok;
+    npre = min(min(S::kStages, ntp), (n - 1 - t0p) / kTileTok);
+    if (warp == kConsumers && lane == 0 && npre > 0) {
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+      if constexpr (kMx) {
+        prefetch_tensormap(&tmKS);
+        prefetch_tensormap(&tmVS);
+      }
+      const uint64_t pol = l2_policy_evict_first();
+      const int row0p = (int)((int64_t)bg * p.cap + t0p);
+      for (int i = 0; i < npre; ++i)
+        issue_tile<D, kMx>(ring, i, row0p + i * kTileTok, &full[i], &tmK, &tmV, &tmKS, &tmVS, pol);
+    }
+  }
+  pdl_wait();
+  MXG_TL_WAITED();
+  pdl_trigger();
+  if (bad_len) {  // (nothing was issued before the wait)
     if (split == 0 && g == 0 && threadIdx.x == 0) set_error(p.err, MXG_EDEVICE);
     // several splits: weight zero for every split of the sequence, so the combine writes zeros
     if (p.max_splits > 1 && threadIdx.x < p.group)
@@ -542,17 +576,6 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
   const int ntiles = (t1 - t0 + kTileTok - 1) / kTileTok;
   const int row0 = (int)((int64_t)bg * p.cap + t0);  // host guarantees bs*Hkv*cap < 2^31 (contiguous)
 
-  // set by a consumer warp whose wait ran out; read by all consumers after the merge barrier
-  __shared__ volatile int merge_abort;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S::kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumers);
-    }
-    merge_abort = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
 
   if (warp == kConsumers) {
     // ------------------------------------------------------------- producer
@@ -584,7 +607,7 @@ __global__ void __launch_bounds__(kThreads) gqa_split_kernel(const __grid_consta
       }
       const uint64_t pol = l2_policy_evict_first();
       const int nissue = stall ? 0 : ntiles;
-      for (int i = 0; i < nissue; ++i) {
+      for (int i = npre; i < nissue; ++i) {  // npre = 0 when the hook stalls the loads
         const int s = i % S::kStages;
         if (i >= S::kStages && !mbar_wait(&empty[s], ((i / S::kStages) - 1) & 1, p.err)) break;
         issue_tile<D, kMx>(ring, s, p.table ? tile_row[i] : row0 + i * kTileTok, &full[s], &tmK, &tmV, &tmKS, &tmVS,

@@ -861,7 +861,8 @@ __global__ void __launch_bounds__(256) kv_append_extend_kernel(uint16_t* __restr
                                                                int64_t cap, int64_t total_q, int max_q_len,
                                                                int32_t* err, KvPages pg) {
   pdl_wait();
-  pdl_trigger();
+  // no early trigger: decode attention reads the cache rows below kv_len - 1 before its own
+  // wait, and these rows are among them, so the successor starts only once this one completes
   const int b = blockIdx.y;
   const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;

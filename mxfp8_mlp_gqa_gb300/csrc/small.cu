@@ -35,7 +35,8 @@ __global__ void __launch_bounds__(256) copy16_kernel(uint4* __restrict__ dst, co
   MXG_TL_SCOPE(kTlCopy16);
   pdl_wait();
   MXG_TL_WAITED();
-  pdl_trigger();
+  // no early trigger: the bytes may be kv_len or K/V cache rows that the next kernel (decode
+  // attention) reads before its own wait, so the successor starts only once this one completes
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x)
     dst[i] = src[i];
 }

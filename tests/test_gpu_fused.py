@@ -1,8 +1,9 @@
 """The fused entry points of the decoder-layer step against the unfused calls they replace:
 gqa_decode_attn_mxfp8 == gqa_decode_attn + mxfp8_quantize (bit-exact), and
 mxfp8_gemm_qkv_kv_append == mxfp8_gemm + kv_append (bit-exact), including the error path
-of an out-of-range kv_len; and the programmatic-dependent-launch chain of a weight quantiser
-followed by a GEMM that reads the weight."""
+of an out-of-range kv_len; and programmatic-dependent-launch chains: a weight quantiser
+followed by a GEMM that reads the weight, and a KV append, an extend append or a kv_len copy
+followed by decode attention (which reads kv_len and the prefix before its own wait)."""
 import math
 
 import numpy as np
@@ -11,7 +12,7 @@ import torch
 
 from mxfp8_mlp_gqa_gb300 import api, synth
 from oracle import mx, ops
-from tests.gpu_util import assert_float_close, dev, dev_bf16, host_f64
+from tests.gpu_util import assert_attn_close, assert_float_close, dev, dev_bf16, host_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -86,3 +87,113 @@ def test_back_to_back_weight_quantise_then_gemm():
         api.mxfp8_gemm(xq, xs, wq, ws, c=c)
         torch.cuda.synchronize()
         assert_float_close(host_f64(c), ref)
+
+
+# --- decode attention reads kv_len and the prefix below row kv_len - 1 before its wait ---
+
+def _attn_ref(q, kp, vp, scale):
+    return ops.gqa_decode_attention(mx.bf16_to_f64(q), [mx.bf16_to_f64(k) for k in kp],
+                                    [mx.bf16_to_f64(v) for v in vp], scale)
+
+
+def _cache(kp, bs, Hkv, cap, D, old=None):
+    """Host bf16 bits [bs, Hkv, cap, D]: the prefixes, zeros past them; rows old[b] (a slice
+    of positions) replaced by other values (what the cache held before the append)."""
+    c = np.zeros((bs, Hkv, cap, D), np.uint16)
+    for b in range(bs):
+        c[b, :, :kp[b].shape[1]] = kp[b]
+        if old is not None:
+            sl = old[b]
+            c[b, :, sl] = synth.normal_bf16((Hkv, sl.stop - sl.start, D), 4.0, b, synth.TID["v"])
+    return c
+
+
+def test_back_to_back_append_then_decode_attention():
+    """kv_append (row kv_len - 1) and gqa_decode_attn enqueued with nothing in between: the
+    attention issues its tiles below row kv_len - 1 while the append may still run, and the
+    appended row only after it. That row first holds other values, so an early read shows."""
+    bs, Hq, Hkv, D, cap, scale = 8, 32, 8, 128, 2048, 1 / math.sqrt(128)
+    lens = synth.kv_lens(bs, 130, cap, seed=11)
+    q = synth.normal_bf16((bs, Hq, D), 1.0, 11, synth.TID["q"])
+    kp = synth.kv_prefix(bs, Hkv, D, lens, 11, synth.TID["k"])
+    vp = synth.kv_prefix(bs, Hkv, D, lens, 11, synth.TID["v"])
+    old = [slice(int(n) - 1, int(n)) for n in lens]
+    k0, v0 = _cache(kp, bs, Hkv, cap, D, old), _cache(vp, bs, Hkv, cap, D, old)
+    kn = dev_bf16(np.stack([k[:, -1] for k in kp]))  # [bs, Hkv, D]
+    vn = dev_bf16(np.stack([v[:, -1] for v in vp]))
+    K = torch.empty((bs, Hkv, cap, D), dtype=torch.bfloat16, device="cuda")
+    V = torch.empty_like(K)
+    qd, kl = dev_bf16(q), dev(lens)
+    out = torch.empty((bs, Hq, D), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(max(1, api.gqa_decode_attn_workspace(bs, Hq, Hkv, D, cap)), dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref = _attn_ref(q, kp, vp, scale)
+    for _ in range(3):
+        K.copy_(dev_bf16(k0))
+        V.copy_(dev_bf16(v0))
+        torch.cuda.synchronize()
+        api.kv_append(K, V, kn, vn, kl, err=err)
+        api.gqa_decode_attn(qd, K, V, kl, cap, scale, out=out, err=err, workspace=ws)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert_attn_close(host_f64(out), ref)
+
+
+def test_back_to_back_extend_append_then_decode_attention():
+    """kv_append_extend writes the last T rows of each prefix and lets its successor start
+    only when it completes: decode attention enqueued right after it sees all T new rows
+    (they first hold other values)."""
+    bs, Hq, Hkv, D, cap, scale = 8, 32, 8, 128, 2048, 1 / math.sqrt(128)
+    lens = synth.kv_lens(bs, 300, cap, seed=12)
+    T = np.array([1, 64, 100, 200, 257, 33, 150, 299], np.int32)
+    q = synth.normal_bf16((bs, Hq, D), 1.0, 12, synth.TID["q"])
+    kp = synth.kv_prefix(bs, Hkv, D, lens, 12, synth.TID["k"])
+    vp = synth.kv_prefix(bs, Hkv, D, lens, 12, synth.TID["v"])
+    old = [slice(int(n) - int(t), int(n)) for n, t in zip(lens, T)]
+    k0, v0 = _cache(kp, bs, Hkv, cap, D, old), _cache(vp, bs, Hkv, cap, D, old)
+    kn = dev_bf16(np.concatenate([k[:, -int(t):].transpose(1, 0, 2) for k, t in zip(kp, T)]))  # [total, Hkv, D]
+    vn = dev_bf16(np.concatenate([v[:, -int(t):].transpose(1, 0, 2) for v, t in zip(vp, T)]))
+    q_start = dev(np.concatenate([[0], np.cumsum(T)]).astype(np.int32))
+    K = torch.empty((bs, Hkv, cap, D), dtype=torch.bfloat16, device="cuda")
+    V = torch.empty_like(K)
+    qd, kl = dev_bf16(q), dev(lens)
+    out = torch.empty((bs, Hq, D), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(max(1, api.gqa_decode_attn_workspace(bs, Hq, Hkv, D, cap)), dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref = _attn_ref(q, kp, vp, scale)
+    for _ in range(3):
+        K.copy_(dev_bf16(k0))
+        V.copy_(dev_bf16(v0))
+        torch.cuda.synchronize()
+        api.kv_append_extend(K, V, kn, vn, q_start, kl, int(T.max()), err=err)
+        api.gqa_decode_attn(qd, K, V, kl, cap, scale, out=out, err=err, workspace=ws)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert_attn_close(host_f64(out), ref)
+
+
+def test_back_to_back_kv_len_copy_then_decode_attention():
+    """copy_bytes writing kv_len from pinned host memory, then decode attention with nothing in
+    between: the attention reads kv_len before its own wait, which is safe because the copy
+    lets its successor start only when it completes (kv_len first holds other lengths)."""
+    bs, Hq, Hkv, D, cap, scale = 8, 32, 8, 128, 2048, 1 / math.sqrt(128)
+    lens = synth.kv_lens(bs, 200, cap, seed=13)
+    q = synth.normal_bf16((bs, Hq, D), 1.0, 13, synth.TID["q"])
+    kp = synth.kv_prefix(bs, Hkv, D, lens, 13, synth.TID["k"])
+    vp = synth.kv_prefix(bs, Hkv, D, lens, 13, synth.TID["v"])
+    K, V = dev_bf16(_cache(kp, bs, Hkv, cap, D)), dev_bf16(_cache(vp, bs, Hkv, cap, D))
+    kl = torch.empty(bs, dtype=torch.int32, device="cuda")
+    host = torch.from_numpy(lens.copy()).pin_memory()
+    qd = dev_bf16(q)
+    out = torch.empty((bs, Hq, D), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(max(1, api.gqa_decode_attn_workspace(bs, Hq, Hkv, D, cap)), dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref = _attn_ref(q, kp, vp, scale)
+    for _ in range(3):
+        kl.copy_(dev(lens // 2))
+        torch.cuda.synchronize()
+        api.copy_bytes(kl, host)
+        api.gqa_decode_attn(qd, K, V, kl, cap, scale, out=out, err=err, workspace=ws)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert_attn_close(host_f64(out), ref)
