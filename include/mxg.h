@@ -34,14 +34,15 @@
  *     weights at setup). Every kernel of the library lets its successor start only after
  *     its own predecessor has completed, so at most two library kernels of a stream are in
  *     flight at once and everything before the immediately preceding kernel is complete.
- *     The decode attention calls (gqa_decode_attn*, contiguous caches) likewise read kv_len
- *     and the K/V cache rows below kv_len - 1 of each sequence before the previous kernel has
- *     finished: that kernel may write row kv_len - 1 (the step's KV append: kv_append*,
- *     mxfp8_gemm_qkv_kv_append) but no other row of the prefix and not kv_len. The library's
- *     kernels that write other cache rows or arbitrary bytes (kv_append_extend*, copy_bytes)
- *     let their successor start only after they complete. Paged caches are read only after
- *     the previous kernel completes. Other activations and outputs are touched only after the
- *     previous kernel completes. Environment variable MXG_PDL=0 turns the chaining off.
+ *     The decode attention calls (gqa_decode_attn*) likewise read kv_len, and over a
+ *     contiguous cache the K/V rows (codes and scales) below kv_len - 1 of each sequence,
+ *     before the previous kernel has finished: that kernel may write row kv_len - 1 (the
+ *     step's KV append: kv_append*, mxfp8_gemm_qkv_kv_append) but no other row of the prefix
+ *     and not kv_len. The library's kernels that write other cache rows or arbitrary bytes
+ *     (kv_append_extend*, copy_bytes) let their successor start only after they complete.
+ *     Paged cache rows and the page table are read only after the previous kernel completes,
+ *     as are all other activations and outputs. Environment variable MXG_PDL=0 turns the
+ *     chaining off.
  */
 #ifndef MXG_H
 #define MXG_H
