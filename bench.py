@@ -181,11 +181,11 @@ class ClockSampler:
 
 
 # DRAM traffic of the attention split kernel per algorithmic byte, from one ncu capture of the
-# same kernel on a smaller cache (the bs-64, 4096-position capture: 634.74 MB of
+# same kernel on a smaller cache (the bs-64, 4096-position capture: 634.68 MB of
 # dram__bytes_read.sum + dram__bytes_write.sum for 622.54 MB of algorithmic bytes). Traffic
 # grows in proportion to the prefix tokens read, so it is scaled to the step's launch. Set to
 # None whenever the kernel changes until it is captured again.
-ATTN_TRAFFIC_PER_ALG_BYTE = 634.738176e6 / 622538752
+ATTN_TRAFFIC_PER_ALG_BYTE = 634.677248e6 / 622538752
 
 
 # --------------------------------------------------------------------------- measured peaks
