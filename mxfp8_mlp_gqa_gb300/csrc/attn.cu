@@ -40,7 +40,6 @@ constexpr int kThreads = (kConsumers + 1) * 32;
 // plus their UE8M0 scales [64, D/32]); otherwise bf16 [64, D] per tile.
 template <int D, bool kMx>
 struct AttnShape {
-  static constexpr int kHalves = D / 64;                               // 128-byte TMA boxes per bf16 row
   static constexpr int kTileBytes = kTileTok * D * (kMx ? 1 : 2);      // one K (or V) tile
   static constexpr int kScaleTileBytes = kMx ? kTileTok * D / 32 : 0;  // its scale bytes
   static constexpr int kCodeStageBytes = 2 * kTileBytes;
@@ -232,7 +231,7 @@ __device__ __forceinline__ void issue_tile(uint8_t* ring, int s, int row, uint64
     tma_load_2d_hint(kst + S::kScaleTileBytes, tmVS, full_s, 0, line, pol);
   } else {
 #pragma unroll
-    for (int h = 0; h < S::kHalves; ++h) {
+    for (int h = 0; h < D / 64; ++h) {  // 128-byte boxes (64 bf16) across the row
       tma_load_2d_hint(kt + h * kTileTok * 128, tmK, full_s, h * 64, row, pol);
       tma_load_2d_hint(vt + h * kTileTok * 128, tmV, full_s, h * 64, row, pol);
     }
