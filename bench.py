@@ -694,14 +694,27 @@ def paged_attn_sweep(dev, rn, flush, bs=BS, page_sizes=(64, 128, 256)):
     return res
 
 
+def fp8_peak_tflops():
+    """Dense fp8 tensor peak used for config-5 fractions: the measured bf16 burst of
+    MEASURED_PEAKS.json times the nominal fp8/bf16 ratio 2 (no fp8 figure is measured there)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return 2.0 * float(json.load(f)["bf16_tflops"]), "2 x measured bf16 burst"
+    return 2.0 * 1900.0, "2 x fallback bf16"
+
+
 def gemm_square_sweep(dev, sizes=(1024, 2048, 4096, 8192, 16384)):
     """Config-5 sweep: C = A' B'^T, A and B MXFP8 [N, N], bf16 C; TFLOP/s of 2 N^3 per call,
-    median of 5 timed calls after 2 warm-up calls. Alongside, cuBLAS's MXFP8 GEMM through
-    torch._scaled_mm with UE8M0 block scales where this torch build supports it (context:
-    a library kernel's practical peak on this part)."""
+    median of 5 timed calls after 2 warm-up calls, as a fraction of the fp8 peak
+    (fp8_peak_tflops). Alongside, cuBLAS's MXFP8 GEMM through torch._scaled_mm with UE8M0 block
+    scales where this torch build supports it -- a library kernel's practical peak on this part,
+    a measured lower bound of the fp8 peak -- and this kernel's ratio to it."""
     import torch
 
     from mxfp8_mlp_gqa_gb300 import api
+
+    peak, peak_src = fp8_peak_tflops()
 
     g = torch.Generator(device=dev)
     g.manual_seed(5)
@@ -729,7 +742,9 @@ def gemm_square_sweep(dev, sizes=(1024, 2048, 4096, 8192, 16384)):
         c = torch.empty((n, n), dtype=torch.bfloat16, device=dev)
         ws = torch.zeros(max(1, api.mxfp8_gemm_workspace(n, n, n)), dtype=torch.uint8, device=dev)
         ms = timeit(lambda: api.mxfp8_gemm(aq, as_, bq, bs_, c=c, workspace=ws))
-        ent = {"us": round(ms * 1e3, 1), "TFLOP_s": round(2 * n ** 3 / (ms * 1e-3) / 1e12, 1)}
+        tf = 2 * n ** 3 / (ms * 1e-3) / 1e12
+        ent = {"us": round(ms * 1e3, 1), "TFLOP_s": round(tf, 1), "frac_of_fp8_peak": round(tf / peak, 3),
+               "fp8_peak_TFLOP_s": round(peak, 1), "fp8_peak_source": peak_src}
         try:
             fa = aq.view(torch.float8_e4m3fn)
             fb = bq.view(torch.float8_e4m3fn)
@@ -738,6 +753,7 @@ def gemm_square_sweep(dev, sizes=(1024, 2048, 4096, 8192, 16384)):
             sb = sa.clone()
             ms2 = timeit(lambda: torch._scaled_mm(fa, fb.t(), sa, sb, out_dtype=torch.bfloat16))
             ent["cublas_mxfp8_TFLOP_s"] = round(2 * n ** 3 / (ms2 * 1e-3) / 1e12, 1)
+            ent["of_cublas_mxfp8"] = round(ms2 / ms, 3)
         except Exception as ex:  # noqa: BLE001 - context only
             ent["cublas_mxfp8"] = f"unavailable: {type(ex).__name__}"
         out[str(n)] = ent
