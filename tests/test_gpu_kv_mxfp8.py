@@ -230,3 +230,32 @@ def test_paged_bad_page_id_sets_the_flag_other_sequences_intact():
     assert int(err.item()) == 7
     assert np.isfinite(host_f64(out)).all()
     assert_attn_close(host_f64(out)[:1], _oracle(q[:1], kp[:1], vp[:1], 0.1))
+
+
+def test_back_to_back_append_then_attention():
+    """kv_append_mxfp8 (row kv_len - 1) and gqa_decode_attn_kv_mxfp8 enqueued with nothing in
+    between: the attention issues its tiles (codes and scales) below row kv_len - 1 while the
+    append may still run, the appended row only after it. That row first holds other codes
+    (and the 0xFF scale), so a read that came too early would show."""
+    bs, Hq, Hkv, D, cap, scale = 8, 32, 8, 128, 2048, 1 / math.sqrt(128)
+    lens = synth.kv_lens(bs, 130, cap, seed=14)
+    q, kp, vp = _case(bs, Hq, Hkv, D, lens, 14)
+    kc, ks = _mx_cache([k[:, :-1] for k in kp], cap)  # the prefixes without their last row
+    vc, vs = _mx_cache([v[:, :-1] for v in vp], cap)
+    k0, s0, v0, t0 = kc.clone(), ks.clone(), vc.clone(), vs.clone()
+    kn = dev_bf16(np.stack([k[:, -1] for k in kp]))  # [bs, Hkv, D]
+    vn = dev_bf16(np.stack([v[:, -1] for v in vp]))
+    qd, kl = dev_bf16(q), dev(lens)
+    out = torch.empty((bs, Hq, D), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(max(1, api.gqa_decode_attn_workspace(bs, Hq, Hkv, D, cap)), dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref = _oracle(q, kp, vp, scale)
+    for _ in range(3):
+        for dst, src in ((kc, k0), (ks, s0), (vc, v0), (vs, t0)):
+            dst.copy_(src)
+        torch.cuda.synchronize()
+        api.kv_append_mxfp8(kc, ks, vc, vs, kn, vn, kl, err=err)
+        api.gqa_decode_attn_kv_mxfp8(qd, kc, ks, vc, vs, kl, cap, scale, out=out, err=err, workspace=ws)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert_attn_close(host_f64(out), ref)
